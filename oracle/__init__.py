@@ -1,0 +1,382 @@
+"""CPU oracle of the MoE-layer hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+import this package.  The product path (the CUDA library and its Python
+binding) never imports or calls it, and the two share no code: only the
+seeded input generators in `workloads` feed both.
+
+Each function is the plain definition of one step, written for a reader to
+check against the pages by eye: fp64 arithmetic, library primitives
+(sort, matmul, exp) as steps, no blocking or fusion.
+
+Sources (page title, section):
+  [MoE14]  "14. Serving Mixture-of-Experts Models" -- "Follow one token
+           through an MoE layer" (router, the four runtime steps), "Price
+           one dispatch", "The slowest expert sets the pace" (balancedness),
+           "Worked example: balance the busiest rank",
+           "The network topology is visible in every MoE layer" (replica
+           preference).
+  [MoEInf] "Mixture-of-Experts Inference: parallelism, communication, and
+           load balancing" -- "MoE architecture recap" (grouped routing,
+           shared experts), "Optimized kernels for MoE" (grouped GEMM,
+           contiguous layout).
+  [Zepp]   "Zepp: Accelerating Distributed MoE Serving under Relaxed Balance
+           Constraints" -- Section 2 (top-k router, dispatch/combine),
+           Section 4.1 (replicas, placement).
+
+Readings where the pages are silent (each also listed in the design notes):
+  * top-k order: descending score, ties to the lower expert id; selection
+    compares the fp32 logits (softmax and sigmoid are monotone).
+  * softmax weights are renormalised over the selected k.
+  * group-limited routing: contiguous groups of E/n_groups experts; group
+    score = fp64 sum of the fp64 sigmoids of the group's top-`group_topn`
+    logits (taken in descending order); top `topk_groups` groups by
+    (score desc, group id asc); weights = selected sigmoids / their sum.
+  * expert FFN = SwiGLU: h = bf16(silu(x Wg^T) * (x Wu^T)), y = bf16(h Wd^T),
+    silu(g) = g / (1 + e^-g); fp64 here.
+  * combine: y[t] = bf16(shared[t] + sum_j w[t,j] * y_perm[dest_row[t,j]]).
+  * balancedness: total / (R * max) in fp64, and 1.0 when nothing is routed.
+
+Pins for every function live in tests/test_oracle_pins.py (brute force,
+closed forms, the pages' worked examples); none is "parity unpinned".
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Dict, Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+# ------------------------------------------------------------------ bf16
+def bf16_round(x) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 (8 significant bits), ties to
+    even, returning fp64.  Done in one step from fp64 so there is no double
+    rounding through fp32.  (Finite inputs; magnitudes in the normal bf16
+    range.)"""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                      # x = m * 2**e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """uint16 bf16 bit patterns -> fp64 values (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """fp64 values that are already bf16-representable -> uint16 patterns."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+# ------------------------------------------------------------------ route
+def _order_desc_lower_id(scores_row: np.ndarray) -> np.ndarray:
+    """Indices sorted by (score descending, index ascending)."""
+    idx = np.arange(scores_row.shape[0])
+    return np.lexsort((idx, -scores_row.astype(np.float64)))
+
+
+def route_softmax_topk(logits: np.ndarray, k: int):
+    """Softmax router with top-k ([MoE14] "Follow one token through an MoE
+    layer": expert ids and weights per token; [Zepp] Section 2: a learned
+    router selects the top-k experts).
+
+    Returns (ids int32 [T,k], weights fp64 [T,k]).  The probabilities of the
+    full softmax are renormalised over the k selected experts.
+    """
+    logits = np.asarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    for t in range(T):
+        row = logits[t]
+        order = _order_desc_lower_id(row)[:k]
+        l64 = row.astype(np.float64)
+        p = np.exp(l64 - l64.max())
+        p = p / p.sum()
+        ids[t] = order
+        w[t] = p[order] / p[order].sum()
+    return ids, w
+
+
+def sigmoid64(x) -> np.ndarray:
+    return 1.0 / (1.0 + np.exp(-np.asarray(x, dtype=np.float64)))
+
+
+def route_group_limited(logits: np.ndarray, k: int, n_groups: int,
+                        topk_groups: int, group_topn: int):
+    """Group-limited sigmoid router ([MoEInf] "MoE architecture recap": the
+    routed experts are divided into groups; the router first picks a limited
+    number of groups, then the top experts within them).
+
+    Returns (ids int32 [T,k], weights fp64 [T,k], min relative group-score
+    margin between the last kept and the first dropped group over all
+    tokens, for near-tie reporting).
+    """
+    logits = np.asarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    gs = E // n_groups
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    min_margin = np.inf
+    for t in range(T):
+        row = logits[t]
+        gscore = np.empty(n_groups, dtype=np.float64)
+        for g in range(n_groups):
+            members = row[g * gs:(g + 1) * gs]
+            top = _order_desc_lower_id(members)[:group_topn]
+            s = 0.0
+            for i in top:                       # descending order
+                s = s + float(sigmoid64(members[i]))
+            gscore[g] = s
+        gorder = _order_desc_lower_id(gscore)
+        kept = np.sort(gorder[:topk_groups])
+        if topk_groups < n_groups:
+            a, b = gscore[gorder[topk_groups - 1]], gscore[gorder[topk_groups]]
+            min_margin = min(min_margin, (a - b) / max(abs(a), 1e-300))
+        cand = np.concatenate([np.arange(g * gs, (g + 1) * gs) for g in kept])
+        sub = _order_desc_lower_id(row[cand])[:k]
+        chosen = cand[sub]
+        s = sigmoid64(row[chosen])
+        ids[t] = chosen
+        w[t] = s / s.sum()
+    return ids, w, min_margin
+
+
+# ------------------------------------------------------------------ layout
+def choose_slot(e: int, t: int, pl) -> int:
+    """Physical slot that serves assignment (token t, expert e).
+
+    One copy: its slot.  Several copies: the copy on token t's own node
+    (the lowest such rank), else copy number (t mod n_copies) in ascending
+    rank order.  This is the fixed replica rule of the replica workload;
+    its preference order (same node first, else spread) follows [MoE14]
+    "The network topology is visible in every MoE layer".
+    """
+    lo, hi = int(pl.rep_offsets[e]), int(pl.rep_offsets[e + 1])
+    reps = [int(s) for s in pl.rep_slots[lo:hi]]
+    if len(reps) == 1:
+        return reps[0]
+    src = int(pl.token_src_rank[t]) if pl.token_src_rank is not None else t % pl.n_ranks
+    node = src // pl.ranks_per_node
+    for s in reps:                                   # ascending rank
+        if int(pl.slot_rank[s]) // pl.ranks_per_node == node:
+            return s
+    return reps[t % len(reps)]
+
+
+def dispatch_layout(topk_ids: np.ndarray, pl) -> Dict[str, np.ndarray]:
+    """Dispatch packing ([MoE14] "Follow one token", step 1: a permutation
+    built from a histogram over the expert ids so that kernels see
+    contiguous per-expert segments; here one segment per physical slot,
+    ordered by (rank, expert), so each simulated rank's rows are contiguous
+    as they would be after step 2's send to the owner rank).
+
+    Assignment a = t*k + j.  Rows of a segment keep assignment order
+    (stable).  Written as the literal definition: walk the assignments in
+    order, append each to its slot's list, concatenate the lists.
+    """
+    T, k = topk_ids.shape
+    S = pl.n_slots
+    A = T * k
+    slot = np.empty(A, dtype=np.int32)
+    lists = [[] for _ in range(S)]
+    for a in range(A):
+        t = a // k
+        s = choose_slot(int(topk_ids[t, a % k]), t, pl)
+        slot[a] = s
+        lists[s].append(a)
+    seg_counts = np.array([len(l) for l in lists], dtype=np.int32)
+    seg_offsets = np.zeros(S + 1, dtype=np.int32)
+    seg_offsets[1:] = np.cumsum(seg_counts)
+    src_assign = np.array([a for l in lists for a in l], dtype=np.int32)
+    dest_row = np.empty(A, dtype=np.int32)
+    dest_row[src_assign] = np.arange(A, dtype=np.int32)
+    rank_counts = np.zeros(pl.n_ranks, dtype=np.int32)
+    for s in range(S):
+        rank_counts[int(pl.slot_rank[s])] += seg_counts[s]
+    return dict(slot=slot, seg_counts=seg_counts, seg_offsets=seg_offsets,
+                dest_row=dest_row, src_assign=src_assign, rank_counts=rank_counts)
+
+
+# ------------------------------------------------------------------ permute
+def permute(x: np.ndarray, dest_row: np.ndarray, k: int) -> np.ndarray:
+    """x_perm[dest_row[t*k+j]] = x[t] ([MoE14] "Price one dispatch": every
+    assignment carries one copy of its token's hidden row).  Works on any
+    dtype, so bf16 bit patterns are moved unchanged."""
+    T = x.shape[0]
+    out = np.empty((T * k,) + x.shape[1:], dtype=x.dtype)
+    for a in range(T * k):
+        out[dest_row[a]] = x[a // k]
+    return out
+
+
+# ------------------------------------------------------------------ expert FFN
+def silu64(g: np.ndarray) -> np.ndarray:
+    return g / (1.0 + np.exp(-g))
+
+
+def swiglu_expert(x_rows: np.ndarray, w_gate_up_e: np.ndarray,
+                  w_down_e: np.ndarray, I: int):
+    """One expert's gated MLP on a block of rows, fp64 from bf16 values.
+
+    x_rows [n,H], w_gate_up_e [2I,H] (gate rows then up rows), w_down_e [H,I],
+    all fp64 holding bf16 values.  Returns (h, y) with h rounded to bf16
+    before the down projection and y rounded to bf16.
+    """
+    g = x_rows @ w_gate_up_e[:I].T
+    u = x_rows @ w_gate_up_e[I:].T
+    h = bf16_round(silu64(g) * u)
+    y = bf16_round(h @ w_down_e.T)
+    return h, y
+
+
+def grouped_ffn(x_perm: np.ndarray, seg_offsets: np.ndarray, seg_expert: np.ndarray,
+                w_gate_up: np.ndarray, w_down: np.ndarray, I: int,
+                rows: Optional[np.ndarray] = None):
+    """Grouped expert FFN ([MoE14] "Follow one token", step 3: one kernel
+    runs every expert's segment as a matrix with its own row count;
+    [MoEInf] "Optimized kernels for MoE": grouped GEMM, contiguous layout).
+
+    Segment s covers rows [seg_offsets[s], seg_offsets[s+1]) and uses expert
+    seg_expert[s].  Inputs are fp64 arrays of bf16 values; w_gate_up may be
+    indexed lazily (any object with __getitem__ returning [2I,H]).
+    rows: optional sorted subset of row indices to evaluate.  Returns
+    (h [n,I], y [n,H]) for all rows or for `rows` in that order.
+    """
+    n_rows = x_perm.shape[0] if rows is None else len(rows)
+    H = x_perm.shape[1]
+    want = np.arange(x_perm.shape[0]) if rows is None else np.asarray(rows)
+    h_out = np.zeros((n_rows, I))
+    y_out = np.zeros((n_rows, H))
+    seg_of = np.searchsorted(np.asarray(seg_offsets), want, side="right") - 1
+    for s in np.unique(seg_of):
+        sel = np.nonzero(seg_of == s)[0]
+        e = int(seg_expert[s])
+        h, y = swiglu_expert(x_perm[want[sel]], np.asarray(w_gate_up[e], np.float64),
+                             np.asarray(w_down[e], np.float64), I)
+        h_out[sel] = h
+        y_out[sel] = y
+    return h_out, y_out
+
+
+# ------------------------------------------------------------------ combine
+def combine_f64(y_perm: np.ndarray, dest_row: np.ndarray, topk_w: np.ndarray,
+                shared: Optional[np.ndarray] = None, tokens=None) -> np.ndarray:
+    """Inverse permutation followed by the router-weighted sum ([MoE14]
+    "Follow one token", step 4; [Zepp] Section 2: outputs aggregated at each
+    token's source), plus the shared expert's output with weight one
+    ([MoEInf] "MoE architecture recap": shared experts see every token).
+    fp64 accumulation, bf16 result.  tokens: optional subset."""
+    T, k = topk_w.shape
+    ts = np.arange(T) if tokens is None else np.asarray(tokens)
+    out = np.zeros((len(ts), y_perm.shape[1]))
+    for i, t in enumerate(ts):
+        acc = np.zeros(y_perm.shape[1]) if shared is None else shared[t].astype(np.float64)
+        for j in range(k):
+            acc = acc + float(topk_w[t, j]) * y_perm[dest_row[t * k + j]]
+        out[i] = bf16_round(acc)
+    return out
+
+
+_fma_lib = None
+
+
+def build_c(force: bool = False) -> str:
+    """Compile the oracle's C part (gcc, no CUDA) next to its source."""
+    src = os.path.join(_HERE, "fma_combine.c")
+    so = os.path.join(_HERE, "liboracle_fma.so")
+    if force or not os.path.exists(so) or os.path.getmtime(so) < os.path.getmtime(src):
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                               "-ffp-contract=off", "-o", so, src, "-lm"])
+    return so
+
+
+def _fma():
+    global _fma_lib
+    if _fma_lib is None:
+        lib = ctypes.CDLL(build_c())
+        lib.oracle_combine_fma32.restype = None
+        lib.oracle_combine_fma32.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+        _fma_lib = lib
+    return _fma_lib
+
+
+def combine_fma32(y_perm_bits: np.ndarray, dest_row: np.ndarray, topk_w32: np.ndarray,
+                  shared_bits: Optional[np.ndarray] = None) -> np.ndarray:
+    """The combine with its fp32 evaluation order written out: per element,
+    acc = shared (or 0); for j = 0..k-1: acc = fmaf(w[t,j], y, acc); result
+    bf16 (nearest, ties to even).  Inputs/outputs are bf16 bit patterns
+    (uint16).  This fixes one valid rounding order so that a stage fed the
+    same y_perm can be compared bit for bit."""
+    T, k = topk_w32.shape
+    H = y_perm_bits.shape[1]
+    yp = np.ascontiguousarray(y_perm_bits, dtype=np.uint16)
+    dr = np.ascontiguousarray(dest_row, dtype=np.int32)
+    w = np.ascontiguousarray(topk_w32, dtype=np.float32)
+    sh = None if shared_bits is None else np.ascontiguousarray(shared_bits, dtype=np.uint16)
+    out = np.empty((T, H), dtype=np.uint16)
+    _fma().oracle_combine_fma32(yp.ctypes.data, dr.ctypes.data, w.ctypes.data,
+                                None if sh is None else sh.ctypes.data,
+                                T, k, H, out.ctypes.data)
+    return out
+
+
+# ------------------------------------------------------------------ balance
+def balance_stats(rank_counts: np.ndarray):
+    """Balancedness = mean per-rank load / busiest rank's load ([MoE14] "The
+    slowest expert sets the pace": avg_tokens / max_tokens, 1.0 when
+    perfectly balanced).  Loads count assignments, not unique tokens
+    ([MoE14] "Price one dispatch").  Returns (balancedness, max, total)."""
+    rc = np.asarray(rank_counts, dtype=np.int64)
+    total = int(rc.sum())
+    mx = int(rc.max()) if rc.size else 0
+    if total == 0:
+        return 1.0, mx, total
+    return float(total) / (float(len(rc)) * float(mx)), mx, total
+
+
+# ------------------------------------------------------------------ layer
+def moe_layer_tokens(tokens, logits, x_bits, w_gate_up, w_down, pl, route_cfg,
+                     shared_w=None, I=None, shared_I=None):
+    """Whole layer for a subset of tokens, evaluated one token at a time from
+    its definition: route the token, run each selected expert's FFN on its
+    row, add the shared expert, weighted sum.  Replica choice does not change
+    the value (copies hold identical weights), so it is not needed here.
+
+    tokens: token indices; logits fp32 [T,E]; x_bits uint16 [T,H];
+    w_gate_up / w_down: indexable by expert -> bf16 bit arrays;
+    route_cfg: dict(score_fn, k, n_groups, topk_groups, group_topn).
+    Returns y fp64 (bf16 values) [len(tokens), H].
+    """
+    tokens = np.asarray(tokens)
+    lg = np.asarray(logits)[tokens]
+    if route_cfg["score_fn"] == 0:
+        ids, w = route_softmax_topk(lg, route_cfg["k"])
+    else:
+        ids, w, _ = route_group_limited(lg, route_cfg["k"], route_cfg["n_groups"],
+                                        route_cfg["topk_groups"], route_cfg["group_topn"])
+    w32 = w.astype(np.float32).astype(np.float64)   # the router emits fp32 weights
+    out = np.zeros((len(tokens), x_bits.shape[1]))
+    for i, t in enumerate(tokens):
+        xr = bf16_bits_to_f64(x_bits[t])[None, :]
+        acc = np.zeros(x_bits.shape[1])
+        if shared_w is not None:
+            _, ys = swiglu_expert(xr, bf16_bits_to_f64(shared_w[0]), bf16_bits_to_f64(shared_w[1]),
+                                  shared_I)
+            acc = acc + ys[0]
+        for j in range(ids.shape[1]):
+            e = int(ids[i, j])
+            _, ye = swiglu_expert(xr, bf16_bits_to_f64(w_gate_up[e]), bf16_bits_to_f64(w_down[e]), I)
+            acc = acc + w32[i, j] * ye[0]
+        out[i] = bf16_round(acc)
+    return out
