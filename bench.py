@@ -1,0 +1,474 @@
+"""Benchmark of the MoE-layer hot path on GB300.
+
+One step = route -> dispatch layout -> permute -> grouped SwiGLU FFN (+ the
+shared expert where the workload has one) -> combine -> balancedness, over
+one batch of seeded synthetic inputs already resident in HBM.  Default
+workload: the 4,000-token prefill layer (hidden 8192, 64 experts, top-2,
+I=2048, 8 simulated ranks), on which both target fractions of the metric
+(grouped GEMM vs tensor peak, permute/combine vs HBM bandwidth) are quoted.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload on its own GPU (the path needs no exchange on one
+GPU: ranks are simulated inside each replica), so scaling is weak.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; grouped-GEMM % bf16 peak; permute/combine % HBM BW"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                    source="fallback")
+
+
+# ------------------------------------------------------------------ dist
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ algorithmic work
+def algorithmic(w: wl.Workload, seg_counts: np.ndarray, slot_expert: np.ndarray):
+    """Bytes / flops per step by stage (the per-unit figures times the units)."""
+    A, T, H, I = w.A, w.T, w.H, w.I
+    active_slots = seg_counts > 0
+    # weights are read once per active expert slot (replicas re-read: they
+    # are separate copies in a real deployment)
+    n_active = int(active_slots.sum())
+    wbytes = n_active * 6 * H * I
+    st = {
+        "route": dict(bytes=T * w.E * 4 + T * w.k * 8),
+        "layout": dict(bytes=A * 4 * 4 + A * 4),
+        "permute": dict(bytes=T * H * 2 + A * H * 2),
+        "grouped_ffn": dict(bytes=wbytes + A * H * 2 + A * I * 2 * 2 + A * H * 2,
+                            flops=6 * A * H * I, weight_bytes=wbytes),
+        "combine": dict(bytes=A * H * 2 + T * H * 2 + (T * H * 2 if w.shared_I else 0) + A * 8),
+    }
+    if w.shared_I:
+        st["shared_ffn"] = dict(bytes=6 * H * w.shared_I + T * H * 2 * 2 + T * w.shared_I * 4,
+                                flops=6 * T * H * w.shared_I, weight_bytes=6 * H * w.shared_I)
+    return st
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local):
+    from grouped_ffn_gb300 import MoELayer, moe
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = wl.WORKLOADS[args.workload]
+    if args.zipf is not None:
+        w = w.with_zipf(args.zipf)
+    pl = wl.make_placement(w)
+    logits = wl.make_logits(w, dev)
+    x = wl.make_x(w, dev)
+    wgu = wl.make_w_gate_up(w, dev)
+    wd = wl.make_w_down(w, dev)
+    sgu, sd = wl.make_shared_weights(w, dev)
+    layer = MoELayer(H=w.H, I=w.I, E=w.E, k=w.k, placement=moe.DevicePlacement.from_tables(pl, dev),
+                     w_gate_up=wgu, w_down=wd, max_tokens=w.T, score_fn=w.score_fn,
+                     n_groups=w.n_groups, topk_groups=w.topk_groups, group_topn=w.group_topn,
+                     shared_w_gate_up=sgu, shared_w_down=sd, device=dev)
+    y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # per-stage events, recorded on the launching stream
+    names = ["route", "layout", "permute", "grouped_ffn"] + (["shared_ffn"] if w.shared_I else []) \
+        + ["combine", "balance"]
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+
+    def step(i=None):
+        if i is None:
+            layer.forward(logits, x, y, stream)
+            return
+        marks = iter(ev[i][1:])
+        ev[i][0].record(stream)
+        layer.forward(logits, x, y, stream, mark=lambda n: next(marks).record(stream))
+
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            step()
+    stream.synchronize()
+    layer.check(stream)
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)   # let the sampler start
+        start.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                step(i)
+        end.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / K
+    layer.check(stream)
+
+    stage_ms = {n: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)]))
+                for j, n in enumerate(names)}
+
+    # end to end through the public API from pinned host buffers
+    logits_h = logits.cpu().pin_memory()
+    x_h = x.cpu().pin_memory()
+    y_h = torch.empty(w.T, w.H, dtype=torch.bfloat16).pin_memory()
+    logits_d, x_d, y_d = torch.empty_like(logits), torch.empty_like(x), torch.empty_like(y)
+    for _ in range(W):
+        layer.forward_host(logits_h, x_h, y_h, logits_d, x_d, y_d, stream)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        layer.forward_host(logits_h, x_h, y_h, logits_d, x_d, y_d, stream)
+    e1.record(stream)
+    stream.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / K
+    layer.check(stream)
+    assert torch.equal(y_h, y.cpu()), "end-to-end output differs from the device-resident run"
+
+    peaks = load_peaks()
+    seg_counts = layer.seg_counts.cpu().numpy()
+    alg = algorithmic(w, seg_counts, pl.slot_expert)
+    stages = {}
+    for n in names:
+        if n == "balance":
+            stages[n] = {"us": stage_ms[n] * 1e3}
+            continue
+        a = alg[n]
+        s = {"us": stage_ms[n] * 1e3, "gbs": a["bytes"] / (stage_ms[n] * 1e-3) / 1e9}
+        s["hbm_frac"] = s["gbs"] / peaks["hbm_gbs"]
+        if "flops" in a:
+            s["tflops"] = a["flops"] / (stage_ms[n] * 1e-3) / 1e12
+            s["tensor_frac"] = s["tflops"] / peaks["bf16_tflops_sustained"]
+            s["weight_gbs"] = a["weight_bytes"] / (stage_ms[n] * 1e-3) / 1e9
+            bound_ms = max(a["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),
+                           a["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
+            s["roofline_frac"] = bound_ms / stage_ms[n]
+        stages[n] = s
+    g = alg["grouped_ffn"]
+    g_ms = stage_ms["grouped_ffn"]
+    intensity = g["flops"] / g["bytes"]
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if intensity < ridge:
+        roof = {"bound": "hbm", "achieved": g["bytes"] / (g_ms * 1e-3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": g["flops"] / (g_ms * 1e-3) / 1e12,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = "grouped_ffn_kernel (gate/up + down launches)"
+    roof["peak_source"] = peaks["source"] + (" sustained" if roof["bound"] == "tensor" else "")
+    roof["algorithmic_bytes_per_step"] = g["bytes"]
+    roof["algorithmic_flops_per_step"] = g["flops"]
+
+    value = world * w.T / (ms_step * 1e-3)
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.T, "hidden": w.H, "experts": w.E, "top_k": w.k,
+                   "ffn_intermediate": w.I, "shared_intermediate": w.shared_I,
+                   "simulated_ranks": w.R, "zipf_s": w.zipf_s, "assignments": w.A,
+                   "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2: %.2f GB of expert weights stream per step"
+                         % (g["weight_bytes"] / 1e9)},
+        "e2e": {"value": world * w.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": logits.numel() * 4 + x.numel() * 2,
+                "d2h_bytes_per_step": y.numel() * 2},
+        "gpu_launches": layer.launches_per_step * K,
+        "roofline": roof,
+        "stages": stages,
+        "gemm_pct_bf16_peak": 100.0 * stages["grouped_ffn"]["tflops"] / peaks["bf16_tflops"],
+        "permute_pct_hbm": 100.0 * stages["permute"]["hbm_frac"],
+        "combine_pct_hbm": 100.0 * stages["combine"]["hbm_frac"],
+        "balancedness": float(layer.balancedness.item()),
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, pl, logits, x, wgu, wd, sgu, sd, args.cpu_seconds)
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_sample_step(w, pl, logits_np, x_bits, experts_gu, experts_d, shared, tokens):
+    """The oracle's stage-wise path on a sample of tokens: route, layout,
+    permute, grouped FFN, combine, balancedness."""
+    import oracle
+    lg = logits_np[tokens]
+    if w.score_fn == wl.SCORE_SOFTMAX and w.n_groups == 1:
+        ids, wts = oracle.route_softmax_topk(lg, w.k)
+    else:
+        ids, wts, _ = oracle.route_group_limited(lg, w.k, w.n_groups, w.topk_groups, w.group_topn)
+    lay = oracle.dispatch_layout(ids, pl if pl.token_src_rank is None else pl)
+    xs = oracle.bf16_bits_to_f64(x_bits[tokens])
+    xp = oracle.permute(xs, lay["dest_row"], w.k)
+    _, yp = oracle.grouped_ffn(xp, lay["seg_offsets"], pl.slot_expert, experts_gu, experts_d, w.I)
+    sh = None
+    if shared is not None:
+        _, sh = oracle.swiglu_expert(xs, shared[0], shared[1], w.shared_I)
+    y = oracle.combine_f64(yp, lay["dest_row"], wts.astype(np.float32).astype(np.float64), sh)
+    oracle.balance_stats(lay["rank_counts"])
+    return y
+
+
+class _HostExperts:
+    """Expert weights for the oracle: bf16 bits copied to the host once
+    (outside any timer), converted to fp64 on each use (inside it)."""
+
+    def __init__(self, t):
+        self.t, self.cache = t, {}
+
+    def fetch(self, e):
+        if e not in self.cache:
+            self.cache[e] = _bits(self.t[e])
+
+    def __getitem__(self, e):
+        import oracle
+        self.fetch(e)
+        return oracle.bf16_bits_to_f64(self.cache[e])
+
+
+def cpu_baseline(w, pl, logits, x, wgu, wd, sgu, sd, seconds):
+    """Time the oracle, as it stands, on a bounded sample of the workload."""
+    rng = np.random.default_rng(12345)
+    logits_np = logits.cpu().numpy()
+    x_bits = _bits(x)
+    gu, d = _HostExperts(wgu), _HostExperts(wd)
+    shared = None if sgu is None else (
+        __import__("oracle").bf16_bits_to_f64(_bits(sgu[0])),
+        __import__("oracle").bf16_bits_to_f64(_bits(sd[0])))
+    n = 4
+    done_tokens, t_used = 0, 0.0
+    while t_used < seconds and done_tokens < w.T and n <= 256:
+        toks = np.sort(rng.choice(w.T, size=min(n, w.T), replace=False))
+        # host copies of the experts this sample needs are made outside the timer
+        import oracle
+        ids = (oracle.route_softmax_topk(logits_np[toks], w.k)[0]
+               if (w.score_fn == wl.SCORE_SOFTMAX and w.n_groups == 1)
+               else oracle.route_group_limited(logits_np[toks], w.k, w.n_groups,
+                                               w.topk_groups, w.group_topn)[0])
+        for e in np.unique(ids):
+            gu.fetch(int(e))
+            d.fetch(int(e))
+        t0 = time.perf_counter()
+        oracle_sample_step(w, pl, logits_np, x_bits, gu, d, shared, toks)
+        t_used += time.perf_counter() - t0
+        done_tokens += len(toks)
+        n *= 2
+    return {"value": done_tokens / t_used, "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{done_tokens} of {w.T} tokens of the {w.name} layer through the oracle's "
+                      f"stage-wise path (route, layout, permute, grouped FFN, combine, balance) "
+                      f"in {t_used:.1f} s; numpy fp64, BLAS threads = host cores"}
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the CPU oracle, timed per step on a bounded sample."""
+    if rank != 0:
+        return None
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    w = wl.WORKLOADS[args.workload]
+    if args.zipf is not None:
+        w = w.with_zipf(args.zipf)
+    pl = wl.make_placement(w)
+    logits = wl.make_logits(w, dev)
+    x = wl.make_x(w, dev)
+    wgu = wl.make_w_gate_up(w, dev)
+    wd = wl.make_w_down(w, dev)
+    sgu, sd = wl.make_shared_weights(w, dev)
+    import oracle
+    logits_np = logits.cpu().numpy()
+    x_bits = _bits(x)
+    gu, d = _HostExperts(wgu), _HostExperts(wd)
+    shared = None if sgu is None else (oracle.bf16_bits_to_f64(_bits(sgu[0])),
+                                       oracle.bf16_bits_to_f64(_bits(sd[0])))
+    rng = np.random.default_rng(777)
+    n_tok = max(1, min(w.T, args.ref_tokens))
+    samples = [np.sort(rng.choice(w.T, size=n_tok, replace=False))
+               for _ in range(args.warmup + args.steps)]
+    for toks in samples:      # host copies of the needed experts, outside the timer
+        ids = (oracle.route_softmax_topk(logits_np[toks], w.k)[0]
+               if (w.score_fn == wl.SCORE_SOFTMAX and w.n_groups == 1)
+               else oracle.route_group_limited(logits_np[toks], w.k, w.n_groups,
+                                               w.topk_groups, w.group_topn)[0])
+        for e in np.unique(ids):
+            gu.fetch(int(e))
+            d.fetch(int(e))
+    for toks in samples[: args.warmup]:
+        oracle_sample_step(w, pl, logits_np, x_bits, gu, d, shared, toks)
+    t0 = time.perf_counter()
+    for toks in samples[args.warmup:]:
+        oracle_sample_step(w, pl, logits_np, x_bits, gu, d, shared, toks)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n_tok / dt
+    sample = (f"{n_tok} of {w.T} tokens per step of the {w.name} layer through the oracle's "
+              f"stage-wise path; numpy fp64")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": w.T, "hidden": w.H, "experts": w.E,
+                       "top_k": w.k, "ffn_intermediate": w.I, "zipf_s": w.zipf_s,
+                       "parallelism": "replicas1", "sampled_tokens_per_step": n_tok},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--zipf", type=float, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        out = run_reference(args, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+        out = run_ours(args, world, rank, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,586 @@
+// Grouped SwiGLU expert FFN on 5th-generation tensor cores (sm_103a).
+//
+// "14. Serving Mixture-of-Experts Models", "Follow one token through an MoE
+// layer", step 3: one kernel processes every expert's segment as a matrix
+// with its own row count.  "Mixture-of-Experts Inference", "Optimized
+// kernels for MoE": grouped GEMM over a contiguous layout.  The gated MLP
+// (gate, up, activation, down) is SwiGLU: h = silu(x Wg^T) * (x Wu^T),
+// y = h Wd^T.
+//
+// Two launches of one persistent, warp-specialised kernel:
+//   mode 0 (gate/up):  acc[128 x 256] = X[128 x H] * [Wg; Wu]^T tile,
+//                      epilogue h = bf16(silu(acc[:, :128]) * acc[:, 128:])
+//   mode 1 (down):     acc[128 x 256] = h[128 x I] * Wd^T tile, epilogue bf16.
+// A 128-row tile always starts at a segment's first row plus a multiple of
+// 128 and uses that segment's expert; rows past the segment's end are
+// computed from whatever follows (or TMA zero fill) and are never stored.
+//
+// Per CTA (one per SM, 192 threads):
+//   warp 0     TMA producer: A tile 128x64 and two B halves 128x64 per
+//              k-block into a 4-stage ring (48 KiB per stage, 128-byte
+//              swizzle), completion via mbarrier transaction counts.
+//   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators);
+//              one lane issues tcgen05.mma kind::f16 (M=128, N=256, K=16,
+//              4 per k-block) and tcgen05.commit to free smem stages and to
+//              hand a finished accumulator to the epilogue.
+//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
+//              SwiGLU in fp32, bf16 stores masked to the segment.
+// Double-buffered accumulators overlap a tile's epilogue with the next
+// tile's main loop.  Tiles are ordered (segment, n-block, m-block) so that
+// CTAs running side by side share B tiles (weights) and A rows in L2.
+// All waits are bounded (%globaltimer); on expiry the CTA records
+// MOE_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, frees TMEM, exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBHalfBytes = 128 * kBK * 2;
+constexpr int kStageBytes = kABytes + 2 * kBHalfBytes;
+constexpr int kMaxSegs = 1024;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+struct __align__(8) Bars {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+};
+
+constexpr size_t kBarsOff = (size_t)kStages * kStageBytes;
+constexpr size_t kMiscOff = kBarsOff + sizeof(Bars);
+constexpr size_t kSegOff = kMiscOff + 16;
+constexpr size_t kSmemBytes = kSegOff + (size_t)(3 * kMaxSegs + 2) * 4 + 1024;
+
+struct FfnParams {
+  const int32_t *seg_offsets;
+  const int32_t *seg_expert;
+  int32_t S, E, n_rows, K, n_blocks;
+  int32_t b_rows_per_expert;  // rows of one expert's B matrix (2I or H)
+  int32_t b_nblk_stride;      // B row step per n-block (128 or 256)
+  int32_t b_second_off;       // row offset of the second 128-row half (I or 128)
+  uint16_t *out;
+  int32_t out_ld;
+  int32_t out_nblk_stride;    // output column step per n-block (128 or 256)
+  int32_t mode;               // 0 gate/up + SwiGLU, 1 down
+  int32_t *status;
+};
+
+// ------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; gives up when another role aborted or the deadline passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int32_t *abort_flag, int32_t *status,
+                                          int32_t kid) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = moe::global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    const uint64_t dt = moe::global_timer_ns() - t0;
+    if (dt > moe::kWaitLimitNs) {
+      *abort_flag = 1;
+      moe::report_error(status, MOE_ERR_DEVICE_TIMEOUT, (int32_t)(dt / 1000), kid);
+      return false;
+    }
+  }
+}
+
+// Bounded wait used while tearing down: ignores the abort flag.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = moe::global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (moe::global_timer_ns() - t0 > moe::kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m, int32_t x,
+                                            int32_t y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128
+// bytes, 8-row groups 1024 bytes apart (SBO), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;            // leading-dimension offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride-dimension offset
+  d |= (uint64_t)1 << 46;            // version
+  d |= (uint64_t)2 << 61;            // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&p);
+}
+
+__device__ __forceinline__ float silu_mul(uint32_t g_bits, uint32_t u_bits) {
+  const float g = __uint_as_float(g_bits);
+  const float u = __uint_as_float(u_bits);
+  return g / (1.0f + expf(-g)) * u;
+}
+
+// Tile t -> (segment, n-block, m-block).  tile_prefix[s] = m-tiles before
+// segment s; segment s owns tiles [tile_prefix[s]*NB, tile_prefix[s+1]*NB).
+__device__ __forceinline__ void decode_tile(int64_t t, const int32_t *tile_prefix, int S, int NB,
+                                            int &s, int &n_blk, int &m_blk) {
+  int lo = 0, hi = S - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)tile_prefix[mid] * NB <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  s = lo;
+  const int64_t local = t - (int64_t)tile_prefix[s] * NB;
+  const int mt = tile_prefix[s + 1] - tile_prefix[s];
+  n_blk = (int)(local / mt);
+  m_blk = (int)(local % mt);
+}
+
+// --------------------------------------------------------------- the kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                       const __grid_constant__ CUtensorMap tmap_b, const FfnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Bars *bars = reinterpret_cast<Bars *>(smem + kBarsOff);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kMiscOff);
+  volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + kMiscOff + 4);
+  int32_t *seg_off = reinterpret_cast<int32_t *>(smem + kSegOff);  // [S+1]
+  int32_t *tile_prefix = seg_off + (kMaxSegs + 1);                 // [S+1]
+  int32_t *seg_exp = tile_prefix + (kMaxSegs + 1);                 // [S]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t kid = p.mode == 0 ? moe::K_FFN_GATE_UP : moe::K_FFN_DOWN;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->tfull[i], 1);
+      mbar_init(&bars->tempty[i], 128);
+    }
+    mbar_init(&bars->drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  for (int s = threadIdx.x; s <= p.S; s += kThreads) seg_off[s] = p.seg_offsets[s];
+  for (int s = threadIdx.x; s < p.S; s += kThreads) seg_exp[s] = p.seg_expert[s];
+  __syncthreads();
+  for (int s = threadIdx.x; s < p.S; s += kThreads) {
+    const int lo = seg_off[s];
+    const int hi = min(seg_off[s + 1], p.n_rows);
+    const int e = seg_exp[s];
+    int mt = (hi > lo && lo >= 0) ? (hi - lo + kBM - 1) / kBM : 0;
+    if (mt > 0 && (e < 0 || e >= p.E)) {
+      moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, s, kid);
+      mt = 0;
+    }
+    tile_prefix[s] = mt;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the m-tile counts; lane L owns a chunk
+    const int per = (p.S + 31) / 32;
+    const int lo = lane * per, hi = min(p.S, lo + per);
+    int sum = 0;
+    for (int s = lo; s < hi; ++s) sum += tile_prefix[s];
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int run = incl - sum;
+    for (int s = lo; s < hi; ++s) {
+      const int c = tile_prefix[s];
+      tile_prefix[s] = run;
+      run += c;
+    }
+    if (lane == 31) tile_prefix[p.S] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int NB = p.n_blocks;
+  const int64_t total = (int64_t)tile_prefix[p.S] * NB;
+  const int nk = p.K / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      prefetch_tmap(&tmap_a);
+      prefetch_tmap(&tmap_b);
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int s, n_blk, m_blk;
+        decode_tile(t, tile_prefix, p.S, NB, s, n_blk, m_blk);
+        const int e = seg_exp[s];
+        const int row_a = seg_off[s] + m_blk * kBM;
+        const int row_b0 = e * p.b_rows_per_expert + n_blk * p.b_nblk_stride;
+        const int row_b1 = row_b0 + p.b_second_off;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.status, kid)) {
+            ok = false;
+            break;
+          }
+          uint8_t *sa = smem + (size_t)stage * kStageBytes;
+          mbar_arrive_expect_tx(&bars->full[stage], kStageBytes);
+          tma_load_2d(sa, &tmap_a, kb * kBK, row_a, &bars->full[stage]);
+          tma_load_2d(sa + kABytes, &tmap_b, kb * kBK, row_b0, &bars->full[stage]);
+          tma_load_2d(sa + kABytes + kBHalfBytes, &tmap_b, kb * kBK, row_b1, &bars->full[stage]);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int i = 0; i < kStages; ++i)  // own copies land before the CTA exits
+        if ((armed >> i) & 1u) mbar_wait_drain(&bars->full[i], (armed_par >> i) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, p.status, kid)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&bars->full[stage], phase, abort_flag, p.status, kid)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc,
+                      (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(&bars->empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&bars->tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_commit(&bars->drain);  // every MMA of this thread has finished
+      mbar_wait_drain(&bars->drain, 0);
+    }
+  } else {
+    // -------------------------------------------------- epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r_in = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+      int s, n_blk, m_blk;
+      decode_tile(t, tile_prefix, p.S, NB, s, n_blk, m_blk);
+      const int row = seg_off[s] + m_blk * kBM + r_in;
+      const bool valid = row < min(seg_off[s + 1], p.n_rows);
+      if (!mbar_wait(&bars->tfull[acc], acc_phase, abort_flag, p.status, kid)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN);
+      if (p.mode == 0) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tbase + c * 32, g);
+          tmem_ld32(tbase + 128 + c * 32, u);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(silu_mul(g[2 * i], u[2 * i]), silu_mul(g[2 * i + 1], u[2 * i + 1]));
+          if (valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + (int64_t)row * p.out_ld +
+                                                   (int64_t)n_blk * p.out_nblk_stride + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c * 32, v);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          if (valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + (int64_t)row * p.out_ld +
+                                                   (int64_t)n_blk * p.out_nblk_stride + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 row-major [rows, cols] map with a 64-column x 128-row box.
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool ensure_smem_attr() {
+  constexpr int kMaxDevices = 64;
+  static bool done[kMaxDevices] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev >= 0 && dev < kMaxDevices && done[dev]) return true;
+  if (cudaFuncSetAttribute(grouped_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes) != cudaSuccess)
+    return false;
+  if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
+  return true;
+}
+
+moe_status launch(const CUtensorMap &ma, const CUtensorMap &mb, const FfnParams &p,
+                  int64_t max_tiles, cudaStream_t st) {
+  int64_t grid = moe_host::sm_count();
+  if (max_tiles < grid) grid = max_tiles;
+  if (grid < 1) return MOE_OK;
+  grouped_ffn_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(ma, mb, p);
+  return moe_host::launch_status();
+}
+
+}  // namespace
+
+extern "C" moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows,
+                                      const int32_t *seg_offsets, const int32_t *seg_expert,
+                                      int32_t S, int32_t E, const uint16_t *w_gate_up,
+                                      const uint16_t *w_down, int32_t H, int32_t I, uint16_t *h,
+                                      uint16_t *y_perm, void *ws, size_t ws_bytes, void *stream) {
+  if (n_rows < 0 || S < 1 || E < 1 || H < 1 || I < 1) return MOE_ERR_INVALID_ARG;
+  if (S > kMaxSegs || H % 256 != 0 || I % 128 != 0 || n_rows >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)E * 2 * I >= ((int64_t)1 << 31) || (int64_t)E * H >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (!seg_offsets || !seg_expert || !w_gate_up || !w_down) return MOE_ERR_INVALID_ARG;
+  if (moe_status s = moe_host::check_ws(ws, ws_bytes, moe::kStatusBytes)) return s;
+  if (n_rows == 0) return MOE_OK;
+  if (!x_perm || !h || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!moe_host::aligned16(x_perm) || !moe_host::aligned16(h) || !moe_host::aligned16(y_perm) ||
+      !moe_host::aligned16(w_gate_up) || !moe_host::aligned16(w_down))
+    return MOE_ERR_INVALID_ARG;
+  if (!ensure_smem_attr()) return MOE_ERR_CUDA;
+
+  CUtensorMap m_x, m_wgu, m_h, m_wd;
+  if (!make_map(&m_x, x_perm, (uint64_t)n_rows, (uint64_t)H) ||
+      !make_map(&m_wgu, w_gate_up, (uint64_t)E * 2 * I, (uint64_t)H) ||
+      !make_map(&m_h, h, (uint64_t)n_rows, (uint64_t)I) ||
+      !make_map(&m_wd, w_down, (uint64_t)E * H, (uint64_t)I))
+    return MOE_ERR_CUDA;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t m_tiles_max = (n_rows + kBM - 1) / kBM + S;  // sum of ceil(count/128)
+  int32_t *status = moe_host::status_ptr(ws);
+
+  FfnParams p1{};
+  p1.seg_offsets = seg_offsets;
+  p1.seg_expert = seg_expert;
+  p1.S = S;
+  p1.E = E;
+  p1.n_rows = (int32_t)n_rows;
+  p1.K = H;
+  p1.n_blocks = I / 128;
+  p1.b_rows_per_expert = 2 * I;
+  p1.b_nblk_stride = 128;
+  p1.b_second_off = I;
+  p1.out = h;
+  p1.out_ld = I;
+  p1.out_nblk_stride = 128;
+  p1.mode = 0;
+  p1.status = status;
+  if (moe_status s = launch(m_x, m_wgu, p1, m_tiles_max * p1.n_blocks, st)) return s;
+
+  FfnParams p2 = p1;
+  p2.K = I;
+  p2.n_blocks = H / 256;
+  p2.b_rows_per_expert = H;
+  p2.b_nblk_stride = 256;
+  p2.b_second_off = 128;
+  p2.out = y_perm;
+  p2.out_ld = H;
+  p2.out_nblk_stride = 256;
+  p2.mode = 1;
+  return launch(m_h, m_wd, p2, m_tiles_max * p2.n_blocks, st);
+}

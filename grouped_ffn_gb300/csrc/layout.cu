@@ -1,0 +1,310 @@
+// Dispatch layout: slot choice, histogram, stable prefix-scan permutation
+// into contiguous per-slot segments, and per-rank counts.
+// "14. Serving Mixture-of-Experts Models", "Follow one token through an MoE
+// layer", steps 1-2: a permutation built from a histogram over the expert
+// ids, so that the kernels that follow see contiguous per-expert segments,
+// each sent to the rank that owns the expert.  Replica preference: "The
+// network topology is visible in every MoE layer" (a copy on the same node
+// first, otherwise spread).
+//
+// One pass over the assignments, single launch plus a tiny finalize:
+//  * CTAs take 4096-assignment tiles in launch order from an atomic ticket.
+//  * Each warp ranks its 256 assignments stably with __match_any_sync and a
+//    per-warp shared-memory histogram; a per-slot scan over the 16 warps
+//    gives the tile's own histogram and each warp's offset.
+//  * Tiles chain their per-slot histograms with a decoupled look-back
+//    (one 32-bit word per (tile, slot): 2-bit flag + 30-bit count), so each
+//    assignment's rank within its slot is known after one read of the
+//    input.  Every spin is bounded by a %globaltimer deadline.
+//  * The CTA of the last tile turns the totals into seg_counts,
+//    seg_offsets (exclusive scan) and rank_counts; the finalize kernel adds
+//    seg_offsets to every partial rank and writes the inverse permutation.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kPerWarp = 256;
+constexpr int kRounds = kPerWarp / 32;
+constexpr int kTileA = kWarps * kPerWarp;  // 4096 assignments per tile
+constexpr int kMaxSlots = 1024;
+constexpr int kMaxRanks = 1024;
+
+constexpr uint32_t kFlagAgg = 1u << 30;
+constexpr uint32_t kFlagInc = 2u << 30;
+constexpr uint32_t kFlagErr = 3u << 30;
+constexpr uint32_t kValMask = (1u << 30) - 1;
+
+struct LayoutArgs {
+  const int32_t *topk_ids;
+  int64_t A;
+  int32_t k, E, S, R, rpn;
+  const int32_t *slot_expert, *slot_rank, *rep_offsets, *rep_slots, *token_src_rank;
+  int32_t *slot, *seg_counts, *seg_offsets, *dest_row, *src_assign, *rank_counts;
+  uint32_t *tile_flags;  // [n_tiles][S]
+  int32_t *ticket;
+  int32_t *status;
+  int32_t n_tiles;
+};
+
+// Slot serving assignment a, or -1 after reporting an error.
+__device__ int choose_slot(const LayoutArgs &p, int64_t a) {
+  const int64_t t = a / p.k;
+  const int e = p.topk_ids[a];
+  if (e < 0 || e >= p.E) {
+    moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, (int32_t)a, moe::K_LAYOUT_SCAN);
+    return -1;
+  }
+  const int lo = p.rep_offsets[e], hi = p.rep_offsets[e + 1];
+  const int n = hi - lo;
+  int s = -1;
+  if (n == 1) {
+    s = p.rep_slots[lo];
+  } else if (n > 1) {
+    const int src = p.token_src_rank ? p.token_src_rank[t] : (int)(t % p.R);
+    const int node = src / p.rpn;
+    for (int i = lo; i < hi; ++i) {
+      const int c = p.rep_slots[i];
+      if (c >= 0 && c < p.S && p.slot_rank[c] / p.rpn == node) {
+        s = c;
+        break;
+      }
+    }
+    if (s < 0) s = p.rep_slots[lo + (int)(t % n)];
+  }
+  if (s < 0 || s >= p.S || p.slot_expert[s] != e) {
+    moe::report_error(p.status, MOE_ERR_PLACEMENT, e, moe::K_LAYOUT_SCAN);
+    return -1;
+  }
+  return s;
+}
+
+__global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
+  extern __shared__ int32_t smem[];
+  int32_t *whist = smem;                       // [kWarps][S]: counts, then warp offsets
+  int32_t *tile_prefix = smem + kWarps * p.S;  // [S]
+  int32_t *tile_agg = tile_prefix + p.S;       // [S]
+  int32_t *rload = tile_agg + p.S;             // [R], last tile only
+  __shared__ int32_t s_tile;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) s_tile = atomicAdd(p.ticket, 1);
+  for (int i = tid; i < kWarps * p.S; i += kThreads) whist[i] = 0;
+  __syncthreads();
+  const int tile = s_tile;
+
+  // ---- stable rank of each assignment inside its warp's 256-run
+  const int64_t base = (int64_t)tile * kTileA + (int64_t)warp * kPerWarp;
+  int my_slot[kRounds], my_rank[kRounds];
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int64_t a = base + r * 32 + lane;
+    const int s = (a < p.A) ? choose_slot(p, a) : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, s);
+    const int leader = __ffs(peers) - 1;
+    const int before = (s >= 0) ? whist[warp * p.S + s] : 0;
+    __syncwarp();
+    if (s >= 0 && lane == leader) whist[warp * p.S + s] = before + __popc(peers);
+    __syncwarp();
+    my_slot[r] = s;
+    my_rank[r] = before + __popc(peers & ((1u << lane) - 1u));
+  }
+  __syncthreads();
+
+  // ---- per slot: warp offsets, tile aggregate, decoupled look-back
+  for (int s = tid; s < p.S; s += kThreads) {
+    int run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = whist[w * p.S + s];
+      whist[w * p.S + s] = run;
+      run += c;
+    }
+    tile_agg[s] = run;
+    uint32_t *my_flag = p.tile_flags + (size_t)tile * p.S + s;
+    int prefix = 0;
+    bool ok = true;
+    if (tile == 0) {
+      moe::st_relaxed_u32(my_flag, kFlagInc | (uint32_t)run);
+    } else {
+      moe::st_relaxed_u32(my_flag, kFlagAgg | (uint32_t)run);
+      const uint64_t t0 = moe::global_timer_ns();
+      for (int j = tile - 1; j >= 0;) {
+        const uint32_t f = moe::ld_relaxed_u32(p.tile_flags + (size_t)j * p.S + s);
+        const uint32_t flag = f & ~kValMask;
+        if (flag == 0) {
+          if (moe::global_timer_ns() - t0 > moe::kWaitLimitNs) {
+            moe::report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, tile, moe::K_LAYOUT_SCAN);
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+          continue;
+        }
+        if (flag == kFlagErr) {
+          ok = false;
+          break;
+        }
+        prefix += (int)(f & kValMask);
+        if (flag == kFlagInc) break;
+        --j;
+      }
+      moe::st_relaxed_u32(my_flag, ok ? (kFlagInc | (uint32_t)(prefix + run)) : kFlagErr);
+    }
+    tile_prefix[s] = prefix;
+  }
+  __syncthreads();
+
+  // ---- partial destination rows (seg_offsets added by the finalize kernel)
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int64_t a = base + r * 32 + lane;
+    if (a < p.A) {
+      const int s = my_slot[r];
+      p.slot[a] = s;
+      p.dest_row[a] = (s >= 0) ? tile_prefix[s] + whist[warp * p.S + s] + my_rank[r] : -1;
+    }
+  }
+
+  // ---- the last tile knows the totals
+  if (tile != p.n_tiles - 1) return;
+  int32_t *tot = whist;  // reuse: [S] totals
+  __syncthreads();
+  for (int s = tid; s < p.S; s += kThreads) {
+    tot[s] = tile_prefix[s] + tile_agg[s];
+    p.seg_counts[s] = tot[s];
+  }
+  for (int r = tid; r < p.R; r += kThreads) rload[r] = 0;
+  __syncthreads();
+  for (int s = tid; s < p.S; s += kThreads) {
+    const int r = p.slot_rank[s], e = p.slot_expert[s];
+    bool bad = r < 0 || r >= p.R || e < 0 || e >= p.E;
+    if (s > 0) {
+      const int pr = p.slot_rank[s - 1], pe = p.slot_expert[s - 1];
+      bad = bad || pr > r || (pr == r && pe >= e);
+    }
+    if (bad)
+      moe::report_error(p.status, MOE_ERR_PLACEMENT, s, moe::K_LAYOUT_SCAN);
+    else
+      atomicAdd(&rload[r], tot[s]);
+  }
+  // exclusive scan of the totals by warp 0: lane L owns a contiguous chunk
+  if (warp == 0) {
+    const int per = (p.S + 31) / 32;
+    const int lo = lane * per, hi = min(p.S, lo + per);
+    int sum = 0;
+    for (int s = lo; s < hi; ++s) sum += tot[s];
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int run = incl - sum;
+    for (int s = lo; s < hi; ++s) {
+      p.seg_offsets[s] = run;
+      run += tot[s];
+    }
+    if (lane == 31) p.seg_offsets[p.S] = incl;
+  }
+  __syncthreads();
+  for (int r = tid; r < p.R; r += kThreads) p.rank_counts[r] = rload[r];
+}
+
+__global__ void layout_finalize_kernel(LayoutArgs p) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t a = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; a < p.A; a += stride) {
+    const int s = p.slot[a];
+    if (s < 0) continue;
+    const int d = p.dest_row[a] + p.seg_offsets[s];
+    if (d < 0 || d >= p.A) {
+      moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, (int32_t)a, moe::K_LAYOUT_FINALIZE);
+      p.dest_row[a] = -1;
+      continue;
+    }
+    p.dest_row[a] = d;
+    p.src_assign[d] = (int32_t)a;
+  }
+}
+
+inline int64_t n_tiles_for(int64_t A) { return A > 0 ? (A + kTileA - 1) / kTileA : 0; }
+
+constexpr size_t kTicketOff = moe::kStatusBytes;      // 256
+constexpr size_t kFlagsOff = moe::kStatusBytes + 256;  // 512
+
+}  // namespace
+
+extern "C" size_t moe_workspace_size(int64_t T, int32_t k, int32_t n_slots) {
+  if (T < 0 || k < 1 || n_slots < 1) return 0;
+  const int64_t tiles = std::max<int64_t>(n_tiles_for(T * (int64_t)k), 1);
+  return kFlagsOff + (size_t)tiles * (size_t)n_slots * sizeof(uint32_t);
+}
+
+extern "C" moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k,
+                                          const moe_placement *pl, int32_t *slot,
+                                          int32_t *seg_counts, int32_t *seg_offsets,
+                                          int32_t *dest_row, int32_t *src_assign,
+                                          int32_t *rank_counts, void *ws, size_t ws_bytes,
+                                          void *stream) {
+  if (pl == nullptr || T < 0 || k < 1) return MOE_ERR_INVALID_ARG;
+  const int64_t A = T * (int64_t)k;
+  if (A >= (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  if (pl->n_experts < 1 || pl->n_slots < 1 || pl->n_ranks < 1 || pl->ranks_per_node < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (pl->n_slots > kMaxSlots || pl->n_ranks > kMaxRanks) return MOE_ERR_UNSUPPORTED;
+  if (!pl->slot_expert || !pl->slot_rank || !pl->rep_offsets || !pl->rep_slots || !seg_counts ||
+      !seg_offsets || !rank_counts)
+    return MOE_ERR_INVALID_ARG;
+  if (A > 0 && (!topk_ids || !slot || !dest_row || !src_assign)) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_workspace_size(T, k, pl->n_slots);
+  if (moe_status st = moe_host::check_ws(ws, ws_bytes, need)) return st;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t n_tiles = std::max<int64_t>(n_tiles_for(A), 1);
+  char *wsb = static_cast<char *>(ws);
+  if (cudaMemsetAsync(wsb + kTicketOff, 0, need - kTicketOff, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+
+  LayoutArgs p{};
+  p.topk_ids = topk_ids;
+  p.A = A;
+  p.k = k;
+  p.E = pl->n_experts;
+  p.S = pl->n_slots;
+  p.R = pl->n_ranks;
+  p.rpn = pl->ranks_per_node;
+  p.slot_expert = pl->slot_expert;
+  p.slot_rank = pl->slot_rank;
+  p.rep_offsets = pl->rep_offsets;
+  p.rep_slots = pl->rep_slots;
+  p.token_src_rank = pl->token_src_rank;
+  p.slot = slot;
+  p.seg_counts = seg_counts;
+  p.seg_offsets = seg_offsets;
+  p.dest_row = dest_row;
+  p.src_assign = src_assign;
+  p.rank_counts = rank_counts;
+  p.tile_flags = reinterpret_cast<uint32_t *>(wsb + kFlagsOff);
+  p.ticket = reinterpret_cast<int32_t *>(wsb + kTicketOff);
+  p.status = moe_host::status_ptr(ws);
+  p.n_tiles = (int32_t)n_tiles;
+
+  const size_t smem = ((size_t)(kWarps + 2) * p.S + p.R) * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(layout_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  layout_scan_kernel<<<(unsigned)n_tiles, kThreads, smem, st>>>(p);
+  if (moe_status s = moe_host::launch_status()) return s;
+  if (A > 0) {
+    int64_t blocks = (A + 255) / 256;
+    const int64_t cap = (int64_t)moe_host::sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    layout_finalize_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+    if (moe_status s = moe_host::launch_status()) return s;
+  }
+  return MOE_OK;
+}

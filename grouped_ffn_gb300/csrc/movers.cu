@@ -1,0 +1,219 @@
+// Row movers and the balancedness statistic.
+//
+// permute: "14. Serving Mixture-of-Experts Models", "Price one dispatch" --
+//   every assignment carries one copy of its token's hidden row (2*H bytes).
+//   One CTA per token reads the row once with 128-bit streaming loads and
+//   writes it to its k destination rows.
+// combine: same chapter, "Follow one token", step 4 -- the inverse
+//   permutation followed by the router-weighted sum; plus the shared
+//   expert's output ("Mixture-of-Experts Inference", "MoE architecture
+//   recap").  One CTA per token gathers the k expert rows 16 bytes at a time
+//   and accumulates in fp32 with fmaf in j order, starting from the shared
+//   output (or 0), then rounds once to bf16.
+// balance: "The slowest expert sets the pace" -- avg/max per-rank load.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kMoverThreads = 128;
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(kMoverThreads) permute_kernel(
+    const uint4 *__restrict__ x, int64_t T, int H8, int k, const int32_t *__restrict__ dest_row,
+    uint4 *__restrict__ xp, int64_t A, int32_t *status) {
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    const uint4 *src = x + t * H8;
+    const int32_t *dr = dest_row + t * k;
+    for (int c0 = threadIdx.x; c0 < H8; c0 += kMoverThreads * kUnroll) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int c = c0 + u * kMoverThreads;
+        if (c < H8) v[u] = moe::ld_stream_u4(src + c);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int32_t r = __ldg(dr + j);
+        if (r < 0 || r >= A) {
+          if (threadIdx.x == 0 && c0 == 0)
+            moe::report_error(status, MOE_ERR_DEVICE_INDEX, (int32_t)(t * k + j), moe::K_PERMUTE);
+          continue;
+        }
+        uint4 *dst = xp + (int64_t)r * H8;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int c = c0 + u * kMoverThreads;
+          if (c < H8) dst[c] = v[u];
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void bf16x8_fma(const uint4 &v, float w, float (&acc)[8]) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(u[i] << 16);
+    const float hi = __uint_as_float(u[i] & 0xFFFF0000u);
+    acc[2 * i] = fmaf(w, lo, acc[2 * i]);
+    acc[2 * i + 1] = fmaf(w, hi, acc[2 * i + 1]);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&p);
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kMoverThreads) combine_kernel(
+    const uint4 *__restrict__ yp, const int32_t *__restrict__ dest_row,
+    const float *__restrict__ topk_w, int64_t T, int k, int H8, const uint4 *__restrict__ shared,
+    uint4 *__restrict__ y, int64_t A, int32_t *status) {
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    int32_t r[KMAX];
+    float w[KMAX];
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k) {
+        r[j] = __ldg(dest_row + t * k + j);
+        w[j] = __ldg(topk_w + t * k + j);
+        if (r[j] < 0 || r[j] >= A) ok = false;
+      }
+    }
+    if (!ok) {
+      if (threadIdx.x == 0) moe::report_error(status, MOE_ERR_DEVICE_INDEX, (int32_t)t, moe::K_COMBINE);
+      continue;
+    }
+    for (int c = threadIdx.x; c < H8; c += kMoverThreads) {
+      uint4 v[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) v[j] = moe::ld_stream_u4(yp + (int64_t)r[j] * H8 + c);
+      float acc[8];
+      if (shared) {
+        const uint4 s = moe::ld_stream_u4(shared + t * H8 + c);
+        const uint32_t u[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = __uint_as_float(u[i] << 16);
+          acc[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) bf16x8_fma(v[j], w[j], acc);
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      y[t * H8 + c] = o;
+    }
+  }
+}
+
+__global__ void balance_kernel(const int32_t *__restrict__ rc, int R, double *bal, int32_t *mx,
+                               int64_t *total) {
+  __shared__ long long s_tot[32];
+  __shared__ int s_max[32];
+  long long tsum = 0;
+  int tmax = 0;
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    const int v = rc[r];
+    tsum += v;
+    tmax = max(tmax, v);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    tsum += __shfl_xor_sync(0xffffffffu, tsum, off);
+    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    s_tot[warp] = tsum;
+    s_max[warp] = tmax;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long T = 0;
+    int M = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+      T += s_tot[i];
+      M = max(M, s_max[i]);
+    }
+    *total = T;
+    *mx = M;
+    *bal = (T == 0) ? 1.0 : (double)T / ((double)R * (double)M);
+  }
+}
+
+unsigned mover_grid(int64_t T) {
+  const int64_t cap = (int64_t)moe_host::sm_count() * 32;
+  return (unsigned)(T < cap ? T : cap);
+}
+
+}  // namespace
+
+extern "C" moe_status moe_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                                  const int32_t *dest_row, uint16_t *x_perm, void *ws,
+                                  size_t ws_bytes, void *stream) {
+  if (T < 0 || H < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !dest_row || !x_perm) return MOE_ERR_INVALID_ARG;
+  if (!moe_host::aligned16(x) || !moe_host::aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  if (moe_status s = moe_host::check_ws(ws, ws_bytes, moe::kStatusBytes)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  permute_kernel<<<mover_grid(T), kMoverThreads, 0, st>>>(
+      reinterpret_cast<const uint4 *>(x), T, H / 8, k, dest_row, reinterpret_cast<uint4 *>(x_perm),
+      T * (int64_t)k, moe_host::status_ptr(ws));
+  return moe_host::launch_status();
+}
+
+extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *dest_row,
+                                  const float *topk_w, int64_t T, int32_t k, int32_t H,
+                                  const uint16_t *shared, uint16_t *y, void *ws, size_t ws_bytes,
+                                  void *stream) {
+  if (T < 0 || H < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (H % 8 != 0 || k > 16) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y_perm || !dest_row || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+  if (!moe_host::aligned16(y_perm) || !moe_host::aligned16(y) ||
+      (shared && !moe_host::aligned16(shared)))
+    return MOE_ERR_INVALID_ARG;
+  if (moe_status s = moe_host::check_ws(ws, ws_bytes, moe::kStatusBytes)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint4 *yp = reinterpret_cast<const uint4 *>(y_perm);
+  const uint4 *sh = reinterpret_cast<const uint4 *>(shared);
+  uint4 *yo = reinterpret_cast<uint4 *>(y);
+  const int64_t A = T * (int64_t)k;
+  int32_t *status = moe_host::status_ptr(ws);
+  const unsigned g = mover_grid(T);
+  if (k <= 2)
+    combine_kernel<2><<<g, kMoverThreads, 0, st>>>(yp, dest_row, topk_w, T, k, H / 8, sh, yo, A, status);
+  else if (k <= 4)
+    combine_kernel<4><<<g, kMoverThreads, 0, st>>>(yp, dest_row, topk_w, T, k, H / 8, sh, yo, A, status);
+  else if (k <= 8)
+    combine_kernel<8><<<g, kMoverThreads, 0, st>>>(yp, dest_row, topk_w, T, k, H / 8, sh, yo, A, status);
+  else
+    combine_kernel<16><<<g, kMoverThreads, 0, st>>>(yp, dest_row, topk_w, T, k, H / 8, sh, yo, A, status);
+  return moe_host::launch_status();
+}
+
+extern "C" moe_status moe_balance_stats(const int32_t *rank_counts, int32_t R, double *balancedness,
+                                        int32_t *max_count, int64_t *total, void *ws,
+                                        size_t ws_bytes, void *stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (R < 1 || !rank_counts || !balancedness || !max_count || !total) return MOE_ERR_INVALID_ARG;
+  balance_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(rank_counts, R, balancedness,
+                                                                     max_count, total);
+  return moe_host::launch_status();
+}

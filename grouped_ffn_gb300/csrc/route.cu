@@ -1,0 +1,212 @@
+// Router: softmax or sigmoid top-k with optional group limit, one warp per
+// token.  "14. Serving Mixture-of-Experts Models", "Follow one token through
+// an MoE layer": the router produces expert ids and weights for every
+// token.  "Mixture-of-Experts Inference", "MoE architecture recap": grouped
+// routing picks a limited number of expert groups first, then the top
+// experts within them.
+//
+// Layout: lane L of the warp holds logits L, L+32, L+64, ... of its token
+// (VPL values per lane, coalesced 128-byte loads).  Each of the k rounds is
+// a per-lane scan of its unselected values followed by a 5-step butterfly
+// arg-max; the order (value descending, id ascending) is exactly the one of
+// the result, so no sort is needed.  Selection compares the fp32 logits as
+// IEEE values (so -0 == +0 and ties go to the lower id); group scores and
+// weights are computed in fp64 and rounded once.
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+
+namespace {
+
+struct RouteArgs {
+  int32_t score_fn, k, n_groups, topk_groups, group_topn;
+};
+
+__device__ __forceinline__ double sigmoid64(float x) { return 1.0 / (1.0 + exp(-(double)x)); }
+
+// Does candidate (ov, oid) beat (bv, bid)?  oid == INT_MAX marks "none".
+__device__ __forceinline__ bool beats(float ov, int oid, float bv, int bid) {
+  if (oid == INT_MAX) return false;
+  if (bid == INT_MAX) return true;
+  return ov > bv || (ov == bv && oid < bid);
+}
+
+// Arg-max over the warp of the values whose bit is set in `mask` (bit i =
+// this lane's element i, id = lane + 32 i).  Returns the winner in all lanes.
+template <int VPL>
+__device__ __forceinline__ void warp_argmax(const float (&v)[VPL], uint32_t mask, int lane,
+                                            float &bv, int &bid) {
+  bv = -FLT_MAX;
+  bid = INT_MAX;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    if ((mask >> i) & 1u) {
+      if (beats(v[i], lane + 32 * i, bv, bid)) {
+        bv = v[i];
+        bid = lane + 32 * i;
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+    int oid = __shfl_xor_sync(0xffffffffu, bid, off);
+    if (beats(ov, oid, bv, bid)) {
+      bv = ov;
+      bid = oid;
+    }
+  }
+}
+
+__device__ __forceinline__ double warp_sum_f64(double x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits, int64_t T,
+                                                    int E, RouteArgs a, int32_t *__restrict__ ids,
+                                                    float *__restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int gsz = a.n_groups > 1 ? E / a.n_groups : E;
+
+  for (int64_t t = warp0; t < T; t += nwarps) {
+    const float *row = logits + t * E;
+    float v[VPL];
+    uint32_t avail = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        v[i] = __ldg(row + e);
+        avail |= 1u << i;
+      } else {
+        v[i] = 0.0f;
+      }
+    }
+
+    if (a.n_groups > 1) {
+      // Group score: fp64 sum of the sigmoids of the group's group_topn
+      // largest logits, taken in descending order.  Lane g keeps group g's.
+      double my_gscore = 0.0;
+      for (int g = 0; g < a.n_groups; ++g) {
+        uint32_t gmask = 0;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+          if (((avail >> i) & 1u) && (lane + 32 * i) / gsz == g) gmask |= 1u << i;
+        double s = 0.0;
+        for (int r = 0; r < a.group_topn; ++r) {
+          float bv;
+          int bid;
+          warp_argmax<VPL>(v, gmask, lane, bv, bid);
+          s += sigmoid64(bv);
+          if ((bid & 31) == lane) gmask &= ~(1u << (bid >> 5));
+        }
+        if (lane == g) my_gscore = s;
+      }
+      // Keep the topk_groups best groups (score descending, id ascending).
+      bool gfree = lane < a.n_groups;
+      uint32_t kept = 0;
+      for (int r = 0; r < a.topk_groups; ++r) {
+        double bs = gfree ? my_gscore : 0.0;
+        int bg = gfree ? lane : INT_MAX;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          double os = __shfl_xor_sync(0xffffffffu, bs, off);
+          int og = __shfl_xor_sync(0xffffffffu, bg, off);
+          bool take = og != INT_MAX && (bg == INT_MAX || os > bs || (os == bs && og < bg));
+          if (take) {
+            bs = os;
+            bg = og;
+          }
+        }
+        kept |= 1u << bg;
+        if (lane == bg) gfree = false;
+      }
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (!((kept >> ((lane + 32 * i) / gsz)) & 1u)) avail &= ~(1u << i);
+    }
+
+    // Top-k: lane j keeps the j-th selection.
+    float my_v = 0.0f;
+    int my_id = 0;
+    for (int j = 0; j < a.k; ++j) {
+      float bv;
+      int bid;
+      warp_argmax<VPL>(v, avail, lane, bv, bid);
+      if ((bid & 31) == lane) avail &= ~(1u << (bid >> 5));
+      if (lane == j) {
+        my_v = bv;
+        my_id = bid;
+      }
+    }
+
+    double num = 0.0;
+    if (a.score_fn == MOE_SCORE_SOFTMAX) {
+      const double m = (double)__shfl_sync(0xffffffffu, my_v, 0);  // the largest logit
+      if (lane < a.k) num = exp((double)my_v - m);
+    } else {
+      if (lane < a.k) num = sigmoid64(my_v);
+    }
+    const double den = warp_sum_f64(num);
+    if (lane < a.k) {
+      ids[t * a.k + lane] = my_id;
+      w[t * a.k + lane] = (float)(num / den);
+    }
+  }
+}
+
+template <int VPL>
+void launch_route(const float *logits, int64_t T, int E, RouteArgs a, int32_t *ids, float *w,
+                  cudaStream_t st) {
+  const int threads = 256;
+  int64_t blocks = (T + 7) / 8;
+  const int64_t cap = (int64_t)moe_host::sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  route_kernel<VPL><<<(unsigned)blocks, threads, 0, st>>>(logits, T, E, a, ids, w);
+}
+
+}  // namespace
+
+extern "C" moe_status moe_route(const float *logits, int64_t T, int32_t E, const moe_route_cfg *cfg,
+                                int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes,
+                                void *stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (cfg == nullptr || T < 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (logits == nullptr || topk_ids == nullptr || topk_w == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  RouteArgs a{cfg->score_fn, cfg->k, cfg->n_groups, cfg->topk_groups, cfg->group_topn};
+  if (a.score_fn != MOE_SCORE_SOFTMAX && a.score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (a.k < 1 || a.k > E) return MOE_ERR_INVALID_ARG;
+  if (a.k > 16 || E > 512) return MOE_ERR_UNSUPPORTED;
+  if (a.n_groups < 1) return MOE_ERR_INVALID_ARG;
+  if (a.n_groups > 1) {
+    if (a.score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+    if (a.n_groups > 32 || E % a.n_groups != 0) return MOE_ERR_UNSUPPORTED;
+    const int gsz = E / a.n_groups;
+    if (a.topk_groups < 1 || a.topk_groups > a.n_groups) return MOE_ERR_INVALID_ARG;
+    if (a.group_topn < 1 || a.group_topn > gsz) return MOE_ERR_INVALID_ARG;
+    if (a.k > a.topk_groups * gsz) return MOE_ERR_INVALID_ARG;
+  }
+  if (T == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int vpl = (E + 31) / 32;
+  if (vpl <= 1)
+    launch_route<1>(logits, T, E, a, topk_ids, topk_w, st);
+  else if (vpl <= 2)
+    launch_route<2>(logits, T, E, a, topk_ids, topk_w, st);
+  else if (vpl <= 4)
+    launch_route<4>(logits, T, E, a, topk_ids, topk_w, st);
+  else if (vpl <= 8)
+    launch_route<8>(logits, T, E, a, topk_ids, topk_w, st);
+  else
+    launch_route<16>(logits, T, E, a, topk_ids, topk_w, st);
+  return moe_host::launch_status();
+}

@@ -1,0 +1,123 @@
+"""MoELayer: the whole hot path as one call over persistent device buffers.
+
+route -> dispatch_layout -> permute -> grouped_ffn (+ shared expert) ->
+combine -> balance_stats, each a libmoe.so kernel launch on one stream, with
+no host synchronisation inside a step (the host never reads segment sizes:
+they stay on the device, as "Zepp" Section 6.4 notes for planning without
+per-layer host sync).  Buffers are allocated once, for the largest token
+count, through torch; the library itself allocates nothing.
+"""
+
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import moe
+
+
+class MoELayer:
+    def __init__(self, *, H: int, I: int, E: int, k: int, placement: moe.DevicePlacement,
+                 w_gate_up: torch.Tensor, w_down: torch.Tensor, max_tokens: int,
+                 score_fn: int = moe.MOE_SCORE_SOFTMAX, n_groups: int = 1,
+                 topk_groups: int = 1, group_topn: int = 1,
+                 shared_w_gate_up: Optional[torch.Tensor] = None,
+                 shared_w_down: Optional[torch.Tensor] = None, device="cuda"):
+        self.H, self.I, self.E, self.k = H, I, E, k
+        self.placement = placement
+        self.w_gate_up, self.w_down = w_gate_up, w_down
+        self.shared_w_gate_up, self.shared_w_down = shared_w_gate_up, shared_w_down
+        self.cfg = moe.RouteCfg(score_fn, k, n_groups, topk_groups, group_topn)
+        self.max_tokens = max_tokens
+        dev = torch.device(device)
+        A = max_tokens * k
+        S, R = placement.n_slots, placement.n_ranks
+        i32 = dict(dtype=torch.int32, device=dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.topk_ids = torch.empty(max_tokens, k, **i32)
+        self.topk_w = torch.empty(max_tokens, k, dtype=torch.float32, device=dev)
+        self.slot = torch.empty(A, **i32)
+        self.seg_counts = torch.empty(S, **i32)
+        self.seg_offsets = torch.empty(S + 1, **i32)
+        self.dest_row = torch.empty(A, **i32)
+        self.src_assign = torch.empty(A, **i32)
+        self.rank_counts = torch.empty(R, **i32)
+        self.x_perm = torch.empty(A, H, **bf)
+        self.h = torch.empty(A, I, **bf)
+        self.y_perm = torch.empty(A, H, **bf)
+        self.balancedness = torch.empty(1, dtype=torch.float64, device=dev)
+        self.max_count = torch.empty(1, **i32)
+        self.total = torch.empty(1, dtype=torch.int64, device=dev)
+        self.ws = moe.new_workspace(max_tokens, k, S, device=dev)
+        if shared_w_gate_up is not None:
+            self.shared_I = shared_w_gate_up.shape[1] // 2
+            self.shared_h = torch.empty(max_tokens, self.shared_I, **bf)
+            self.shared_y = torch.empty(max_tokens, H, **bf)
+            self.shared_expert = torch.zeros(1, **i32)
+            self._shared_offsets = {}
+        else:
+            self.shared_I = 0
+        # route, layout scan + finalize, permute, 2 FFN, combine, balance (+2 shared FFN)
+        self.launches_per_step = 8 + (2 if shared_w_gate_up is not None else 0)
+
+    def _shared_offs(self, T: int) -> torch.Tensor:
+        t = self._shared_offsets.get(T)
+        if t is None:
+            t = torch.tensor([0, T], dtype=torch.int32).to(self.shared_expert.device)
+            self._shared_offsets[T] = t
+        return t
+
+    def forward(self, logits: torch.Tensor, x: torch.Tensor, y: torch.Tensor, stream=None,
+                mark=None):
+        """One step on device-resident inputs; y [T,H] bf16 is written.
+        mark(name), if given, is called after each stage is enqueued (the
+        benchmark records a CUDA event there)."""
+        mark = mark or (lambda name: None)
+        T = x.shape[0]
+        if T > self.max_tokens:
+            raise ValueError("more tokens than the layer was sized for")
+        A = T * self.k
+        ids, w = self.topk_ids[:T], self.topk_w[:T]
+        moe.moe_route(logits, self.cfg, ids, w, self.ws, stream)
+        mark("route")
+        moe.moe_dispatch_layout(ids, self.placement, self.slot[:A], self.seg_counts,
+                                self.seg_offsets, self.dest_row[:A], self.src_assign[:A],
+                                self.rank_counts, self.ws, stream)
+        mark("layout")
+        moe.moe_permute(x, self.k, self.dest_row[:A], self.x_perm[:A], self.ws, stream)
+        mark("permute")
+        moe.moe_grouped_ffn(self.x_perm[:A], self.seg_offsets, self.placement.slot_expert,
+                            self.w_gate_up, self.w_down, self.h[:A], self.y_perm[:A], self.ws,
+                            stream)
+        mark("grouped_ffn")
+        shared = None
+        if self.shared_I:
+            moe.moe_grouped_ffn(x, self._shared_offs(T), self.shared_expert,
+                                self.shared_w_gate_up, self.shared_w_down, self.shared_h[:T],
+                                self.shared_y[:T], self.ws, stream)
+            shared = self.shared_y[:T]
+            mark("shared_ffn")
+        moe.moe_combine(self.y_perm[:A], self.dest_row[:A], w, y, self.ws, shared, stream)
+        mark("combine")
+        moe.moe_balance_stats(self.rank_counts, self.balancedness, self.max_count, self.total,
+                              self.ws, stream)
+        mark("balance")
+        return y
+
+    def forward_host(self, logits_host: torch.Tensor, x_host: torch.Tensor,
+                     y_host: torch.Tensor, logits_dev: torch.Tensor, x_dev: torch.Tensor,
+                     y_dev: torch.Tensor, stream=None):
+        """End to end from pinned host memory: copy the step's inputs in, run
+        the layer, copy the output back (asynchronous on the stream)."""
+        s = stream or torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            logits_dev.copy_(logits_host, non_blocking=True)
+            x_dev.copy_(x_host, non_blocking=True)
+            self.forward(logits_dev, x_dev, y_dev, s)
+            y_host.copy_(y_dev, non_blocking=True)
+        return y_host
+
+    def check(self, stream=None):
+        """Raise MoeError if any kernel recorded a device-side error."""
+        moe.moe_check_device_status(self.ws, stream)

@@ -1,0 +1,255 @@
+"""ctypes binding of libmoe.so (declared in include/moe.h).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Functions carry the C names; tensors are torch tensors on the current CUDA
+device (torch supplies device memory and streams).  There is no fallback:
+if libmoe.so is missing or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_SCORE_SOFTMAX = 0
+MOE_SCORE_SIGMOID = 1
+WS_STATUS_BYTES = 256
+
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_CUDA", 4: "MOE_ERR_DEVICE_INDEX", 5: "MOE_ERR_DEVICE_TIMEOUT",
+                6: "MOE_ERR_WORKSPACE", 7: "MOE_ERR_PLACEMENT"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, call: str, status: int, info: Optional[int] = None):
+        self.status = status
+        self.info = info
+        msg = f"{call}: {STATUS_NAMES.get(status, status)}"
+        if info is not None:
+            msg += f" (info={info})"
+        super().__init__(msg)
+
+
+class RouteCfg(ctypes.Structure):
+    _fields_ = [("score_fn", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
+                ("group_topn", ctypes.c_int32)]
+
+
+class PlacementC(ctypes.Structure):
+    _fields_ = [("n_experts", ctypes.c_int32), ("n_slots", ctypes.c_int32),
+                ("n_ranks", ctypes.c_int32), ("ranks_per_node", ctypes.c_int32),
+                ("slot_expert", ctypes.c_void_p), ("slot_rank", ctypes.c_void_p),
+                ("rep_offsets", ctypes.c_void_p), ("rep_slots", ctypes.c_void_p),
+                ("token_src_rank", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "moe_workspace_size": (_SZ, [_I64, _I32, _I32]),
+    "moe_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
+    "moe_check_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(_I32)]),
+    "moe_route": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(RouteCfg), _P, _P, _P, _SZ, _P]),
+    "moe_dispatch_layout": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC),
+                                           _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_ffn": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _I32, _I32,
+                                       _P, _P, _P, _SZ, _P]),
+    "moe_combine": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "moe_balance_stats": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so from this package directory (built by build.py)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with grouped_ffn_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------------ helpers
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous CUDA tensor of {dtype}")
+
+
+def _check(call: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(call, status)
+
+
+def _bf16(t: torch.Tensor, name: str):
+    _need(t, torch.bfloat16, name)
+
+
+# ------------------------------------------------------------------ workspace
+def moe_workspace_size(T: int, k: int, n_slots: int) -> int:
+    return int(lib().moe_workspace_size(T, k, n_slots))
+
+
+def new_workspace(T: int, k: int, n_slots: int, device=None, stream=None) -> torch.Tensor:
+    """Allocate (torch) and zero a workspace for calls on up to T tokens."""
+    n = max(moe_workspace_size(T, k, n_slots), WS_STATUS_BYTES)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    moe_workspace_init(ws, stream)
+    return ws
+
+
+def moe_workspace_init(ws: torch.Tensor, stream=None):
+    _check("moe_workspace_init", lib().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_check_device_status(ws: torch.Tensor, stream=None):
+    """Synchronise the stream; raise MoeError on a recorded device error."""
+    info = _I32(0)
+    st = lib().moe_check_device_status(_ptr(ws), _stream(stream), ctypes.byref(info))
+    if st != MOE_OK:
+        raise MoeError("device", st, info.value)
+
+
+# ------------------------------------------------------------------ placement
+class DevicePlacement:
+    """Placement tables on the device plus the C struct that points at them."""
+
+    def __init__(self, slot_expert, slot_rank, rep_offsets, rep_slots, n_ranks: int,
+                 ranks_per_node: int, token_src_rank=None, device="cuda"):
+        def dev(a):
+            return torch.as_tensor(a, dtype=torch.int32).to(device).contiguous()
+
+        self.slot_expert = dev(slot_expert)
+        self.slot_rank = dev(slot_rank)
+        self.rep_offsets = dev(rep_offsets)
+        self.rep_slots = dev(rep_slots)
+        self.token_src_rank = None if token_src_rank is None else dev(token_src_rank)
+        self.n_experts = int(self.rep_offsets.numel() - 1)
+        self.n_slots = int(self.slot_expert.numel())
+        self.n_ranks = int(n_ranks)
+        self.ranks_per_node = int(ranks_per_node)
+        self.c = PlacementC(self.n_experts, self.n_slots, self.n_ranks, self.ranks_per_node,
+                            self.slot_expert.data_ptr(), self.slot_rank.data_ptr(),
+                            self.rep_offsets.data_ptr(), self.rep_slots.data_ptr(),
+                            None if self.token_src_rank is None else self.token_src_rank.data_ptr())
+
+    @classmethod
+    def from_tables(cls, pl, device="cuda"):
+        """From any object with slot_expert, slot_rank, rep_offsets, rep_slots,
+        n_ranks, ranks_per_node and token_src_rank attributes."""
+        return cls(pl.slot_expert, pl.slot_rank, pl.rep_offsets, pl.rep_slots, pl.n_ranks,
+                   pl.ranks_per_node, pl.token_src_rank, device)
+
+
+# ------------------------------------------------------------------ calls
+def moe_route(logits, cfg: RouteCfg, topk_ids, topk_w, ws=None, stream=None):
+    _need(logits, torch.float32, "logits")
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(topk_w, torch.float32, "topk_w")
+    T, E = logits.shape
+    _check("moe_route", lib().moe_route(_ptr(logits), T, E, ctypes.byref(cfg), _ptr(topk_ids),
+                                        _ptr(topk_w), _ptr(ws), 0 if ws is None else ws.numel(),
+                                        _stream(stream)))
+
+
+def moe_dispatch_layout(topk_ids, placement: DevicePlacement, slot, seg_counts, seg_offsets,
+                        dest_row, src_assign, rank_counts, ws, stream=None):
+    for n, t in (("topk_ids", topk_ids), ("slot", slot), ("seg_counts", seg_counts),
+                 ("seg_offsets", seg_offsets), ("dest_row", dest_row),
+                 ("src_assign", src_assign), ("rank_counts", rank_counts)):
+        _need(t, torch.int32, n)
+    T, k = topk_ids.shape
+    _check("moe_dispatch_layout", lib().moe_dispatch_layout(
+        _ptr(topk_ids), T, k, ctypes.byref(placement.c), _ptr(slot), _ptr(seg_counts),
+        _ptr(seg_offsets), _ptr(dest_row), _ptr(src_assign), _ptr(rank_counts), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_permute(x, k: int, dest_row, x_perm, ws, stream=None):
+    _bf16(x, "x")
+    _bf16(x_perm, "x_perm")
+    _need(dest_row, torch.int32, "dest_row")
+    T, H = x.shape
+    _check("moe_permute", lib().moe_permute(_ptr(x), T, H, k, _ptr(dest_row), _ptr(x_perm),
+                                            _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_grouped_ffn(x_perm, seg_offsets, seg_expert, w_gate_up, w_down, h, y_perm, ws,
+                    stream=None):
+    for n, t in (("x_perm", x_perm), ("w_gate_up", w_gate_up), ("w_down", w_down),
+                 ("h", h), ("y_perm", y_perm)):
+        _bf16(t, n)
+    _need(seg_offsets, torch.int32, "seg_offsets")
+    _need(seg_expert, torch.int32, "seg_expert")
+    n_rows, H = x_perm.shape
+    E, two_i, H2 = w_gate_up.shape
+    I = two_i // 2
+    if H2 != H or tuple(w_down.shape) != (E, H, I) or tuple(h.shape) != (n_rows, I) \
+            or tuple(y_perm.shape) != (n_rows, H):
+        raise ValueError("moe_grouped_ffn: inconsistent shapes")
+    S = seg_expert.numel()
+    _check("moe_grouped_ffn", lib().moe_grouped_ffn(
+        _ptr(x_perm), n_rows, _ptr(seg_offsets), _ptr(seg_expert), S, E, _ptr(w_gate_up),
+        _ptr(w_down), H, I, _ptr(h), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_combine(y_perm, dest_row, topk_w, y, ws, shared=None, stream=None):
+    _bf16(y_perm, "y_perm")
+    _bf16(y, "y")
+    if shared is not None:
+        _bf16(shared, "shared")
+    _need(dest_row, torch.int32, "dest_row")
+    _need(topk_w, torch.float32, "topk_w")
+    T, k = topk_w.shape
+    H = y.shape[1]
+    _check("moe_combine", lib().moe_combine(_ptr(y_perm), _ptr(dest_row), _ptr(topk_w), T, k, H,
+                                            _ptr(shared), _ptr(y), _ptr(ws), ws.numel(),
+                                            _stream(stream)))
+
+
+def moe_balance_stats(rank_counts, balancedness, max_count, total, ws=None, stream=None):
+    _need(rank_counts, torch.int32, "rank_counts")
+    _need(balancedness, torch.float64, "balancedness")
+    _need(max_count, torch.int32, "max_count")
+    _need(total, torch.int64, "total")
+    _check("moe_balance_stats", lib().moe_balance_stats(
+        _ptr(rank_counts), rank_counts.numel(), _ptr(balancedness), _ptr(max_count), _ptr(total),
+        _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def moe_version() -> str:
+    return lib().moe_version().decode()

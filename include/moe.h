@@ -1,0 +1,226 @@
+/*
+ * moe.h -- C ABI of the single-GPU MoE-layer hot path for GB300 (sm_103a).
+ *
+ * The six compute calls follow the four runtime steps of an MoE layer as
+ * "14. Serving Mixture-of-Experts Models" states them ("Follow one token
+ * through an MoE layer"): the router picks expert ids and weights; tokens
+ * are packed into contiguous per-expert segments by a histogram and a
+ * permutation; a grouped GEMM runs every expert's segment with its own row
+ * count; the inverse permutation and a weighted sum combine the outputs.
+ * The balancedness statistic is the one of "The slowest expert sets the
+ * pace" in the same chapter.  Expert-parallel ranks are simulated: a rank's
+ * share of the dispatched rows is a contiguous run of segments in one
+ * device buffer.
+ *
+ * Conventions for every call:
+ *  - Pointers named *device* point to GPU global memory of the current
+ *    device; pointers named *host* to host memory.  The caller allocates and
+ *    owns every buffer; the library allocates nothing and keeps no state
+ *    beyond per-device attribute caches.
+ *  - bf16 tensors are passed as uint16_t bit patterns, row-major, rows
+ *    contiguous.  All bf16 pointers must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call is asynchronous on that stream and never synchronises the host,
+ *    except moe_check_device_status.
+ *  - Errors found on the host (bad sizes, NULL pointers, unsupported shapes)
+ *    return a status at once and launch nothing.  Errors found on the
+ *    device (an expert id or row index out of range, a bounded wait that
+ *    expired) never trap: the kernel records the first one in the status
+ *    word at the start of the workspace, skips the bad access, and returns;
+ *    moe_check_device_status reports it.
+ *  - `ws` is a device workspace of at least moe_workspace_size() bytes,
+ *    16-byte aligned, zeroed once by moe_workspace_init before first use.
+ *    Calls that share a workspace must be ordered on one stream.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* NULL pointer, negative or inconsistent size */
+  MOE_ERR_UNSUPPORTED = 2,    /* shape outside the kernels' limits (see each call) */
+  MOE_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_INDEX = 4,   /* device: expert id, slot or row index out of range */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* device: a bounded wait expired; outputs are invalid */
+  MOE_ERR_WORKSPACE = 6,      /* workspace NULL, misaligned or too small */
+  MOE_ERR_PLACEMENT = 7       /* device: placement tables inconsistent */
+} moe_status;
+
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+
+/* Router configuration.
+ *  score_fn     MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID.
+ *  k            experts per token, 1 <= k <= 16, k <= E.
+ *  n_groups     1 = no group limit; else E % n_groups == 0, n_groups <= 32.
+ *  topk_groups  groups kept (1..n_groups); k <= topk_groups * E / n_groups.
+ *  group_topn   experts summed into a group's score (1..E/n_groups). */
+typedef struct moe_route_cfg {
+  int32_t score_fn;
+  int32_t k;
+  int32_t n_groups;
+  int32_t topk_groups;
+  int32_t group_topn;
+} moe_route_cfg;
+
+/* Expert placement over simulated ranks (all arrays are *device* int32).
+ *  slot_expert[S], slot_rank[S]: physical expert slot s hosts expert
+ *      slot_expert[s] on rank slot_rank[s]; slots are sorted by (rank,
+ *      expert) strictly increasing, so segment s of the dispatched buffer is
+ *      slot s and each rank's segments are contiguous.
+ *  rep_offsets[E+1], rep_slots[rep_offsets[E]]: CSR list of each expert's
+ *      slots, in ascending rank order; every expert has at least one.
+ *  token_src_rank[T] or NULL: the rank each token lives on (NULL: t mod R).
+ *  ranks_per_node: ranks of one node; node(r) = r / ranks_per_node. */
+typedef struct moe_placement {
+  int32_t n_experts;
+  int32_t n_slots;
+  int32_t n_ranks;
+  int32_t ranks_per_node;
+  const int32_t *slot_expert;
+  const int32_t *slot_rank;
+  const int32_t *rep_offsets;
+  const int32_t *rep_slots;
+  const int32_t *token_src_rank;
+} moe_placement;
+
+/* Bytes of device workspace needed by moe_dispatch_layout for T tokens,
+ * top-k and n_slots slots (a 256-byte status block plus the scan's tile
+ * flags).  Every other call needs only the status block
+ * (MOE_WS_STATUS_BYTES).  Returns 0 for invalid sizes. */
+#define MOE_WS_STATUS_BYTES 256
+size_t moe_workspace_size(int64_t T, int32_t k, int32_t n_slots);
+
+/* Zero the workspace (device, `ws_bytes` bytes) on `stream`. */
+moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronise `stream`, read the status word of `ws`, clear it, and return
+ * the first device-side error recorded since the last check (MOE_OK if
+ * none).  *info_host (may be NULL) receives a code-specific detail (the
+ * offending index, or the kernel id of an expired wait). */
+moe_status moe_check_device_status(void *ws, void *stream, int32_t *info_host);
+
+/* Router: per token, the k experts with the largest scores and their
+ * weights.  "14. Serving Mixture-of-Experts Models", "Follow one token
+ * through an MoE layer" (the router produces expert ids and weights for
+ * every token); "Zepp", Section 2 (a learned router selects the top-k
+ * experts); group-limited selection per "Mixture-of-Experts Inference",
+ * "MoE architecture recap" (pick a limited number of expert groups, then
+ * the top experts within them).
+ *  logits   device fp32 [T, E] row-major (finite values).
+ *  topk_ids device int32 [T, k]: descending score, ties to the lower id.
+ *  topk_w   device fp32 [T, k]: softmax -- exp(l_j - l_max) renormalised
+ *           over the selected k; sigmoid -- sigmoid(l_j) / sum over the
+ *           selected k (computed in fp64, rounded once).
+ *  Group-limited (n_groups > 1, sigmoid or softmax scores): groups are E /
+ *  n_groups contiguous experts; a group's score is the fp64 sum of the
+ *  sigmoids of its group_topn largest logits; the topk_groups best groups
+ *  (ties: lower group id) are kept and the k experts are chosen among them.
+ *  Limits: 1 <= E <= 512, k <= 16.  ws may be NULL (no device errors). */
+moe_status moe_route(const float *logits, int64_t T, int32_t E, const moe_route_cfg *cfg,
+                     int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes,
+                     void *stream);
+
+/* Dispatch layout: map every assignment a = t*k + j to a physical slot and
+ * build the stable permutation into contiguous per-slot segments.
+ * "14. Serving Mixture-of-Experts Models", "Follow one token", step 1 (a
+ * permutation built from a histogram over the expert ids into contiguous
+ * per-expert segments) and step 2 (each row goes to the rank that owns the
+ * expert); replica choice per "The network topology is visible in every MoE
+ * layer" (prefer a copy on the token's own node, else spread).
+ *  Slot rule: one copy -> its slot; several -> the lowest-rank copy on the
+ *  node of the token's source rank, else copy (t mod n_copies).
+ *  Outputs (device int32, caller-allocated):
+ *   slot[A]            slot of each assignment;
+ *   seg_counts[S]      assignments per slot (histogram);
+ *   seg_offsets[S+1]   exclusive prefix sum of seg_counts;
+ *   dest_row[A]        row of assignment a in the dispatched buffer:
+ *                      seg_offsets[slot[a]] + #{a' < a : slot[a'] == slot[a]};
+ *   src_assign[A]      inverse permutation: src_assign[dest_row[a]] == a;
+ *   rank_counts[R]     assignments per simulated rank.
+ *  Device errors: MOE_ERR_DEVICE_INDEX (expert id outside [0,E)),
+ *  MOE_ERR_PLACEMENT (tables inconsistent), MOE_ERR_DEVICE_TIMEOUT.
+ *  Limits: n_slots <= 1024, T*k < 2^31.  ws: moe_workspace_size(T,k,S). */
+moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k,
+                               const moe_placement *placement, int32_t *slot,
+                               int32_t *seg_counts, int32_t *seg_offsets,
+                               int32_t *dest_row, int32_t *src_assign,
+                               int32_t *rank_counts, void *ws, size_t ws_bytes,
+                               void *stream);
+
+/* Permute: x_perm[dest_row[t*k + j], :] = x[t, :] for every j (a byte
+ * copy).  "14. Serving Mixture-of-Experts Models", "Price one dispatch"
+ * (each assignment carries its token's hidden row: 2 * H bytes).
+ *  x       device bf16 [T, H];  x_perm device bf16 [T*k, H].
+ *  Limits: H % 8 == 0.  Rows whose dest_row is out of range are skipped and
+ *  reported as MOE_ERR_DEVICE_INDEX. */
+moe_status moe_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                       const int32_t *dest_row, uint16_t *x_perm, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* Grouped SwiGLU expert FFN over contiguous segments.  "14. Serving
+ * Mixture-of-Experts Models", "Follow one token", step 3 (a grouped matrix
+ * multiplication: one kernel processes every expert's segment with its own
+ * row count); "Mixture-of-Experts Inference", "Optimized kernels for MoE"
+ * (grouped GEMM, contiguous layout).  For segment s with expert
+ * e = seg_expert[s] and rows [seg_offsets[s], seg_offsets[s+1]):
+ *     G = X Wg_e^T,  U = X Wu_e^T            (fp32 accumulation)
+ *     h = bf16(silu(G) * U),  silu(g) = g / (1 + e^-g)   (fp32)
+ *     y = bf16(h Wd_e^T)                     (fp32 accumulation)
+ *  x_perm     device bf16 [n_rows, H]
+ *  seg_offsets device int32 [S+1], non-decreasing, seg_offsets[S] <= n_rows
+ *  seg_expert device int32 [S], values in [0, E)
+ *  w_gate_up  device bf16 [E, 2I, H]: rows 0..I-1 gate, I..2I-1 up (K-major)
+ *  w_down     device bf16 [E, H, I] (K-major)
+ *  h          device bf16 [n_rows, I] (intermediate, written)
+ *  y_perm     device bf16 [n_rows, H]
+ *  Rows outside every segment are left unwritten.  Uses tcgen05 tensor
+ *  cores with TMA-fed shared memory and TMEM accumulators.
+ *  Limits: H % 256 == 0, I % 128 == 0, S <= 1024, n_rows < 2^31.
+ *  Device errors: MOE_ERR_DEVICE_INDEX (expert id), MOE_ERR_DEVICE_TIMEOUT. */
+moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_offsets,
+                           const int32_t *seg_expert, int32_t S, int32_t E,
+                           const uint16_t *w_gate_up, const uint16_t *w_down, int32_t H,
+                           int32_t I, uint16_t *h, uint16_t *y_perm, void *ws,
+                           size_t ws_bytes, void *stream);
+
+/* Combine: y[t] = bf16(acc) with acc = shared[t] (or 0) and, for j = 0..k-1
+ * in order, acc = fmaf(topk_w[t,j], y_perm[dest_row[t*k+j]], acc) in fp32.
+ * "14. Serving Mixture-of-Experts Models", "Follow one token", step 4 (the
+ * inverse permutation followed by a weighted sum); shared experts per
+ * "Mixture-of-Experts Inference", "MoE architecture recap" (they process
+ * every token; weight one here).
+ *  y_perm device bf16 [T*k, H]; topk_w device fp32 [T, k];
+ *  shared device bf16 [T, H] or NULL; y device bf16 [T, H].
+ *  Limits: H % 8 == 0. */
+moe_status moe_combine(const uint16_t *y_perm, const int32_t *dest_row, const float *topk_w,
+                       int64_t T, int32_t k, int32_t H, const uint16_t *shared, uint16_t *y,
+                       void *ws, size_t ws_bytes, void *stream);
+
+/* Balancedness of one step: mean per-rank load over the busiest rank's
+ * load, total / (R * max) in fp64; 1.0 when total is 0.  "14. Serving
+ * Mixture-of-Experts Models", "The slowest expert sets the pace" (loads
+ * count assignments, "Price one dispatch").
+ *  rank_counts device int32 [R]; outputs are device scalars.
+ *  ws may be NULL. */
+moe_status moe_balance_stats(const int32_t *rank_counts, int32_t R, double *balancedness,
+                             int32_t *max_count, int64_t *total, void *ws, size_t ws_bytes,
+                             void *stream);
+
+/* Static text for a status code. */
+const char *moe_status_string(moe_status status);
+
+/* Library version string. */
+const char *moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads without a GPU, exports every entry point
+that include/moe.h declares, and rejects bad host-side arguments before any
+CUDA call.  CPU only: no kernel is launched here."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from grouped_ffn_gb300 import build, moe
+    build.build()
+    return moe.lib()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"moe_route", "moe_dispatch_layout", "moe_permute", "moe_grouped_ffn",
+            "moe_combine", "moe_balance_stats"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert b"sm_103a" in lib.moe_version()
+
+
+def test_status_strings(lib):
+    from grouped_ffn_gb300 import moe
+    for code, name in moe.STATUS_NAMES.items():
+        s = moe.moe_status_string(code)
+        assert s and s != "unknown status", name
+    assert moe.moe_status_string(99) == "unknown status"
+
+
+def test_workspace_size(lib):
+    from grouped_ffn_gb300 import moe
+    # status block + ticket block + one 32-bit flag per (4096-assignment tile, slot)
+    assert moe.moe_workspace_size(4000, 2, 64) == 512 + 2 * 64 * 4
+    assert moe.moe_workspace_size(16384, 4, 40) == 512 + 16 * 40 * 4
+    assert moe.moe_workspace_size(0, 2, 64) == 512 + 64 * 4
+    assert moe.moe_workspace_size(-1, 2, 64) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: validation fails first
+
+
+def test_host_validation_rejects_before_any_launch(lib):
+    from grouped_ffn_gb300 import moe
+    cfg = moe.RouteCfg(0, 2, 1, 1, 1)
+    assert lib.moe_route(FAKE, -1, 64, ctypes.byref(cfg), FAKE, FAKE, None, 0, None) == 1
+    assert lib.moe_route(FAKE, 8, 600, ctypes.byref(cfg), FAKE, FAKE, None, 0, None) == 2
+    bad_k = moe.RouteCfg(0, 70, 1, 1, 1)
+    assert lib.moe_route(FAKE, 8, 64, ctypes.byref(bad_k), FAKE, FAKE, None, 0, None) == 1
+    grouped_softmax = moe.RouteCfg(0, 8, 8, 4, 2)
+    assert lib.moe_route(FAKE, 8, 256, ctypes.byref(grouped_softmax), FAKE, FAKE, None, 0, None) == 2
+    too_many_groups_kept = moe.RouteCfg(1, 8, 8, 9, 2)
+    assert lib.moe_route(FAKE, 8, 256, ctypes.byref(too_many_groups_kept), FAKE, FAKE, None, 0, None) == 1
+    assert lib.moe_route(None, 8, 64, ctypes.byref(cfg), FAKE, FAKE, None, 0, None) == 1
+    # permute / combine: H must be a multiple of 8, workspace required
+    assert lib.moe_permute(FAKE, 8, 12, 2, FAKE, FAKE, FAKE, 256, None) == 2
+    assert lib.moe_permute(FAKE, 8, 256, 2, FAKE, FAKE, None, 0, None) == 6
+    assert lib.moe_permute(ctypes.c_void_p(0x10008), 8, 256, 2, FAKE, FAKE, FAKE, 256, None) == 1
+    assert lib.moe_combine(FAKE, FAKE, FAKE, 8, 17, 256, None, FAKE, FAKE, 256, None) == 2
+    # grouped FFN: H % 256, I % 128, segment count limit
+    args = lambda H, I, S: (FAKE, 16, FAKE, FAKE, S, 64, FAKE, FAKE, H, I, FAKE, FAKE, FAKE, 256, None)
+    assert lib.moe_grouped_ffn(*args(300, 128, 64)) == 2
+    assert lib.moe_grouped_ffn(*args(256, 96, 64)) == 2
+    assert lib.moe_grouped_ffn(*args(256, 128, 2000)) == 2
+    assert lib.moe_grouped_ffn(*args(256, 128, 0)) == 1
+    # layout: slot limit, workspace size
+    pl = moe.PlacementC(64, 2000, 8, 8, FAKE.value, FAKE.value, FAKE.value, FAKE.value, None)
+    assert lib.moe_dispatch_layout(FAKE, 8, 2, ctypes.byref(pl), FAKE, FAKE, FAKE, FAKE, FAKE,
+                                   FAKE, FAKE, 1 << 20, None) == 2
+    pl = moe.PlacementC(64, 64, 8, 8, FAKE.value, FAKE.value, FAKE.value, FAKE.value, None)
+    assert lib.moe_dispatch_layout(FAKE, 8, 2, ctypes.byref(pl), FAKE, FAKE, FAKE, FAKE, FAKE,
+                                   FAKE, FAKE, 256, None) == 6
+    assert lib.moe_balance_stats(FAKE, 0, FAKE, FAKE, FAKE, None, 0, None) == 1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    from grouped_ffn_gb300 import moe
+    with pytest.raises(TypeError):
+        moe.moe_route(torch.zeros(4, 8), moe.RouteCfg(0, 2, 1, 1, 1),
+                      torch.zeros(4, 2, dtype=torch.int32), torch.zeros(4, 2))

@@ -1,0 +1,443 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Bit-exact: expert ids, slots, counts, offsets, permutation indices, rank
+counts, balancedness, permuted rows, and the combine given the same expert
+outputs (its fp32 fma order is fixed).  Floating outputs: relative
+Frobenius error <= 1e-2 and, per row, max |err| / rms(reference row) <= 2e-2;
+router weights within 1e-6 relative of fp64.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+FROB_TOL = 1e-2
+ROW_TOL = 2e-2
+W_RTOL = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from grouped_ffn_gb300 import build
+    build.build()
+    oracle.build_c()
+    torch.cuda.set_device(0)
+
+
+def moe():
+    from grouped_ffn_gb300 import moe as m
+    return m
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return oracle.bf16_bits_to_f64(bits(t))
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, what: str):
+    got = np.asarray(got, np.float64).reshape(ref.shape[0], -1)
+    ref = np.asarray(ref, np.float64).reshape(ref.shape[0], -1)
+    nrm = np.linalg.norm(ref)
+    rel = np.linalg.norm(got - ref) / max(nrm, 1e-300)
+    rms = np.sqrt(np.mean(ref ** 2, axis=1))
+    err = np.max(np.abs(got - ref), axis=1)
+    row = np.where(rms > 0, err / np.where(rms > 0, rms, 1), err)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    assert rel <= FROB_TOL, f"{what}: rel Frobenius {rel:.3e}"
+    assert row.max() <= ROW_TOL, f"{what}: per-row max/rms {row.max():.3e} at row {row.argmax()}"
+    return rel, row.max()
+
+
+def route_cfg(w):
+    return moe().RouteCfg(w.score_fn, w.k, w.n_groups, w.topk_groups, w.group_topn)
+
+
+def oracle_route(w, logits_np):
+    if w.score_fn == wl.SCORE_SOFTMAX and w.n_groups == 1:
+        ids, wts = oracle.route_softmax_topk(logits_np, w.k)
+        return ids, wts, np.inf
+    return oracle.route_group_limited(logits_np, w.k, w.n_groups, w.topk_groups, w.group_topn)
+
+
+def gpu_route(w, logits):
+    ids = torch.empty(w.T, w.k, dtype=torch.int32, device="cuda")
+    wts = torch.empty(w.T, w.k, dtype=torch.float32, device="cuda")
+    moe().moe_route(logits, route_cfg(w), ids, wts)
+    return ids, wts
+
+
+def gpu_layout(ids, pl_dev, T, k, ws=None):
+    A = T * k
+    m = moe()
+    if ws is None:
+        ws = m.new_workspace(T, k, pl_dev.n_slots)
+    i32 = lambda n: torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    out = dict(slot=i32(A), seg_counts=i32(pl_dev.n_slots), seg_offsets=i32(pl_dev.n_slots + 1),
+               dest_row=i32(A), src_assign=i32(A), rank_counts=i32(pl_dev.n_ranks))
+    m.moe_dispatch_layout(ids, pl_dev, out["slot"], out["seg_counts"], out["seg_offsets"],
+                          out["dest_row"], out["src_assign"], out["rank_counts"], ws)
+    m.moe_check_device_status(ws)
+    return {k_: v.cpu().numpy() for k_, v in out.items()}
+
+
+ALL = ["tiny", "decode", "prefill", "group_limited", "replica"]
+
+
+# ------------------------------------------------------------------ route
+@pytest.mark.parametrize("name,zipf", [(n, None) for n in ALL] +
+                         [("replica", s) for s in (0.0, 0.5, 1.5)])
+def test_route_parity(name, zipf):
+    w = wl.WORKLOADS[name]
+    if zipf is not None:
+        w = w.with_zipf(zipf)
+    logits = wl.make_logits(w, "cuda")
+    ids, wts = gpu_route(w, logits)
+    rid, rw, margin = oracle_route(w, logits.cpu().numpy())
+    assert np.array_equal(ids.cpu().numpy(), rid), f"ids differ (min group margin {margin:.2e})"
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
+
+
+@pytest.mark.parametrize("E,k,score", [(40, 40, 0), (33, 3, 0), (512, 16, 0), (64, 4, 1), (1, 1, 0)])
+def test_route_shapes_and_ties(E, k, score):
+    rng = np.random.default_rng(E * 31 + k)
+    T = 257
+    vals = np.array([-1.0, -0.0, 0.0, 0.5, 1.0], np.float32)
+    lg = rng.choice(vals, size=(T, E)).astype(np.float32)     # many exact ties, signed zeros
+    lg[: T // 2] = rng.standard_normal((T // 2, E)).astype(np.float32)
+    w = wl.Workload("t", 0, T=T, H=8, E=E, k=k, I=8, R=1, ranks_per_node=1, score_fn=score)
+    ids, wts = gpu_route(w, torch.from_numpy(lg).cuda())
+    rid, rw, _ = oracle_route(w, lg)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
+
+
+def test_route_group_limited_small_groups():
+    rng = np.random.default_rng(3)
+    for n_groups, E, topk_groups, topn, k in [(4, 64, 2, 3, 5), (32, 128, 3, 1, 4), (2, 40, 1, 2, 6)]:
+        w = wl.Workload("g", 0, T=300, H=8, E=E, k=k, I=8, R=1, ranks_per_node=1,
+                        score_fn=wl.SCORE_SIGMOID, n_groups=n_groups, topk_groups=topk_groups,
+                        group_topn=topn)
+        lg = rng.standard_normal((w.T, E)).astype(np.float32)
+        ids, wts = gpu_route(w, torch.from_numpy(lg).cuda())
+        rid, rw, _ = oracle_route(w, lg)
+        assert np.array_equal(ids.cpu().numpy(), rid)
+        np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
+
+
+# ------------------------------------------------------------------ layout + balance
+@pytest.mark.parametrize("name,zipf", [(n, None) for n in ALL] +
+                         [("replica", s) for s in (0.0, 0.5, 1.5)])
+def test_layout_and_balance_parity(name, zipf):
+    w = wl.WORKLOADS[name]
+    if zipf is not None:
+        w = w.with_zipf(zipf)
+    pl = wl.make_placement(w)
+    pl_dev = moe().DevicePlacement.from_tables(pl)
+    ids, _ = gpu_route(w, wl.make_logits(w, "cuda"))
+    ids_np = ids.cpu().numpy()
+    got = gpu_layout(ids, pl_dev, w.T, w.k)
+    ref = oracle.dispatch_layout(ids_np, pl)
+    for key in ("slot", "seg_counts", "seg_offsets", "dest_row", "src_assign", "rank_counts"):
+        assert np.array_equal(got[key], ref[key]), key
+    b = torch.empty(1, dtype=torch.float64, device="cuda")
+    mx = torch.empty(1, dtype=torch.int32, device="cuda")
+    tot = torch.empty(1, dtype=torch.int64, device="cuda")
+    moe().moe_balance_stats(torch.from_numpy(got["rank_counts"]).cuda(), b, mx, tot)
+    assert (b.item(), mx.item(), tot.item()) == oracle.balance_stats(ref["rank_counts"])
+
+
+def test_layout_many_tiles_many_slots_and_ragged_tail():
+    # 25 tiles of 4096 assignments (the last one ragged), 1024 slots on 256 ranks
+    T, k, E, R = 51111, 2, 1024, 256
+    rng = np.random.default_rng(11)
+    ids_np = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    ids_np[:, 1] = (ids_np[:, 0] + 1 + rng.integers(0, E - 1, size=T)) % E
+    pl = wl.placement_from_hosts(E, R, 4, wl.round_robin_hosts(E, R))
+    got = gpu_layout(torch.from_numpy(ids_np).cuda(), moe().DevicePlacement.from_tables(pl), T, k)
+    ref = oracle.dispatch_layout(ids_np, pl)
+    for key in ref:
+        assert np.array_equal(got[key], ref[key]), key
+
+
+def test_layout_empty_and_single_token():
+    pl = wl.make_placement(wl.WORKLOADS["tiny"])
+    pl_dev = moe().DevicePlacement.from_tables(pl)
+    got = gpu_layout(torch.empty(0, 2, dtype=torch.int32, device="cuda"), pl_dev, 0, 2)
+    assert np.all(got["seg_counts"] == 0) and np.all(got["seg_offsets"] == 0)
+    assert np.all(got["rank_counts"] == 0)
+    one = np.array([[5, 63]], np.int32)
+    got = gpu_layout(torch.from_numpy(one).cuda(), pl_dev, 1, 2)
+    ref = oracle.dispatch_layout(one, pl)
+    for key in ref:
+        assert np.array_equal(got[key], ref[key]), key
+
+
+def test_layout_is_deterministic_run_to_run():
+    w = wl.WORKLOADS["replica"]
+    pl_dev = moe().DevicePlacement.from_tables(wl.make_placement(w))
+    ids, _ = gpu_route(w, wl.make_logits(w, "cuda"))
+    a = gpu_layout(ids, pl_dev, w.T, w.k)
+    b = gpu_layout(ids, pl_dev, w.T, w.k)
+    for key in a:
+        assert np.array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("case", ["contiguous_pairs", "repack", "replicate_e0_on_rank3"])
+def test_worked_example_on_gpu(case):
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "worked_example_balance.json")) as f:
+        g = json.load(f)
+    cs = g["cases"][case]
+    ids_np = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(g["expert_counts"])])[:, None]
+    T = ids_np.shape[0]
+    if case == "replicate_e0_on_rank3":
+        src = np.zeros(T, np.int32)
+        src[np.nonzero(ids_np[:, 0] == 0)[0][1::2]] = 3
+        pl = wl.placement_from_hosts(8, 4, 1, cs["hosts"], token_src_rank=src)
+    else:
+        pl = wl.placement_from_hosts(8, 4, 4, cs["hosts"])
+    got = gpu_layout(torch.from_numpy(ids_np).cuda(), moe().DevicePlacement.from_tables(pl), T, 1)
+    assert list(got["rank_counts"]) == cs["rank_loads"]
+    b = torch.empty(1, dtype=torch.float64, device="cuda")
+    mx = torch.empty(1, dtype=torch.int32, device="cuda")
+    tot = torch.empty(1, dtype=torch.int64, device="cuda")
+    moe().moe_balance_stats(torch.from_numpy(got["rank_counts"]).cuda(), b, mx, tot)
+    assert b.item() == cs["balancedness_num"] / cs["balancedness_den"]
+
+
+def test_layout_reports_bad_expert_id_without_faulting():
+    m = moe()
+    pl = wl.make_placement(wl.WORKLOADS["tiny"])
+    pl_dev = m.DevicePlacement.from_tables(pl)
+    ids = torch.tensor([[1, 2], [3, 64], [5, -1]], dtype=torch.int32, device="cuda")
+    ws = m.new_workspace(3, 2, pl_dev.n_slots)
+    A = 6
+    o = [torch.zeros(n, dtype=torch.int32, device="cuda") for n in (A, 64, 65, A, A, 8)]
+    m.moe_dispatch_layout(ids, pl_dev, *o, ws)
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_check_device_status(ws)
+    assert ei.value.status == 4
+    m.moe_check_device_status(ws)   # cleared after reading
+
+
+# ------------------------------------------------------------------ permute / combine
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill"])
+def test_permute_bit_exact(name):
+    w = wl.WORKLOADS[name]
+    m = moe()
+    pl = wl.make_placement(w)
+    ids, _ = gpu_route(w, wl.make_logits(w, "cuda"))
+    lay = oracle.dispatch_layout(ids.cpu().numpy(), pl)
+    x = wl.make_x(w, "cuda")
+    xp = torch.empty(w.A, w.H, dtype=torch.bfloat16, device="cuda")
+    ws = m.new_workspace(w.T, w.k, pl.n_slots)
+    m.moe_permute(x, w.k, torch.from_numpy(lay["dest_row"]).cuda(), xp, ws)
+    m.moe_check_device_status(ws)
+    assert np.array_equal(bits(xp), oracle.permute(bits(x), lay["dest_row"], w.k))
+
+
+@pytest.mark.parametrize("k,H,shared", [(2, 256, False), (4, 4096, False), (8, 7168, True),
+                                        (3, 136, True), (16, 64, False)])
+def test_combine_bit_exact(k, H, shared):
+    m = moe()
+    T = 333
+    g = torch.Generator(device="cuda").manual_seed(k * 1000 + H)
+    yp = torch.randn(T * k, H, generator=g, device="cuda").to(torch.bfloat16)
+    sh = torch.randn(T, H, generator=g, device="cuda").to(torch.bfloat16) if shared else None
+    dr = torch.randperm(T * k, generator=g, device="cuda").to(torch.int32)
+    wts = torch.rand(T, k, generator=g, device="cuda")
+    y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    ws = m.new_workspace(T, k, 1)
+    m.moe_combine(yp, dr, wts, y, ws, sh)
+    m.moe_check_device_status(ws)
+    ref = oracle.combine_fma32(bits(yp), dr.cpu().numpy(), wts.cpu().numpy(),
+                               None if sh is None else bits(sh))
+    assert np.array_equal(bits(y), ref)
+
+
+def test_permute_then_combine_one_hot_is_identity():
+    m = moe()
+    w = wl.WORKLOADS["replica"]
+    pl = wl.make_placement(w)
+    pl_dev = m.DevicePlacement.from_tables(pl)
+    ids, _ = gpu_route(w, wl.make_logits(w, "cuda"))
+    ws = m.new_workspace(w.T, w.k, pl.n_slots)
+    dest = torch.empty(w.A, dtype=torch.int32, device="cuda")
+    scratch = [torch.empty(n, dtype=torch.int32, device="cuda") for n in (w.A, pl.n_slots, pl.n_slots + 1)]
+    src = torch.empty(w.A, dtype=torch.int32, device="cuda")
+    rc = torch.empty(w.R, dtype=torch.int32, device="cuda")
+    m.moe_dispatch_layout(ids, pl_dev, scratch[0], scratch[1], scratch[2], dest, src, rc, ws)
+    x = wl.make_x(w, "cuda")
+    xp = torch.empty(w.A, w.H, dtype=torch.bfloat16, device="cuda")
+    m.moe_permute(x, w.k, dest, xp, ws)
+    onehot = torch.zeros(w.T, w.k, device="cuda")
+    onehot[:, w.k - 1] = 1.0
+    y = torch.empty_like(x)
+    m.moe_combine(xp, dest, onehot, y, ws)
+    m.moe_check_device_status(ws)
+    assert torch.equal(y, x)
+
+
+# ------------------------------------------------------------------ grouped FFN
+def _ffn_case(w, offsets, seg_expert, dev="cuda"):
+    m = moe()
+    n_rows = int(offsets[-1]) + 37          # rows past the last segment stay unwritten
+    g = torch.Generator(device=dev).manual_seed(w.index)
+    xp = torch.randn(n_rows, w.H, generator=g, device=dev).to(torch.bfloat16)
+    wgu = wl.make_w_gate_up(w, dev)
+    wd = wl.make_w_down(w, dev)
+    h = torch.full((n_rows, w.I), float("nan"), dtype=torch.bfloat16, device=dev)
+    yp = torch.full((n_rows, w.H), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = m.new_workspace(1, 1, 1)
+    offs_t = torch.tensor(offsets, dtype=torch.int32, device=dev)
+    exp_t = torch.tensor(seg_expert, dtype=torch.int32, device=dev)
+    m.moe_grouped_ffn(xp, offs_t, exp_t, wgu, wd, h, yp, ws)
+    m.moe_check_device_status(ws)
+    rh, ry = oracle.grouped_ffn(f64(xp[: offsets[-1]]), np.array(offsets), np.array(seg_expert),
+                                oracle.bf16_bits_to_f64(bits(wgu)), oracle.bf16_bits_to_f64(bits(wd)),
+                                w.I)
+    return h, yp, rh, ry, n_rows
+
+
+@pytest.mark.parametrize("H,I,counts", [
+    (256, 128, [3, 0, 5, 8]),                          # tiny layer shape, fewer rows than a tile
+    (512, 384, [130, 1, 0, 257, 128, 75, 300, 12]),    # several tiles, ragged tails, empty
+    (768, 256, [600]),                                 # one segment = a dense GEMM
+    (256, 640, [129, 127, 2, 64]),
+])
+def test_grouped_ffn_small_full_compare(H, I, counts):
+    E = len(counts) + 1
+    w = wl.Workload("ffn", 50 + H // 256 + I, T=1, H=H, E=E, k=1, I=I, R=1, ranks_per_node=1)
+    offsets = [0]
+    for c in counts:
+        offsets.append(offsets[-1] + c)
+    seg_expert = [(3 * s + 1) % E for s in range(len(counts))]
+    h, yp, rh, ry, n_rows = _ffn_case(w, offsets, seg_expert)
+    A = offsets[-1]
+    assert_close(f64(h[:A]), rh, "h")
+    assert_close(f64(yp[:A]), ry, "y_perm")
+    assert torch.isnan(yp[A:].float()).all() and torch.isnan(h[A:].float()).all()
+
+
+def _sample_rows(seg_offsets, rng, n=48):
+    A = int(seg_offsets[-1])
+    rows = set(rng.choice(A, size=min(n, A), replace=False).tolist())
+    for s in range(len(seg_offsets) - 1):      # first and last row of some segments
+        lo, hi = int(seg_offsets[s]), int(seg_offsets[s + 1])
+        if hi > lo and len(rows) < 2 * n:
+            rows.update([lo, hi - 1])
+    return np.array(sorted(rows))
+
+
+class _LazyExperts:
+    """Copies one expert's weights to the host on first use."""
+
+    def __init__(self, t):
+        self.t, self.cache = t, {}
+
+    def __getitem__(self, e):
+        if e not in self.cache:
+            self.cache[e] = oracle.bf16_bits_to_f64(bits(self.t[e]))
+        return self.cache[e]
+
+
+def _full_layer(w, dev="cuda"):
+    from grouped_ffn_gb300 import MoELayer
+    m = moe()
+    pl = wl.make_placement(w)
+    logits = wl.make_logits(w, dev)
+    x = wl.make_x(w, dev)
+    wgu = wl.make_w_gate_up(w, dev)
+    wd = wl.make_w_down(w, dev)
+    sgu, sd = wl.make_shared_weights(w, dev)
+    layer = MoELayer(H=w.H, I=w.I, E=w.E, k=w.k, placement=m.DevicePlacement.from_tables(pl, dev),
+                     w_gate_up=wgu, w_down=wd, max_tokens=w.T, score_fn=w.score_fn,
+                     n_groups=w.n_groups, topk_groups=w.topk_groups, group_topn=w.group_topn,
+                     shared_w_gate_up=sgu, shared_w_down=sd, device=dev)
+    y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
+    layer.forward(logits, x, y)
+    layer.check()
+    torch.cuda.synchronize()
+    return pl, logits, x, wgu, wd, sgu, sd, layer, y
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "group_limited", "replica"])
+def test_full_layer_sampled(name):
+    """Full-size layer in the configuration the benchmark times: every
+    integer output bit-exact, FFN rows and combined tokens sampled against
+    the oracle, and the combine bit-exact given the GPU's expert outputs."""
+    w = wl.WORKLOADS[name]
+    pl, logits, x, wgu, wd, sgu, sd, layer, y = _full_layer(w)
+    A = w.A
+    ids_ref, _, _ = oracle_route(w, logits.cpu().numpy())
+    assert np.array_equal(layer.topk_ids.cpu().numpy(), ids_ref)
+    lay = oracle.dispatch_layout(ids_ref, pl)
+    for key in ("seg_counts", "seg_offsets", "rank_counts"):
+        assert np.array_equal(getattr(layer, key).cpu().numpy(), lay[key]), key
+    assert np.array_equal(layer.dest_row[:A].cpu().numpy(), lay["dest_row"])
+    assert np.array_equal(layer.src_assign[:A].cpu().numpy(), lay["src_assign"])
+    rng = np.random.default_rng(w.index)
+    # sampled rows of the grouped FFN (x_perm -> h, y_perm)
+    rows = _sample_rows(lay["seg_offsets"], rng)
+    xp_rows = f64(layer.x_perm[torch.from_numpy(rows).cuda()])
+    lazy_gu, lazy_d = _LazyExperts(wgu), _LazyExperts(wd)
+    full_x = np.zeros((int(rows.max()) + 1, w.H))
+    full_x[rows] = xp_rows
+    rh, ry = oracle.grouped_ffn(full_x, lay["seg_offsets"], pl.slot_expert, lazy_gu, lazy_d, w.I,
+                                rows=rows)
+    assert_close(f64(layer.h[torch.from_numpy(rows).cuda()]), rh, "h rows")
+    assert_close(f64(layer.y_perm[torch.from_numpy(rows).cuda()]), ry, "y_perm rows")
+    # combine bit-exact from the GPU's own expert outputs
+    shared_bits = bits(layer.shared_y[: w.T]) if w.shared_I else None
+    ref_y = oracle.combine_fma32(bits(layer.y_perm[:A]), lay["dest_row"],
+                                 layer.topk_w[: w.T].cpu().numpy(), shared_bits)
+    assert np.array_equal(bits(y), ref_y)
+    # whole layer on sampled tokens, from the definition
+    toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, size=min(12, w.T), replace=False)]))
+    cfg = dict(score_fn=w.score_fn, k=w.k, n_groups=w.n_groups, topk_groups=w.topk_groups,
+               group_topn=w.group_topn)
+    shared = None if sgu is None else (bits(sgu[0]), bits(sd[0]))
+    ref = oracle.moe_layer_tokens(toks, logits.cpu().numpy(), bits(x), _BitsExperts(wgu),
+                                  _BitsExperts(wd), pl, cfg, shared_w=shared, I=w.I,
+                                  shared_I=w.shared_I)
+    assert_close(f64(y[torch.from_numpy(toks).cuda()]), ref, "layer output")
+    bal, mx, tot = oracle.balance_stats(lay["rank_counts"])
+    assert layer.balancedness.item() == bal and layer.max_count.item() == mx
+    assert layer.total.item() == tot == A
+
+
+class _BitsExperts:
+    """Copies one expert's bf16 bits to the host on first use."""
+
+    def __init__(self, t):
+        self.t, self.cache = t, {}
+
+    def __getitem__(self, e):
+        if e not in self.cache:
+            self.cache[e] = bits(self.t[e])
+        return self.cache[e]
+
+
+def test_shared_expert_alone_matches_dense_definition():
+    """The shared expert is one segment covering every token."""
+    w = wl.WORKLOADS["group_limited"].scaled(T=200, H=512, I=256, shared_I=256, E=8)
+    m = moe()
+    x = wl.make_x(w, "cuda")
+    sgu, sd = wl.make_shared_weights(w, "cuda")
+    h = torch.empty(w.T, w.shared_I, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    ws = m.new_workspace(1, 1, 1)
+    m.moe_grouped_ffn(x, torch.tensor([0, w.T], dtype=torch.int32, device="cuda"),
+                      torch.zeros(1, dtype=torch.int32, device="cuda"), sgu, sd, h, y, ws)
+    m.moe_check_device_status(ws)
+    rh, ry = oracle.swiglu_expert(f64(x), f64(sgu[0]), f64(sd[0]), w.shared_I)
+    assert_close(f64(y), ry, "shared y")
