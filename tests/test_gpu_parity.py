@@ -3,8 +3,9 @@
 Bit-exact: expert ids, slots, counts, offsets, permutation indices, rank
 counts, balancedness, permuted rows, and the combine given the same expert
 outputs (its fp32 fma order is fixed).  Floating outputs: relative
-Frobenius error <= 1e-2 and, per row, max |err| / rms(reference row) <= 2e-2;
-router weights within 1e-6 relative of fp64.
+Frobenius error <= 1e-2 and, after normalising each row by its largest
+|reference| value, max |err| <= 2e-2; router weights within 1e-6 relative
+of fp64.
 """
 
 import numpy as np
@@ -47,12 +48,12 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str):
     ref = np.asarray(ref, np.float64).reshape(ref.shape[0], -1)
     nrm = np.linalg.norm(ref)
     rel = np.linalg.norm(got - ref) / max(nrm, 1e-300)
-    rms = np.sqrt(np.mean(ref ** 2, axis=1))
+    scale = np.max(np.abs(ref), axis=1)
     err = np.max(np.abs(got - ref), axis=1)
-    row = np.where(rms > 0, err / np.where(rms > 0, rms, 1), err)
+    row = np.where(scale > 0, err / np.where(scale > 0, scale, 1), err)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     assert rel <= FROB_TOL, f"{what}: rel Frobenius {rel:.3e}"
-    assert row.max() <= ROW_TOL, f"{what}: per-row max/rms {row.max():.3e} at row {row.argmax()}"
+    assert row.max() <= ROW_TOL, f"{what}: per-row normalised max err {row.max():.3e} at row {row.argmax()}"
     return rel, row.max()
 
 
@@ -105,7 +106,7 @@ def test_route_parity(name, zipf):
     np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
 
 
-@pytest.mark.parametrize("E,k,score", [(40, 40, 0), (33, 3, 0), (512, 16, 0), (64, 4, 1), (1, 1, 0)])
+@pytest.mark.parametrize("E,k,score", [(40, 16, 0), (33, 3, 0), (512, 16, 0), (64, 4, 1), (1, 1, 0), (16, 16, 1)])
 def test_route_shapes_and_ties(E, k, score):
     rng = np.random.default_rng(E * 31 + k)
     T = 257
