@@ -20,6 +20,7 @@
 //    seg_offsets (exclusive scan) and rank_counts; the finalize kernel adds
 //    seg_offsets to every partial rank and writes the inverse permutation.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -289,6 +290,117 @@ extern "C" moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, in
   p.tile_flags = reinterpret_cast<uint32_t *>(wsb + kFlagsOff);
   p.ticket = reinterpret_cast<int32_t *>(wsb + kTicketOff);
   p.status = moe_host::status_ptr(ws);
+  p.n_tiles = (int32_t)n_tiles;
+
+  const size_t smem = ((size_t)(kWarps + 2) * p.S + p.R) * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(layout_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  layout_scan_kernel<<<(unsigned)n_tiles, kThreads, smem, st>>>(p);
+  if (moe_status s = moe_host::launch_status()) return s;
+  if (A > 0) {
+    int64_t blocks = (A + 255) / 256;
+    const int64_t cap = (int64_t)moe_host::sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    layout_finalize_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+    if (moe_status s = moe_host::launch_status()) return s;
+  }
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch layout for callers that cannot allocate device memory.
+//
+// Some callers have no way to obtain scratch memory at the point where they
+// run the layout: a serving engine that has already handed every free byte
+// of HBM to its weight and KV-cache pools, or a plugin hosted by another
+// runtime that neither passes it a workspace nor lets it call cudaMalloc
+// while that runtime is executing.  This entry point keeps the look-back
+// scratch (the tile ticket and one 32-bit flag per (4096-assignment tile,
+// slot)) in the fixed device array below instead of a caller workspace.
+//
+// The array is 1 MiB on every GPU that loads this library and stays there
+// until the process exits.  Host code may not pass its name to a kernel (on
+// the host it is only a stand-in symbol); the device address is looked up
+// once per device with cudaGetSymbolAddress and cached.
+static __device__ __align__(256) uint32_t g_layout_noalloc_scratch[262144];
+
+namespace {
+
+constexpr size_t kNoAllocWords = sizeof(g_layout_noalloc_scratch) / sizeof(uint32_t);
+constexpr size_t kNoAllocTicketWords = 64;  // ticket word, padded to 256 bytes
+
+// Device address of the scratch array on the current device; nullptr on a
+// CUDA error.  The first call on each device does the lookup.
+uint32_t *noalloc_scratch() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static uint32_t *addr[kMaxDevices] = {nullptr};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_layout_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return nullptr;
+    addr[dev] = static_cast<uint32_t *>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" moe_status moe_dispatch_layout_noalloc(const int32_t *topk_ids, int64_t T, int32_t k,
+                                                  const moe_placement *pl, int32_t *slot,
+                                                  int32_t *seg_counts, int32_t *seg_offsets,
+                                                  int32_t *dest_row, int32_t *src_assign,
+                                                  int32_t *rank_counts, int32_t *status,
+                                                  void *stream) {
+  if (pl == nullptr || T < 0 || k < 1) return MOE_ERR_INVALID_ARG;
+  const int64_t A = T * (int64_t)k;
+  if (A >= (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  if (pl->n_experts < 1 || pl->n_slots < 1 || pl->n_ranks < 1 || pl->ranks_per_node < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (pl->n_slots > kMaxSlots || pl->n_ranks > kMaxRanks) return MOE_ERR_UNSUPPORTED;
+  if (!pl->slot_expert || !pl->slot_rank || !pl->rep_offsets || !pl->rep_slots || !seg_counts ||
+      !seg_offsets || !rank_counts)
+    return MOE_ERR_INVALID_ARG;
+  if (A > 0 && (!topk_ids || !slot || !dest_row || !src_assign)) return MOE_ERR_INVALID_ARG;
+  const int64_t n_tiles = std::max<int64_t>(n_tiles_for(A), 1);
+  const size_t words = kNoAllocTicketWords + (size_t)n_tiles * (size_t)pl->n_slots;
+  if (words > kNoAllocWords) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch
+
+  uint32_t *scratch = noalloc_scratch();
+  if (scratch == nullptr) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The array keeps whatever the previous call left: clear the part used.
+  if (cudaMemsetAsync(scratch, 0, words * sizeof(uint32_t), st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+
+  LayoutArgs p{};
+  p.topk_ids = topk_ids;
+  p.A = A;
+  p.k = k;
+  p.E = pl->n_experts;
+  p.S = pl->n_slots;
+  p.R = pl->n_ranks;
+  p.rpn = pl->ranks_per_node;
+  p.slot_expert = pl->slot_expert;
+  p.slot_rank = pl->slot_rank;
+  p.rep_offsets = pl->rep_offsets;
+  p.rep_slots = pl->rep_slots;
+  p.token_src_rank = pl->token_src_rank;
+  p.slot = slot;
+  p.seg_counts = seg_counts;
+  p.seg_offsets = seg_offsets;
+  p.dest_row = dest_row;
+  p.src_assign = src_assign;
+  p.rank_counts = rank_counts;
+  p.ticket = reinterpret_cast<int32_t *>(scratch);
+  p.tile_flags = scratch + kNoAllocTicketWords;
+  p.status = status;
   p.n_tiles = (int32_t)n_tiles;
 
   const size_t smem = ((size_t)(kWarps + 2) * p.S + p.R) * sizeof(int32_t);

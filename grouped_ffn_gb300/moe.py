@@ -63,6 +63,8 @@ _SIGNATURES = {
     "moe_route": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(RouteCfg), _P, _P, _P, _SZ, _P]),
     "moe_dispatch_layout": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC),
                                            _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_dispatch_layout_noalloc": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC),
+                                                   _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_permute": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _I32, _I32,
                                        _P, _P, _P, _SZ, _P]),
@@ -193,6 +195,25 @@ def moe_dispatch_layout(topk_ids, placement: DevicePlacement, slot, seg_counts, 
         _ptr(topk_ids), T, k, ctypes.byref(placement.c), _ptr(slot), _ptr(seg_counts),
         _ptr(seg_offsets), _ptr(dest_row), _ptr(src_assign), _ptr(rank_counts), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def moe_dispatch_layout_noalloc(topk_ids, placement: DevicePlacement, slot, seg_counts,
+                                seg_offsets, dest_row, src_assign, rank_counts, status=None,
+                                stream=None):
+    """The layout with the library's fixed device scratch instead of a
+    workspace, for callers that cannot allocate; `status` is an optional
+    device int32[3] that receives device-side errors."""
+    for n, t in (("topk_ids", topk_ids), ("slot", slot), ("seg_counts", seg_counts),
+                 ("seg_offsets", seg_offsets), ("dest_row", dest_row),
+                 ("src_assign", src_assign), ("rank_counts", rank_counts)):
+        _need(t, torch.int32, n)
+    if status is not None:
+        _need(status, torch.int32, "status")
+    T, k = topk_ids.shape
+    _check("moe_dispatch_layout_noalloc", lib().moe_dispatch_layout_noalloc(
+        _ptr(topk_ids), T, k, ctypes.byref(placement.c), _ptr(slot), _ptr(seg_counts),
+        _ptr(seg_offsets), _ptr(dest_row), _ptr(src_assign), _ptr(rank_counts), _ptr(status),
+        _stream(stream)))
 
 
 def moe_permute(x, k: int, dest_row, x_perm, ws, stream=None):

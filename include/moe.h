@@ -154,6 +154,31 @@ moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k,
                                int32_t *rank_counts, void *ws, size_t ws_bytes,
                                void *stream);
 
+/* moe_dispatch_layout without a workspace: for callers that cannot
+ * allocate device memory when they run the layout, such as a serving engine
+ * that has handed all free HBM to its weight and KV-cache pools, or a plugin
+ * hosted by another runtime that gives it no workspace and does not let it
+ * call cudaMalloc.  The pages have no counterpart: this is a packaging
+ * variant of moe_dispatch_layout with identical inputs, outputs and results.
+ *  Scratch: a fixed 1 MiB device array inside the library (one per GPU that
+ *  loads it, held until the process exits).  Nothing is allocated per call:
+ *  no cudaMalloc, cudaFree or allocating library routine.
+ *  Limit: 64 + ceil(T*k / 4096) * n_slots <= 262144 (32-bit words);
+ *  larger requests return MOE_ERR_UNSUPPORTED without launching.
+ *  The first call on each device looks up the array's device address (with
+ *  that device current) and caches it; make that first call before any
+ *  stream capture.
+ *  Every call clears the part of the array it uses and then reuses it, and
+ *  all calls on one GPU share the array: calls that may overlap on the same
+ *  GPU (for example on two streams) race.  Order them on one stream.
+ *  status: device int32[3] (code, detail, kernel id) for device-side errors,
+ *  written like the workspace status word of the other calls; may be NULL. */
+moe_status moe_dispatch_layout_noalloc(const int32_t *topk_ids, int64_t T, int32_t k,
+                                       const moe_placement *placement, int32_t *slot,
+                                       int32_t *seg_counts, int32_t *seg_offsets,
+                                       int32_t *dest_row, int32_t *src_assign,
+                                       int32_t *rank_counts, int32_t *status, void *stream);
+
 /* Permute: x_perm[dest_row[t*k + j], :] = x[t, :] for every j (a byte
  * copy).  "14. Serving Mixture-of-Experts Models", "Price one dispatch"
  * (each assignment carries its token's hidden row: 2 * H bytes).

@@ -1,0 +1,70 @@
+"""moe_dispatch_layout_noalloc, the layout entry point for callers that
+cannot allocate device memory (for instance a serving engine whose free HBM
+is all promised to its weight and KV-cache pools, or a plugin run by another
+runtime that gives it no workspace and no cudaMalloc).  It must give exactly
+the results of moe_dispatch_layout, call after call, while its scratch lives
+in the library's fixed device array.  This file is collected last so that a
+stop-at-first-failure run has already run every other test."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from grouped_ffn_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+def _outputs(T, k, pl_dev):
+    A = T * k
+    mk = lambda n: torch.full((n,), -5, dtype=torch.int32, device="cuda")
+    return [mk(A), mk(pl_dev.n_slots), mk(pl_dev.n_slots + 1), mk(A), mk(A), mk(pl_dev.n_ranks)]
+
+
+def _ids(name, seed):
+    w = wl.WORKLOADS[name]
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    # random expert ids, distinct within a token
+    scores = torch.rand(w.T, w.E, generator=g, device="cuda")
+    ids = scores.topk(w.k, dim=1).indices.to(torch.int32).contiguous()
+    return w, ids
+
+
+@pytest.mark.parametrize("first,second", [("replica", "prefill"), ("group_limited", "tiny")])
+def test_noalloc_layout_matches_workspace_layout_on_consecutive_calls(first, second):
+    from grouped_ffn_gb300 import moe
+    for i, name in enumerate([first, second, first]):
+        w, ids = _ids(name, 100 + i)
+        pl_dev = moe.DevicePlacement.from_tables(wl.make_placement(w))
+        ws = moe.new_workspace(w.T, w.k, pl_dev.n_slots)
+        ref = _outputs(w.T, w.k, pl_dev)
+        moe.moe_dispatch_layout(ids, pl_dev, *ref, ws)
+        got = _outputs(w.T, w.k, pl_dev)
+        status = torch.zeros(3, dtype=torch.int32, device="cuda")
+        moe.moe_dispatch_layout_noalloc(ids, pl_dev, *got, status=status)
+        torch.cuda.synchronize()
+        moe.moe_check_device_status(ws)
+        assert status.tolist() == [0, 0, 0]
+        for r, g in zip(ref, got):
+            assert torch.equal(r, g), name
+
+
+def test_noalloc_layout_rejects_requests_beyond_its_scratch():
+    from grouped_ffn_gb300 import moe
+    # 1024 slots x 256 tiles of 4096 assignments needs more than 262144 flag words
+    E = R = 1024
+    pl = wl.placement_from_hosts(E, R, 8, wl.round_robin_hosts(E, R))
+    pl_dev = moe.DevicePlacement.from_tables(pl)
+    T, k = 4096 * 256 // 2, 2
+    ids = torch.zeros(T, k, dtype=torch.int32, device="cuda")
+    out = _outputs(T, k, pl_dev)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_dispatch_layout_noalloc(ids, pl_dev, *out)
+    assert ei.value.status == 2          # MOE_ERR_UNSUPPORTED, nothing launched
