@@ -168,9 +168,7 @@ def run_ours(args, world, rank, local):
     from grouped_ffn_gb300 import MoELayer, moe
 
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = wl.WORKLOADS[args.workload]
-    if args.zipf is not None:
-        w = w.with_zipf(args.zipf)
+    w = workload_from_args(args)
     pl = wl.make_placement(w)
     logits = wl.make_logits(w, dev)
     x = wl.make_x(w, dev)
@@ -225,26 +223,12 @@ def run_ours(args, world, rank, local):
     stage_ms = {n: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)]))
                 for j, n in enumerate(names)}
 
-    # end to end through the public API from pinned host buffers
-    logits_h = logits.cpu().pin_memory()
-    x_h = x.cpu().pin_memory()
-    y_h = torch.empty(w.T, w.H, dtype=torch.bfloat16).pin_memory()
-    logits_d, x_d, y_d = torch.empty_like(logits), torch.empty_like(x), torch.empty_like(y)
-    for _ in range(W):
-        layer.forward_host(logits_h, x_h, y_h, logits_d, x_d, y_d, stream)
-    stream.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(K):
-        layer.forward_host(logits_h, x_h, y_h, logits_d, x_d, y_d, stream)
-    e1.record(stream)
-    stream.synchronize()
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / K
-    layer.check(stream)
-    assert torch.equal(y_h, y.cpu()), "end-to-end output differs from the device-resident run"
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(layer, logits, x, y, stream, world, K, W)
+        e2e["value"] = world * w.T / (e2e["ms_per_step"] * 1e-3)
+        e2e["h2d_bytes_per_step"] = logits.numel() * 4 + x.numel() * 2
+        e2e["d2h_bytes_per_step"] = y.numel() * 2
 
     peaks = load_peaks()
     seg_counts = layer.seg_counts.cpu().numpy()
@@ -293,10 +277,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2: %.2f GB of expert weights stream per step"
                          % (g["weight_bytes"] / 1e9)},
-        "e2e": {"value": world * w.T / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": logits.numel() * 4 + x.numel() * 2,
-                "d2h_bytes_per_step": y.numel() * 2},
+        "e2e": e2e,
         "gpu_launches": layer.launches_per_step * K,
         "roofline": roof,
         "stages": stages,
@@ -309,6 +290,48 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, pl, logits, x, wgu, wd, sgu, sd, args.cpu_seconds)
     return out
+
+
+def run_e2e(layer, logits, x, y, stream, world, K, W):
+    """The same step end to end through the public API: pinned host inputs
+    copied in, the layer, the output copied back, all inside the timer."""
+    logits_h = logits.cpu().pin_memory()
+    x_h = x.cpu().pin_memory()
+    y_h = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
+    logits_d, x_d, y_d = torch.empty_like(logits), torch.empty_like(x), torch.empty_like(y)
+    for _ in range(W):
+        layer.forward_host(logits_h, x_h, y_h, logits_d, x_d, y_d, stream)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        layer.forward_host(logits_h, x_h, y_h, logits_d, x_d, y_d, stream)
+    e1.record(stream)
+    stream.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / K
+    layer.check(stream)
+    assert torch.equal(y_h, y.cpu()), "end-to-end output differs from the device-resident run"
+    return {"unit": "tokens/s", "ms_per_step": e2e_ms}
+
+
+def workload_from_args(args) -> wl.Workload:
+    w = wl.WORKLOADS[args.workload]
+    if args.zipf is not None:
+        w = w.with_zipf(args.zipf)
+    over = {}
+    if args.tokens:
+        over["T"] = args.tokens
+    if args.experts:
+        # a smaller case of the same layer shape (profiling captures)
+        over["E"] = args.experts
+        over["R"] = min(w.R, args.experts)
+        over["ranks_per_node"] = min(w.ranks_per_node, over["R"])
+    if over:
+        w = w.scaled(name=w.name + "_scaled", **over)
+    return w
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -393,9 +416,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
-    w = wl.WORKLOADS[args.workload]
-    if args.zipf is not None:
-        w = w.with_zipf(args.zipf)
+    w = workload_from_args(args)
     pl = wl.make_placement(w)
     logits = wl.make_logits(w, dev)
     x = wl.make_x(w, dev)
@@ -453,6 +474,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
+    ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
