@@ -178,7 +178,8 @@ def run_ours(args, world, rank, local):
     layer = MoELayer(H=w.H, I=w.I, E=w.E, k=w.k, placement=moe.DevicePlacement.from_tables(pl, dev),
                      w_gate_up=wgu, w_down=wd, max_tokens=w.T, score_fn=w.score_fn,
                      n_groups=w.n_groups, topk_groups=w.topk_groups, group_topn=w.group_topn,
-                     shared_w_gate_up=sgu, shared_w_down=sd, device=dev)
+                     shared_w_gate_up=sgu, shared_w_down=sd, device=dev,
+                     packed=not args.unpacked)
     y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -275,6 +276,7 @@ def run_ours(args, world, rank, local):
                    "ffn_intermediate": w.I, "shared_intermediate": w.shared_I,
                    "simulated_ranks": w.R, "zipf_s": w.zipf_s, "assignments": w.A,
                    "parallelism": f"replicas{world}",
+                   "weight_layout": "plain" if args.unpacked else "packed",
                    "l2": "inputs larger than L2: %.2f GB of expert weights stream per step"
                          % (g["weight_bytes"] / 1e9)},
         "e2e": e2e,
@@ -475,6 +477,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--unpacked", action="store_true",
+                    help="stream the expert weights in their plain [E,2I,H]/[E,H,I] layout")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count")
     args = ap.parse_args()

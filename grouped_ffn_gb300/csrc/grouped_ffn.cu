@@ -81,6 +81,7 @@ struct FfnParams {
   int32_t out_ld;
   int32_t out_nblk_stride;    // output column step per n-block (128 or 256)
   int32_t mode;               // 0 gate/up + SwiGLU, 1 down
+  int32_t b_packed;           // B in the tile-contiguous layout (see moe_pack_expert_weights)
   int32_t *status;
 };
 
@@ -347,8 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         decode_tile(t, tile_prefix, p.S, NB, s, n_blk, m_blk);
         const int e = seg_exp[s];
         const int row_a = seg_off[s] + m_blk * kBM;
-        const int row_b0 = e * p.b_rows_per_expert + n_blk * p.b_nblk_stride;
-        const int row_b1 = row_b0 + p.b_second_off;
+        // B rows of k-block 0; packed: [e][n_blk][kb][half][128 rows][64 cols],
+        // so one k-block of the tile is 32 contiguous KiB.
+        const int64_t packed0 = (int64_t)(e * NB + n_blk) * nk * 256;
+        const int row_b0 = p.b_packed ? (int)packed0 : e * p.b_rows_per_expert + n_blk * p.b_nblk_stride;
+        const int row_b1 = p.b_packed ? row_b0 + 128 : row_b0 + p.b_second_off;
+        const int b_x_step = p.b_packed ? 0 : kBK;
+        const int b_y_step = p.b_packed ? 256 : 0;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.status, kid)) {
             ok = false;
@@ -357,8 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t *sa = smem + (size_t)stage * kStageBytes;
           mbar_arrive_expect_tx(&bars->full[stage], kStageBytes);
           tma_load_2d(sa, &tmap_a, kb * kBK, row_a, &bars->full[stage]);
-          tma_load_2d(sa + kABytes, &tmap_b, kb * kBK, row_b0, &bars->full[stage]);
-          tma_load_2d(sa + kABytes + kBHalfBytes, &tmap_b, kb * kBK, row_b1, &bars->full[stage]);
+          tma_load_2d(sa + kABytes, &tmap_b, kb * b_x_step, row_b0 + kb * b_y_step,
+                      &bars->full[stage]);
+          tma_load_2d(sa + kABytes + kBHalfBytes, &tmap_b, kb * b_x_step, row_b1 + kb * b_y_step,
+                      &bars->full[stage]);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -522,18 +530,37 @@ moe_status launch(const CUtensorMap &ma, const CUtensorMap &mb, const FfnParams 
   return moe_host::launch_status();
 }
 
-}  // namespace
+// Pack kernel: W[e][row][k] -> P[e][nb][kb][half][128][64] in 16-byte units.
+// Source row of (nb, half, r): gate/up (mode 0) half*I + nb*128 + r; down
+// (mode 1) nb*256 + half*128 + r.
+__global__ void pack_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int64_t total16,
+                            int NB, int nk, int rows_per_expert, int K8, int mode, int I) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t d = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; d < total16; d += stride) {
+    int64_t q = d;
+    const int c16 = (int)(q % 8);
+    q /= 8;
+    const int r = (int)(q % 128);
+    q /= 128;
+    const int half = (int)(q % 2);
+    q /= 2;
+    const int kb = (int)(q % nk);
+    q /= nk;
+    const int nb = (int)(q % NB);
+    const int64_t e = q / NB;
+    const int row = mode == 0 ? half * I + nb * 128 + r : nb * 256 + half * 128 + r;
+    dst[d] = __ldg(src + (e * rows_per_expert + row) * K8 + kb * 8 + c16);
+  }
+}
 
-extern "C" moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows,
-                                      const int32_t *seg_offsets, const int32_t *seg_expert,
-                                      int32_t S, int32_t E, const uint16_t *w_gate_up,
-                                      const uint16_t *w_down, int32_t H, int32_t I, uint16_t *h,
-                                      uint16_t *y_perm, void *ws, size_t ws_bytes, void *stream) {
+moe_status check_ffn_args(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_offsets,
+                          const int32_t *seg_expert, int32_t S, int32_t E,
+                          const uint16_t *w_gate_up, const uint16_t *w_down, int32_t H, int32_t I,
+                          uint16_t *h, uint16_t *y_perm, void *ws, size_t ws_bytes) {
   if (n_rows < 0 || S < 1 || E < 1 || H < 1 || I < 1) return MOE_ERR_INVALID_ARG;
   if (S > kMaxSegs || H % 256 != 0 || I % 128 != 0 || n_rows >= ((int64_t)1 << 31))
     return MOE_ERR_UNSUPPORTED;
-  if ((int64_t)E * 2 * I >= ((int64_t)1 << 31) || (int64_t)E * H >= ((int64_t)1 << 31))
-    return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)E * 2 * I * (int64_t)H / 64 >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (!seg_offsets || !seg_expert || !w_gate_up || !w_down) return MOE_ERR_INVALID_ARG;
   if (moe_status s = moe_host::check_ws(ws, ws_bytes, moe::kStatusBytes)) return s;
   if (n_rows == 0) return MOE_OK;
@@ -541,13 +568,28 @@ extern "C" moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows,
   if (!moe_host::aligned16(x_perm) || !moe_host::aligned16(h) || !moe_host::aligned16(y_perm) ||
       !moe_host::aligned16(w_gate_up) || !moe_host::aligned16(w_down))
     return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_offsets,
+                   const int32_t *seg_expert, int32_t S, int32_t E, const uint16_t *w_gate_up,
+                   const uint16_t *w_down, int32_t H, int32_t I, uint16_t *h, uint16_t *y_perm,
+                   void *ws, size_t ws_bytes, void *stream, bool packed) {
+  if (moe_status s = check_ffn_args(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up,
+                                    w_down, H, I, h, y_perm, ws, ws_bytes))
+    return s;
+  if (n_rows == 0) return MOE_OK;
   if (!ensure_smem_attr()) return MOE_ERR_CUDA;
 
   CUtensorMap m_x, m_wgu, m_h, m_wd;
+  const uint64_t gu_rows = packed ? (uint64_t)E * 2 * I * H / kBK : (uint64_t)E * 2 * I;
+  const uint64_t gu_cols = packed ? (uint64_t)kBK : (uint64_t)H;
+  const uint64_t d_rows = packed ? (uint64_t)E * H * I / kBK : (uint64_t)E * H;
+  const uint64_t d_cols = packed ? (uint64_t)kBK : (uint64_t)I;
   if (!make_map(&m_x, x_perm, (uint64_t)n_rows, (uint64_t)H) ||
-      !make_map(&m_wgu, w_gate_up, (uint64_t)E * 2 * I, (uint64_t)H) ||
+      !make_map(&m_wgu, w_gate_up, gu_rows, gu_cols) ||
       !make_map(&m_h, h, (uint64_t)n_rows, (uint64_t)I) ||
-      !make_map(&m_wd, w_down, (uint64_t)E * H, (uint64_t)I))
+      !make_map(&m_wd, w_down, d_rows, d_cols))
     return MOE_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -569,6 +611,7 @@ extern "C" moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows,
   p1.out_ld = I;
   p1.out_nblk_stride = 128;
   p1.mode = 0;
+  p1.b_packed = packed ? 1 : 0;
   p1.status = status;
   if (moe_status s = launch(m_x, m_wgu, p1, m_tiles_max * p1.n_blocks, st)) return s;
 
@@ -583,4 +626,50 @@ extern "C" moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows,
   p2.out_nblk_stride = 256;
   p2.mode = 1;
   return launch(m_h, m_wd, p2, m_tiles_max * p2.n_blocks, st);
+}
+
+}  // namespace
+
+extern "C" moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows,
+                                      const int32_t *seg_offsets, const int32_t *seg_expert,
+                                      int32_t S, int32_t E, const uint16_t *w_gate_up,
+                                      const uint16_t *w_down, int32_t H, int32_t I, uint16_t *h,
+                                      uint16_t *y_perm, void *ws, size_t ws_bytes, void *stream) {
+  return run_ffn(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up, w_down, H, I, h, y_perm,
+                 ws, ws_bytes, stream, false);
+}
+
+extern "C" moe_status moe_grouped_ffn_packed(const uint16_t *x_perm, int64_t n_rows,
+                                             const int32_t *seg_offsets, const int32_t *seg_expert,
+                                             int32_t S, int32_t E, const uint16_t *w_gate_up_packed,
+                                             const uint16_t *w_down_packed, int32_t H, int32_t I,
+                                             uint16_t *h, uint16_t *y_perm, void *ws,
+                                             size_t ws_bytes, void *stream) {
+  return run_ffn(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up_packed, w_down_packed, H,
+                 I, h, y_perm, ws, ws_bytes, stream, true);
+}
+
+extern "C" moe_status moe_pack_expert_weights(const uint16_t *w_gate_up, const uint16_t *w_down,
+                                              int32_t E, int32_t H, int32_t I,
+                                              uint16_t *w_gate_up_packed, uint16_t *w_down_packed,
+                                              void *stream) {
+  if (E < 1 || H < 1 || I < 1) return MOE_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!w_gate_up || !w_down || !w_gate_up_packed || !w_down_packed) return MOE_ERR_INVALID_ARG;
+  if (!moe_host::aligned16(w_gate_up) || !moe_host::aligned16(w_down) ||
+      !moe_host::aligned16(w_gate_up_packed) || !moe_host::aligned16(w_down_packed))
+    return MOE_ERR_INVALID_ARG;
+  if (w_gate_up == w_gate_up_packed || w_down == w_down_packed) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t grid = (int64_t)moe_host::sm_count() * 8;
+  const int64_t gu16 = (int64_t)E * 2 * I * H / 8;
+  pack_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const uint4 *>(w_gate_up),
+                                               reinterpret_cast<uint4 *>(w_gate_up_packed), gu16,
+                                               I / 128, H / kBK, 2 * I, H / 8, 0, I);
+  if (moe_status s = moe_host::launch_status()) return s;
+  const int64_t d16 = (int64_t)E * H * I / 8;
+  pack_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const uint4 *>(w_down),
+                                               reinterpret_cast<uint4 *>(w_down_packed), d16,
+                                               H / 256, I / kBK, H, I / 8, 1, I);
+  return moe_host::launch_status();
 }

@@ -33,6 +33,7 @@ constexpr int kRounds = kPerWarp / 32;
 constexpr int kTileA = kWarps * kPerWarp;  // 4096 assignments per tile
 constexpr int kMaxSlots = 1024;
 constexpr int kMaxRanks = 1024;
+constexpr int kMaxExperts = 4096;
 
 constexpr uint32_t kFlagAgg = 1u << 30;
 constexpr uint32_t kFlagInc = 2u << 30;
@@ -51,36 +52,50 @@ struct LayoutArgs {
   int32_t n_tiles;
 };
 
-// Slot serving assignment a, or -1 after reporting an error.
-__device__ int choose_slot(const LayoutArgs &p, int64_t a) {
-  const int64_t t = a / p.k;
-  const int e = p.topk_ids[a];
+// Placement tables cached in shared memory by every layout CTA.
+struct PlacementCache {
+  const int32_t *rep_offsets;  // [E+1]
+  const int32_t *rep_slots;    // [S]
+  const int32_t *slot_expert;  // [S]
+  const int32_t *slot_rank;    // [S]
+};
+
+// Slot serving assignment a (expert e), or -1 after reporting an error.
+__device__ int choose_slot(const LayoutArgs &p, const PlacementCache &c, int64_t a, int e) {
   if (e < 0 || e >= p.E) {
     moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, (int32_t)a, moe::K_LAYOUT_SCAN);
     return -1;
   }
-  const int lo = p.rep_offsets[e], hi = p.rep_offsets[e + 1];
+  const int64_t t = a / p.k;
+  const int lo = c.rep_offsets[e], hi = c.rep_offsets[e + 1];
   const int n = hi - lo;
   int s = -1;
-  if (n == 1) {
-    s = p.rep_slots[lo];
-  } else if (n > 1) {
+  if (lo < 0 || hi > p.S || n < 1) {
+    s = -1;
+  } else if (n == 1) {
+    s = c.rep_slots[lo];
+  } else {
     const int src = p.token_src_rank ? p.token_src_rank[t] : (int)(t % p.R);
     const int node = src / p.rpn;
     for (int i = lo; i < hi; ++i) {
-      const int c = p.rep_slots[i];
-      if (c >= 0 && c < p.S && p.slot_rank[c] / p.rpn == node) {
-        s = c;
+      const int cs = c.rep_slots[i];
+      if (cs >= 0 && cs < p.S && c.slot_rank[cs] / p.rpn == node) {
+        s = cs;
         break;
       }
     }
-    if (s < 0) s = p.rep_slots[lo + (int)(t % n)];
+    if (s < 0) s = c.rep_slots[lo + (int)(t % n)];
   }
-  if (s < 0 || s >= p.S || p.slot_expert[s] != e) {
+  if (s < 0 || s >= p.S || c.slot_expert[s] != e) {
     moe::report_error(p.status, MOE_ERR_PLACEMENT, e, moe::K_LAYOUT_SCAN);
     return -1;
   }
   return s;
+}
+
+// Dynamic shared memory of layout_scan_kernel, in 32-bit words.
+inline size_t layout_smem_words(int S, int R, int E) {
+  return (size_t)(kWarps + 2) * S + R + (E + 1) + 3 * (size_t)S;
 }
 
 __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
@@ -89,28 +104,50 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
   int32_t *tile_prefix = smem + kWarps * p.S;  // [S]
   int32_t *tile_agg = tile_prefix + p.S;       // [S]
   int32_t *rload = tile_agg + p.S;             // [R], last tile only
+  int32_t *c_rep_offsets = rload + p.R;        // [E+1]
+  int32_t *c_rep_slots = c_rep_offsets + p.E + 1;  // [S]
+  int32_t *c_slot_expert = c_rep_slots + p.S;      // [S]
+  int32_t *c_slot_rank = c_slot_expert + p.S;      // [S]
   __shared__ int32_t s_tile;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) s_tile = atomicAdd(p.ticket, 1);
   for (int i = tid; i < kWarps * p.S; i += kThreads) whist[i] = 0;
+  for (int i = tid; i <= p.E; i += kThreads) c_rep_offsets[i] = p.rep_offsets[i];
+  for (int i = tid; i < p.S; i += kThreads) {
+    c_rep_slots[i] = p.rep_slots[i];
+    c_slot_expert[i] = p.slot_expert[i];
+    c_slot_rank[i] = p.slot_rank[i];
+  }
   __syncthreads();
   const int tile = s_tile;
+  const PlacementCache cache{c_rep_offsets, c_rep_slots, c_slot_expert, c_slot_rank};
 
-  // ---- stable rank of each assignment inside its warp's 256-run
+  // ---- slots of this warp's 256 assignments (all loads issued together)
   const int64_t base = (int64_t)tile * kTileA + (int64_t)warp * kPerWarp;
+  int ids[kRounds];
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int64_t a = base + r * 32 + lane;
+    ids[r] = (a < p.A) ? __ldg(p.topk_ids + a) : 0;
+  }
   int my_slot[kRounds], my_rank[kRounds];
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
     const int64_t a = base + r * 32 + lane;
-    const int s = (a < p.A) ? choose_slot(p, a) : -1;
+    my_slot[r] = (a < p.A) ? choose_slot(p, cache, a, ids[r]) : -1;
+  }
+
+  // ---- stable rank of each assignment inside its warp's 256-run
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int s = my_slot[r];
     const uint32_t peers = __match_any_sync(0xffffffffu, s);
     const int leader = __ffs(peers) - 1;
     const int before = (s >= 0) ? whist[warp * p.S + s] : 0;
     __syncwarp();
     if (s >= 0 && lane == leader) whist[warp * p.S + s] = before + __popc(peers);
     __syncwarp();
-    my_slot[r] = s;
     my_rank[r] = before + __popc(peers & ((1u << lane) - 1u));
   }
   __syncthreads();
@@ -254,7 +291,8 @@ extern "C" moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, in
   if (A >= (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
   if (pl->n_experts < 1 || pl->n_slots < 1 || pl->n_ranks < 1 || pl->ranks_per_node < 1)
     return MOE_ERR_INVALID_ARG;
-  if (pl->n_slots > kMaxSlots || pl->n_ranks > kMaxRanks) return MOE_ERR_UNSUPPORTED;
+  if (pl->n_slots > kMaxSlots || pl->n_ranks > kMaxRanks || pl->n_experts > kMaxExperts)
+    return MOE_ERR_UNSUPPORTED;
   if (!pl->slot_expert || !pl->slot_rank || !pl->rep_offsets || !pl->rep_slots || !seg_counts ||
       !seg_offsets || !rank_counts)
     return MOE_ERR_INVALID_ARG;
@@ -292,7 +330,7 @@ extern "C" moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, in
   p.status = moe_host::status_ptr(ws);
   p.n_tiles = (int32_t)n_tiles;
 
-  const size_t smem = ((size_t)(kWarps + 2) * p.S + p.R) * sizeof(int32_t);
+  const size_t smem = layout_smem_words(p.S, p.R, p.E) * sizeof(int32_t);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(layout_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
@@ -363,7 +401,8 @@ extern "C" moe_status moe_dispatch_layout_noalloc(const int32_t *topk_ids, int64
   if (A >= (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
   if (pl->n_experts < 1 || pl->n_slots < 1 || pl->n_ranks < 1 || pl->ranks_per_node < 1)
     return MOE_ERR_INVALID_ARG;
-  if (pl->n_slots > kMaxSlots || pl->n_ranks > kMaxRanks) return MOE_ERR_UNSUPPORTED;
+  if (pl->n_slots > kMaxSlots || pl->n_ranks > kMaxRanks || pl->n_experts > kMaxExperts)
+    return MOE_ERR_UNSUPPORTED;
   if (!pl->slot_expert || !pl->slot_rank || !pl->rep_offsets || !pl->rep_slots || !seg_counts ||
       !seg_offsets || !rank_counts)
     return MOE_ERR_INVALID_ARG;
@@ -403,7 +442,7 @@ extern "C" moe_status moe_dispatch_layout_noalloc(const int32_t *topk_ids, int64
   p.status = status;
   p.n_tiles = (int32_t)n_tiles;
 
-  const size_t smem = ((size_t)(kWarps + 2) * p.S + p.R) * sizeof(int32_t);
+  const size_t smem = layout_smem_words(p.S, p.R, p.E) * sizeof(int32_t);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(layout_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)

@@ -10,8 +10,15 @@
 // a per-lane scan of its unselected values followed by a 5-step butterfly
 // arg-max; the order (value descending, id ascending) is exactly the one of
 // the result, so no sort is needed.  Selection compares the fp32 logits as
-// IEEE values (so -0 == +0 and ties go to the lower id); group scores and
-// weights are computed in fp64 and rounded once.
+// IEEE values (so -0 == +0 and ties go to the lower id).
+//
+// GB300 issues fp64 at a small fraction of the fp32 rate, so fp64 is used
+// only where a floating value decides an integer: each lane computes its own
+// group's score (the fp64 sum of fp64 sigmoids), all groups in parallel.
+// Weights are fp32: the softmax exponent l_j - l_max is split error-free
+// (TwoSum) into hi + lo and exp(hi + lo) = expf(hi) * (1 + lo); the k terms
+// are summed with a TwoSum-compensated butterfly; one IEEE division.  The
+// weights are within a few fp32 ulps of the exact values.
 #include <cfloat>
 #include <climits>
 
@@ -59,10 +66,27 @@ __device__ __forceinline__ void warp_argmax(const float (&v)[VPL], uint32_t mask
   }
 }
 
-__device__ __forceinline__ double warp_sum_f64(double x) {
+constexpr int kMaxGroupTopn = 8;
+
+// s + e == a + b exactly (round-to-nearest, no overflow).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Compensated butterfly sum; every lane ends with the same value.
+__device__ __forceinline__ float warp_sum_compensated(float x) {
+  float s = x, c = 0.0f;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  return x;
+  for (int off = 16; off > 0; off >>= 1) {
+    const float os = __shfl_xor_sync(0xffffffffu, s, off);
+    const float oc = __shfl_xor_sync(0xffffffffu, c, off);
+    float e;
+    two_sum(s, os, s, e);
+    c = __fadd_rn(__fadd_rn(c, oc), e);
+  }
+  return __fadd_rn(s, c);
 }
 
 template <int VPL>
@@ -91,22 +115,32 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
 
     if (a.n_groups > 1) {
       // Group score: fp64 sum of the sigmoids of the group's group_topn
-      // largest logits, taken in descending order.  Lane g keeps group g's.
-      double my_gscore = 0.0;
+      // largest logits, taken in descending order.  Lane g collects group
+      // g's values, then every lane scores its own group in parallel.
+      float gv[kMaxGroupTopn];
+#pragma unroll
+      for (int r = 0; r < kMaxGroupTopn; ++r) gv[r] = 0.0f;
       for (int g = 0; g < a.n_groups; ++g) {
         uint32_t gmask = 0;
 #pragma unroll
         for (int i = 0; i < VPL; ++i)
           if (((avail >> i) & 1u) && (lane + 32 * i) / gsz == g) gmask |= 1u << i;
-        double s = 0.0;
-        for (int r = 0; r < a.group_topn; ++r) {
-          float bv;
-          int bid;
-          warp_argmax<VPL>(v, gmask, lane, bv, bid);
-          s += sigmoid64(bv);
-          if ((bid & 31) == lane) gmask &= ~(1u << (bid >> 5));
+#pragma unroll
+        for (int r = 0; r < kMaxGroupTopn; ++r) {
+          if (r < a.group_topn) {
+            float bv;
+            int bid;
+            warp_argmax<VPL>(v, gmask, lane, bv, bid);
+            if (lane == g) gv[r] = bv;
+            if ((bid & 31) == lane) gmask &= ~(1u << (bid >> 5));
+          }
         }
-        if (lane == g) my_gscore = s;
+      }
+      double my_gscore = 0.0;
+      if (lane < a.n_groups) {
+#pragma unroll
+        for (int r = 0; r < kMaxGroupTopn; ++r)
+          if (r < a.group_topn) my_gscore += sigmoid64(gv[r]);
       }
       // Keep the topk_groups best groups (score descending, id ascending).
       bool gfree = lane < a.n_groups;
@@ -146,17 +180,21 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
       }
     }
 
-    double num = 0.0;
+    float num = 0.0f;
     if (a.score_fn == MOE_SCORE_SOFTMAX) {
-      const double m = (double)__shfl_sync(0xffffffffu, my_v, 0);  // the largest logit
-      if (lane < a.k) num = exp((double)my_v - m);
+      const float m = __shfl_sync(0xffffffffu, my_v, 0);  // the largest logit
+      if (lane < a.k) {
+        float d, dlo;
+        two_sum(my_v, -m, d, dlo);
+        num = __fmul_rn(expf(d), __fadd_rn(1.0f, dlo));
+      }
     } else {
-      if (lane < a.k) num = sigmoid64(my_v);
+      if (lane < a.k) num = __frcp_rn(__fadd_rn(1.0f, expf(-my_v)));
     }
-    const double den = warp_sum_f64(num);
+    const float den = warp_sum_compensated(num);
     if (lane < a.k) {
       ids[t * a.k + lane] = my_id;
-      w[t * a.k + lane] = (float)(num / den);
+      w[t * a.k + lane] = __fdiv_rn(num, den);
     }
   }
 }
@@ -193,6 +231,7 @@ extern "C" moe_status moe_route(const float *logits, int64_t T, int32_t E, const
     const int gsz = E / a.n_groups;
     if (a.topk_groups < 1 || a.topk_groups > a.n_groups) return MOE_ERR_INVALID_ARG;
     if (a.group_topn < 1 || a.group_topn > gsz) return MOE_ERR_INVALID_ARG;
+    if (a.group_topn > kMaxGroupTopn) return MOE_ERR_UNSUPPORTED;
     if (a.k > a.topk_groups * gsz) return MOE_ERR_INVALID_ARG;
   }
   if (T == 0) return MOE_OK;

@@ -23,9 +23,17 @@ class MoELayer:
                  score_fn: int = moe.MOE_SCORE_SOFTMAX, n_groups: int = 1,
                  topk_groups: int = 1, group_topn: int = 1,
                  shared_w_gate_up: Optional[torch.Tensor] = None,
-                 shared_w_down: Optional[torch.Tensor] = None, device="cuda"):
+                 shared_w_down: Optional[torch.Tensor] = None, device="cuda",
+                 packed: bool = True):
         self.H, self.I, self.E, self.k = H, I, E, k
         self.placement = placement
+        self.packed = packed
+        if packed:
+            # one-time rearrangement into the tile-contiguous layout the FFN
+            # kernel streams best (each TMA box is one contiguous block)
+            w_gate_up, w_down = self._pack(w_gate_up, w_down)
+            if shared_w_gate_up is not None:
+                shared_w_gate_up, shared_w_down = self._pack(shared_w_gate_up, shared_w_down)
         self.w_gate_up, self.w_down = w_gate_up, w_down
         self.shared_w_gate_up, self.shared_w_down = shared_w_gate_up, shared_w_down
         self.cfg = moe.RouteCfg(score_fn, k, n_groups, topk_groups, group_topn)
@@ -58,8 +66,21 @@ class MoELayer:
             self._shared_offsets = {}
         else:
             self.shared_I = 0
-        # route, layout scan + finalize, permute, 2 FFN, combine, balance (+2 shared FFN)
+        # per step: route, layout scan + finalize, permute, 2 FFN, combine,
+        # balance (+2 shared FFN); packing happens once, here
         self.launches_per_step = 8 + (2 if shared_w_gate_up is not None else 0)
+
+    @staticmethod
+    def _pack(w_gate_up, w_down):
+        gu, d = torch.empty_like(w_gate_up), torch.empty_like(w_down)
+        moe.moe_pack_expert_weights(w_gate_up, w_down, gu, d)
+        return gu, d
+
+    def _ffn(self, *args):
+        if self.packed:
+            moe.moe_grouped_ffn_packed(*args)
+        else:
+            moe.moe_grouped_ffn(*args)
 
     def _shared_offs(self, T: int) -> torch.Tensor:
         t = self._shared_offsets.get(T)
@@ -87,15 +108,13 @@ class MoELayer:
         mark("layout")
         moe.moe_permute(x, self.k, self.dest_row[:A], self.x_perm[:A], self.ws, stream)
         mark("permute")
-        moe.moe_grouped_ffn(self.x_perm[:A], self.seg_offsets, self.placement.slot_expert,
-                            self.w_gate_up, self.w_down, self.h[:A], self.y_perm[:A], self.ws,
-                            stream)
+        self._ffn(self.x_perm[:A], self.seg_offsets, self.placement.slot_expert,
+                  self.w_gate_up, self.w_down, self.h[:A], self.y_perm[:A], self.ws, stream)
         mark("grouped_ffn")
         shared = None
         if self.shared_I:
-            moe.moe_grouped_ffn(x, self._shared_offs(T), self.shared_expert,
-                                self.shared_w_gate_up, self.shared_w_down, self.shared_h[:T],
-                                self.shared_y[:T], self.ws, stream)
+            self._ffn(x, self._shared_offs(T), self.shared_expert, self.shared_w_gate_up,
+                      self.shared_w_down, self.shared_h[:T], self.shared_y[:T], self.ws, stream)
             shared = self.shared_y[:T]
             mark("shared_ffn")
         moe.moe_combine(self.y_perm[:A], self.dest_row[:A], w, y, self.ws, shared, stream)

@@ -68,6 +68,9 @@ _SIGNATURES = {
     "moe_permute": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _I32, _I32,
                                        _P, _P, _P, _SZ, _P]),
+    "moe_grouped_ffn_packed": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _I32, _I32,
+                                              _P, _P, _P, _SZ, _P]),
+    "moe_pack_expert_weights": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "moe_balance_stats": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -242,6 +245,43 @@ def moe_grouped_ffn(x_perm, seg_offsets, seg_expert, w_gate_up, w_down, h, y_per
     _check("moe_grouped_ffn", lib().moe_grouped_ffn(
         _ptr(x_perm), n_rows, _ptr(seg_offsets), _ptr(seg_expert), S, E, _ptr(w_gate_up),
         _ptr(w_down), H, I, _ptr(h), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_grouped_ffn_packed(x_perm, seg_offsets, seg_expert, w_gate_up_packed, w_down_packed,
+                           h, y_perm, ws, stream=None):
+    """moe_grouped_ffn on weights packed by moe_pack_expert_weights (same
+    shapes as the plain [E,2I,H] and [E,H,I] tensors)."""
+    for n, t in (("x_perm", x_perm), ("w_gate_up_packed", w_gate_up_packed),
+                 ("w_down_packed", w_down_packed), ("h", h), ("y_perm", y_perm)):
+        _bf16(t, n)
+    _need(seg_offsets, torch.int32, "seg_offsets")
+    _need(seg_expert, torch.int32, "seg_expert")
+    n_rows, H = x_perm.shape
+    E, two_i, H2 = w_gate_up_packed.shape
+    I = two_i // 2
+    if H2 != H or tuple(w_down_packed.shape) != (E, H, I) or tuple(h.shape) != (n_rows, I) \
+            or tuple(y_perm.shape) != (n_rows, H):
+        raise ValueError("moe_grouped_ffn_packed: inconsistent shapes")
+    S = seg_expert.numel()
+    _check("moe_grouped_ffn_packed", lib().moe_grouped_ffn_packed(
+        _ptr(x_perm), n_rows, _ptr(seg_offsets), _ptr(seg_expert), S, E, _ptr(w_gate_up_packed),
+        _ptr(w_down_packed), H, I, _ptr(h), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_pack_expert_weights(w_gate_up, w_down, w_gate_up_packed, w_down_packed, stream=None):
+    """Rearrange [E,2I,H] / [E,H,I] expert weights into the library's
+    tile-contiguous layout (outputs have the same shapes)."""
+    for n, t in (("w_gate_up", w_gate_up), ("w_down", w_down),
+                 ("w_gate_up_packed", w_gate_up_packed), ("w_down_packed", w_down_packed)):
+        _bf16(t, n)
+    E, two_i, H = w_gate_up.shape
+    I = two_i // 2
+    if tuple(w_down.shape) != (E, H, I) or w_gate_up_packed.shape != w_gate_up.shape \
+            or w_down_packed.shape != w_down.shape:
+        raise ValueError("moe_pack_expert_weights: inconsistent shapes")
+    _check("moe_pack_expert_weights", lib().moe_pack_expert_weights(
+        _ptr(w_gate_up), _ptr(w_down), E, H, I, _ptr(w_gate_up_packed), _ptr(w_down_packed),
+        _stream(stream)))
 
 
 def moe_combine(y_perm, dest_row, topk_w, y, ws, shared=None, stream=None):

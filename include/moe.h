@@ -74,8 +74,9 @@ typedef struct moe_route_cfg {
  *      slot_expert[s] on rank slot_rank[s]; slots are sorted by (rank,
  *      expert) strictly increasing, so segment s of the dispatched buffer is
  *      slot s and each rank's segments are contiguous.
- *  rep_offsets[E+1], rep_slots[rep_offsets[E]]: CSR list of each expert's
- *      slots, in ascending rank order; every expert has at least one.
+ *  rep_offsets[E+1], rep_slots[S]: CSR list of each expert's slots, in
+ *      ascending rank order; every expert has at least one and every slot
+ *      appears once (rep_offsets[E] == S).
  *  token_src_rank[T] or NULL: the rank each token lives on (NULL: t mod R).
  *  ranks_per_node: ranks of one node; node(r) = r / ranks_per_node. */
 typedef struct moe_placement {
@@ -117,12 +118,14 @@ moe_status moe_check_device_status(void *ws, void *stream, int32_t *info_host);
  *  topk_ids device int32 [T, k]: descending score, ties to the lower id.
  *  topk_w   device fp32 [T, k]: softmax -- exp(l_j - l_max) renormalised
  *           over the selected k; sigmoid -- sigmoid(l_j) / sum over the
- *           selected k (computed in fp64, rounded once).
- *  Group-limited (n_groups > 1, sigmoid or softmax scores): groups are E /
- *  n_groups contiguous experts; a group's score is the fp64 sum of the
+ *           selected k.  fp32 with compensated sums: within a few fp32
+ *           ulps of the exact value.
+ *  Group-limited (n_groups > 1, sigmoid scores only): groups are E /
+ *  n_groups contiguous experts; a group's score is the fp64 sum of the fp64
  *  sigmoids of its group_topn largest logits; the topk_groups best groups
  *  (ties: lower group id) are kept and the k experts are chosen among them.
- *  Limits: 1 <= E <= 512, k <= 16.  ws may be NULL (no device errors). */
+ *  Limits: 1 <= E <= 512, k <= 16, n_groups <= 32, group_topn <= 8.
+ *  ws may be NULL (no device errors). */
 moe_status moe_route(const float *logits, int64_t T, int32_t E, const moe_route_cfg *cfg,
                      int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes,
                      void *stream);
@@ -146,7 +149,8 @@ moe_status moe_route(const float *logits, int64_t T, int32_t E, const moe_route_
  *   rank_counts[R]     assignments per simulated rank.
  *  Device errors: MOE_ERR_DEVICE_INDEX (expert id outside [0,E)),
  *  MOE_ERR_PLACEMENT (tables inconsistent), MOE_ERR_DEVICE_TIMEOUT.
- *  Limits: n_slots <= 1024, T*k < 2^31.  ws: moe_workspace_size(T,k,S). */
+ *  Limits: n_slots <= 1024, n_ranks <= 1024, n_experts <= 4096, T*k < 2^30.
+ *  ws: moe_workspace_size(T,k,S). */
 moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k,
                                const moe_placement *placement, int32_t *slot,
                                int32_t *seg_counts, int32_t *seg_offsets,
@@ -214,6 +218,31 @@ moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t
                            const uint16_t *w_gate_up, const uint16_t *w_down, int32_t H,
                            int32_t I, uint16_t *h, uint16_t *y_perm, void *ws,
                            size_t ws_bytes, void *stream);
+
+/* Expert weights rearranged for streaming: each 128-row x 64-column block
+ * that the grouped GEMM loads per pipeline stage becomes one contiguous
+ * 16 KiB run, so the weight stream is sequential in HBM.  Expert execution
+ * with few tokens per expert is dominated by loading the expert weights
+ * ("Mixture-of-Experts Inference", "Memory pressure"); the layout itself is
+ * this library's own.  Done once per set of weights.
+ *  Packed gate/up, index (e, nb, kb, half, r, c) with nb < I/128, kb < H/64,
+ *  half < 2, r < 128, c < 64, holds w_gate_up[e][half*I + nb*128 + r][kb*64 + c].
+ *  Packed down, (e, nb, kb, half, r, c) with nb < H/256, kb < I/64 holds
+ *  w_down[e][nb*256 + half*128 + r][kb*64 + c].
+ *  Outputs have the sizes of the inputs and must not alias them.
+ *  Limits: H % 256 == 0, I % 128 == 0. */
+moe_status moe_pack_expert_weights(const uint16_t *w_gate_up, const uint16_t *w_down, int32_t E,
+                                   int32_t H, int32_t I, uint16_t *w_gate_up_packed,
+                                   uint16_t *w_down_packed, void *stream);
+
+/* moe_grouped_ffn on weights packed by moe_pack_expert_weights: same
+ * arguments, same results bit for bit. */
+moe_status moe_grouped_ffn_packed(const uint16_t *x_perm, int64_t n_rows,
+                                  const int32_t *seg_offsets, const int32_t *seg_expert,
+                                  int32_t S, int32_t E, const uint16_t *w_gate_up_packed,
+                                  const uint16_t *w_down_packed, int32_t H, int32_t I,
+                                  uint16_t *h, uint16_t *y_perm, void *ws, size_t ws_bytes,
+                                  void *stream);
 
 /* Combine: y[t] = bf16(acc) with acc = shared[t] (or 0) and, for j = 0..k-1
  * in order, acc = fmaf(topk_w[t,j], y_perm[dest_row[t*k+j]], acc) in fp32.

@@ -329,6 +329,36 @@ def test_grouped_ffn_small_full_compare(H, I, counts):
     assert torch.isnan(yp[A:].float()).all() and torch.isnan(h[A:].float()).all()
 
 
+@pytest.mark.parametrize("H,I,counts", [(256, 128, [3, 0, 5, 8]),
+                                         (512, 384, [130, 1, 0, 257, 128, 75, 300, 12])])
+def test_packed_ffn_is_bit_identical_to_plain(H, I, counts):
+    m = moe()
+    E = len(counts) + 1
+    w = wl.Workload("ffnp", 70 + H // 256 + I, T=1, H=H, E=E, k=1, I=I, R=1, ranks_per_node=1)
+    offs = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32, device="cuda")
+    se = torch.tensor([(5 * s + 2) % E for s in range(len(counts))], dtype=torch.int32, device="cuda")
+    n = int(offs[-1]) + 5
+    g = torch.Generator(device="cuda").manual_seed(3)
+    xp = torch.randn(n, H, generator=g, device="cuda").to(torch.bfloat16)
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    pgu, pd = torch.empty_like(wgu), torch.empty_like(wd)
+    m.moe_pack_expert_weights(wgu, wd, pgu, pd)
+    # the packed layout, as the header defines it
+    NB1, nk1, NB2, nk2 = I // 128, H // 64, H // 256, I // 64
+    want_gu = wgu.view(E, 2, NB1, 128, nk1, 64).permute(0, 2, 4, 1, 3, 5).reshape(E, 2 * I, H)
+    want_d = wd.view(E, NB2, 2, 128, nk2, 64).permute(0, 1, 4, 2, 3, 5).reshape(E, H, I)
+    assert torch.equal(pgu, want_gu) and torch.equal(pd, want_d)
+    ws = m.new_workspace(1, 1, 1)
+    outs = []
+    for fn, a, b in ((m.moe_grouped_ffn, wgu, wd), (m.moe_grouped_ffn_packed, pgu, pd)):
+        h = torch.zeros(n, I, dtype=torch.bfloat16, device="cuda")
+        y = torch.zeros(n, H, dtype=torch.bfloat16, device="cuda")
+        fn(xp, offs, se, a, b, h, y, ws)
+        outs.append((h, y))
+    m.moe_check_device_status(ws)
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 def _sample_rows(seg_offsets, rng, n=48):
     A = int(seg_offsets[-1])
     rows = set(rng.choice(A, size=min(n, A), replace=False).tolist())
