@@ -295,28 +295,32 @@ def run_ours(args, world, rank, local):
 
 
 def run_e2e(layer, logits, x, y, stream, world, K, W):
-    """The same step end to end through the public API: pinned host inputs
-    copied in, the layer, the output copied back, all inside the timer."""
+    """The same step end to end through the public API: every step copies its
+    inputs from pinned host memory and its output back, inside the timer.
+    HostPipeline overlaps step i's copies with the neighbouring steps'
+    compute on separate streams."""
+    from grouped_ffn_gb300.layer import HostPipeline
+    T, E = logits.shape
     logits_h = logits.cpu().pin_memory()
     x_h = x.cpu().pin_memory()
     y_h = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
-    logits_d, x_d, y_d = torch.empty_like(logits), torch.empty_like(x), torch.empty_like(y)
+    pipe = HostPipeline(layer, T, E, depth=2, device=y.device)
     for _ in range(W):
-        layer.forward_host(logits_h, x_h, y_h, logits_d, x_d, y_d, stream)
-    stream.synchronize()
+        pipe.submit(logits_h, x_h, y_h)
+    pipe.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    e0.record(stream)
+    e0.record(pipe.h2d)
     for _ in range(K):
-        layer.forward_host(logits_h, x_h, y_h, logits_d, x_d, y_d, stream)
-    e1.record(stream)
-    stream.synchronize()
+        pipe.submit(logits_h, x_h, y_h)
+    e1.record(pipe.d2h)
+    pipe.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / K
-    layer.check(stream)
+    layer.check(pipe.comp)
     assert torch.equal(y_h, y.cpu()), "end-to-end output differs from the device-resident run"
-    return {"unit": "tokens/s", "ms_per_step": e2e_ms}
+    return {"unit": "tokens/s", "ms_per_step": e2e_ms, "copies": "overlapped (3 streams, 2 buffers)"}
 
 
 def workload_from_args(args) -> wl.Workload:

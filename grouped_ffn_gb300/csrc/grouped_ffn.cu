@@ -34,6 +34,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -50,6 +51,8 @@ constexpr int kStageBytes = kABytes + 2 * kBHalfBytes;
 constexpr int kMaxSegs = 1024;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
+// Workspace: status block, then (from byte 512) one readiness counter per segment.
+constexpr size_t kReadyOff = 512;
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
@@ -70,10 +73,9 @@ constexpr size_t kMiscOff = kBarsOff + sizeof(Bars);
 constexpr size_t kSegOff = kMiscOff + 16;
 constexpr size_t kSmemBytes = kSegOff + (size_t)(3 * kMaxSegs + 2) * 4 + 1024;
 
-struct FfnParams {
-  const int32_t *seg_offsets;
-  const int32_t *seg_expert;
-  int32_t S, E, n_rows, K, n_blocks;
+// One GEMM phase: gate/up with the SwiGLU epilogue (mode 0) or down (mode 1).
+struct Phase {
+  int32_t K, n_blocks;
   int32_t b_rows_per_expert;  // rows of one expert's B matrix (2I or H)
   int32_t b_nblk_stride;      // B row step per n-block (128 or 256)
   int32_t b_second_off;       // row offset of the second 128-row half (I or 128)
@@ -81,8 +83,19 @@ struct FfnParams {
   int32_t out_ld;
   int32_t out_nblk_stride;    // output column step per n-block (128 or 256)
   int32_t mode;               // 0 gate/up + SwiGLU, 1 down
-  int32_t b_packed;           // B in the tile-contiguous layout (see moe_pack_expert_weights)
+  const uint8_t *b_packed_ptr;  // packed weights (L2 prefetch addresses), or null
+};
+
+struct FfnParams {
+  const int32_t *seg_offsets;
+  const int32_t *seg_expert;
+  int32_t S, E, n_rows;
+  int32_t b_packed;   // B in the tile-contiguous layout (see moe_pack_expert_weights)
+  int32_t n_phases;   // 2: phase 1 reads what phase 0 writes, in the same launch
+  int32_t *ready;     // [S] finished phase-0 tiles per segment (zeroed by the host)
   int32_t *status;
+  int32_t pf_depth;   // weight k-blocks prefetched into L2 ahead of the smem ring
+  Phase ph[2];
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -157,6 +170,26 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Orders generic-proxy global writes/reads with async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bulk prefetch of a contiguous global range into L2 (no smem, no barrier).
+__device__ __forceinline__ void prefetch_l2(const void *gptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ int32_t ld_acquire_s32(const int32_t *p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void epilogue_bar() {  // the 128 epilogue threads only
+  asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
@@ -260,21 +293,44 @@ __device__ __forceinline__ void decode_tile(int64_t t, const int32_t *tile_prefi
 }
 
 // --------------------------------------------------------------- the kernel
+struct TileInfo {
+  int ph, s, n_blk, m_blk;
+};
+
+// Tiles [0, T0) are phase 0, [T0, T0 + T1) phase 1; each phase is ordered
+// (segment, n-block, m-block).
+__device__ __forceinline__ TileInfo decode(int64_t t, int64_t T0, const int32_t *tile_prefix,
+                                           int S, int NB0, int NB1) {
+  TileInfo ti;
+  if (t < T0) {
+    ti.ph = 0;
+    decode_tile(t, tile_prefix, S, NB0, ti.s, ti.n_blk, ti.m_blk);
+  } else {
+    ti.ph = 1;
+    decode_tile(t - T0, tile_prefix, S, NB1, ti.s, ti.n_blk, ti.m_blk);
+  }
+  return ti;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                       const __grid_constant__ CUtensorMap tmap_b, const FfnParams p) {
+    grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmap_a0,
+                       const __grid_constant__ CUtensorMap tmap_b0,
+                       const __grid_constant__ CUtensorMap tmap_a1,
+                       const __grid_constant__ CUtensorMap tmap_b1, const FfnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars *bars = reinterpret_cast<Bars *>(smem + kBarsOff);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kMiscOff);
   volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + kMiscOff + 4);
+  // the epilogue's shared go/stop decision, one per accumulator buffer
+  volatile int32_t *epi_ok = reinterpret_cast<int32_t *>(smem + kMiscOff + 8);
   int32_t *seg_off = reinterpret_cast<int32_t *>(smem + kSegOff);  // [S+1]
   int32_t *tile_prefix = seg_off + (kMaxSegs + 1);                 // [S+1]
   int32_t *seg_exp = tile_prefix + (kMaxSegs + 1);                 // [S]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int32_t kid = p.mode == 0 ? moe::K_FFN_GATE_UP : moe::K_FFN_DOWN;
+  const int32_t kid = p.ph[0].mode == 0 ? moe::K_FFN_GATE_UP : moe::K_FFN_DOWN;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -331,28 +387,92 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int NB = p.n_blocks;
-  const int64_t total = (int64_t)tile_prefix[p.S] * NB;
-  const int nk = p.K / kBK;
+  const int NB0 = p.ph[0].n_blocks;
+  const int NB1 = p.n_phases > 1 ? p.ph[1].n_blocks : 0;
+  const int64_t mtot = tile_prefix[p.S];
+  const int64_t T0 = mtot * NB0;
+  const int64_t total = T0 + mtot * NB1;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      prefetch_tmap(&tmap_a);
-      prefetch_tmap(&tmap_b);
+      prefetch_tmap(&tmap_a0);
+      prefetch_tmap(&tmap_b0);
+      if (p.n_phases > 1) {
+        prefetch_tmap(&tmap_a1);
+        prefetch_tmap(&tmap_b1);
+      }
+      // L2 prefetch cursor: runs pf_depth weight k-blocks (32 KiB each,
+      // contiguous in the packed layout) ahead of the TMA loads, across tile
+      // boundaries, so more DRAM requests are in flight than the smem ring
+      // alone allows.  Weights are constant: no ordering is needed.
+      const bool do_pf = p.b_packed && p.pf_depth > 0;
+      int64_t pf_t = blockIdx.x;
+      int pf_kb = 0, pf_nk = 0;
+      const uint8_t *pf_base = nullptr;
+      auto pf_tile = [&]() {
+        if (pf_t >= total) return;
+        const TileInfo pi = decode(pf_t, T0, tile_prefix, p.S, NB0, NB1);
+        const Phase &PP = p.ph[pi.ph];
+        pf_nk = PP.K / kBK;
+        const int nb = pi.ph ? NB1 : NB0;
+        pf_base = PP.b_packed_ptr +
+                  (size_t)((int64_t)(seg_exp[pi.s] * nb + pi.n_blk) * pf_nk) * (2 * kBHalfBytes);
+      };
+      auto pf_next = [&]() {
+        if (pf_t >= total) return;
+        prefetch_l2(pf_base + (size_t)pf_kb * (2 * kBHalfBytes), 2 * kBHalfBytes);
+        if (++pf_kb == pf_nk) {
+          pf_kb = 0;
+          pf_t += gridDim.x;
+          pf_tile();
+        }
+      };
+      if (do_pf) {
+        pf_tile();
+        for (int i = 0; i < p.pf_depth; ++i) pf_next();
+      }
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        int s, n_blk, m_blk;
-        decode_tile(t, tile_prefix, p.S, NB, s, n_blk, m_blk);
-        const int e = seg_exp[s];
-        const int row_a = seg_off[s] + m_blk * kBM;
+        const TileInfo ti = decode(t, T0, tile_prefix, p.S, NB0, NB1);
+        const Phase &P = p.ph[ti.ph];
+        const CUtensorMap *ma = ti.ph ? &tmap_a1 : &tmap_a0;
+        const CUtensorMap *mb = ti.ph ? &tmap_b1 : &tmap_b0;
+        const int NB = ti.ph ? NB1 : NB0;
+        const int nk = P.K / kBK;
+        if (ti.ph == 1) {
+          // every phase-0 tile of this segment must have stored its h rows
+          const int need = (tile_prefix[ti.s + 1] - tile_prefix[ti.s]) * NB0;
+          if (ld_acquire_s32(p.ready + ti.s) < need) {
+            const uint64_t t0 = moe::global_timer_ns();
+            while (ld_acquire_s32(p.ready + ti.s) < need) {
+              if (*abort_flag) {
+                ok = false;
+                break;
+              }
+              const uint64_t dt = moe::global_timer_ns() - t0;
+              if (dt > moe::kWaitLimitNs) {
+                *abort_flag = 1;
+                moe::report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, (int32_t)(dt / 1000), kid);
+                ok = false;
+                break;
+              }
+              __nanosleep(64);
+            }
+            if (!ok) break;
+          }
+          fence_proxy_async_global();
+        }
+        const int e = seg_exp[ti.s];
+        const int row_a = seg_off[ti.s] + ti.m_blk * kBM;
         // B rows of k-block 0; packed: [e][n_blk][kb][half][128 rows][64 cols],
         // so one k-block of the tile is 32 contiguous KiB.
-        const int64_t packed0 = (int64_t)(e * NB + n_blk) * nk * 256;
-        const int row_b0 = p.b_packed ? (int)packed0 : e * p.b_rows_per_expert + n_blk * p.b_nblk_stride;
-        const int row_b1 = p.b_packed ? row_b0 + 128 : row_b0 + p.b_second_off;
+        const int64_t packed0 = (int64_t)(e * NB + ti.n_blk) * nk * 256;
+        const int row_b0 = p.b_packed ? (int)packed0
+                                      : e * P.b_rows_per_expert + ti.n_blk * P.b_nblk_stride;
+        const int row_b1 = p.b_packed ? row_b0 + 128 : row_b0 + P.b_second_off;
         const int b_x_step = p.b_packed ? 0 : kBK;
         const int b_y_step = p.b_packed ? 256 : 0;
         for (int kb = 0; kb < nk; ++kb) {
@@ -362,10 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t *sa = smem + (size_t)stage * kStageBytes;
           mbar_arrive_expect_tx(&bars->full[stage], kStageBytes);
-          tma_load_2d(sa, &tmap_a, kb * kBK, row_a, &bars->full[stage]);
-          tma_load_2d(sa + kABytes, &tmap_b, kb * b_x_step, row_b0 + kb * b_y_step,
-                      &bars->full[stage]);
-          tma_load_2d(sa + kABytes + kBHalfBytes, &tmap_b, kb * b_x_step, row_b1 + kb * b_y_step,
+          tma_load_2d(sa, ma, kb * kBK, row_a, &bars->full[stage]);
+          tma_load_2d(sa + kABytes, mb, kb * b_x_step, row_b0 + kb * b_y_step, &bars->full[stage]);
+          tma_load_2d(sa + kABytes + kBHalfBytes, mb, kb * b_x_step, row_b1 + kb * b_y_step,
                       &bars->full[stage]);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -373,6 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             stage = 0;
             phase ^= 1u;
           }
+          if (do_pf) pf_next();
         }
       }
       for (int i = 0; i < kStages; ++i)  // own copies land before the CTA exits
@@ -385,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int nk = p.ph[t < T0 ? 0 : 1].K / kBK;
         if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, p.status, kid)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
@@ -421,14 +542,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-      int s, n_blk, m_blk;
-      decode_tile(t, tile_prefix, p.S, NB, s, n_blk, m_blk);
-      const int row = seg_off[s] + m_blk * kBM + r_in;
-      const bool valid = row < min(seg_off[s + 1], p.n_rows);
-      if (!mbar_wait(&bars->tfull[acc], acc_phase, abort_flag, p.status, kid)) break;
+      const TileInfo ti = decode(t, T0, tile_prefix, p.S, NB0, NB1);
+      const Phase &P = p.ph[ti.ph];
+      const int row = seg_off[ti.s] + ti.m_blk * kBM + r_in;
+      const bool valid = row < min(seg_off[ti.s + 1], p.n_rows);
+      // One thread waits for the accumulator; all 128 then act on its verdict,
+      // so the named barriers below are always reached by every epilogue warp.
+      if (warp == 2 && lane == 0)
+        epi_ok[acc] = mbar_wait(&bars->tfull[acc], acc_phase, abort_flag, p.status, kid) ? 1 : 0;
+      epilogue_bar();
+      if (!epi_ok[acc]) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN);
-      if (p.mode == 0) {
+      uint16_t *orow = valid ? P.out + (int64_t)row * P.out_ld + (int64_t)ti.n_blk * P.out_nblk_stride
+                             : nullptr;
+      if (P.mode == 0) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t g[32], u[32];
@@ -440,8 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16x2(silu_mul(g[2 * i], u[2 * i]), silu_mul(g[2 * i + 1], u[2 * i + 1]));
           if (valid) {
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + (int64_t)row * p.out_ld +
-                                                   (int64_t)n_blk * p.out_nblk_stride + c * 32);
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -458,8 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
           if (valid) {
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + (int64_t)row * p.out_ld +
-                                                   (int64_t)n_blk * p.out_nblk_stride + c * 32);
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -468,6 +594,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&bars->tempty[acc]);
+      if (p.n_phases > 1 && ti.ph == 0) {
+        // publish this tile's h rows to the phase-1 TMA loads of any CTA
+        fence_proxy_async_global();
+        __threadfence();
+        epilogue_bar();
+        if (warp == 2 && lane == 0) atomicAdd(p.ready + ti.s, 1);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -508,6 +641,17 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Weight k-blocks prefetched into L2 ahead of the TMA loads (packed layout
+// only).  MOE_FFN_PREFETCH_DEPTH overrides the default, for tuning.
+int prefetch_depth() {
+  static int depth = [] {
+    const char *e = getenv("MOE_FFN_PREFETCH_DEPTH");
+    int d = e ? atoi(e) : 0;
+    return d < 0 ? 0 : (d > 64 ? 64 : d);
+  }();
+  return depth;
+}
+
 bool ensure_smem_attr() {
   constexpr int kMaxDevices = 64;
   static bool done[kMaxDevices] = {false};
@@ -521,12 +665,25 @@ bool ensure_smem_attr() {
   return true;
 }
 
-moe_status launch(const CUtensorMap &ma, const CUtensorMap &mb, const FfnParams &p,
-                  int64_t max_tiles, cudaStream_t st) {
+// Cooperative launch: every CTA is resident at once, so a phase-1 tile that
+// waits for phase-0 tiles of other CTAs can always be satisfied.
+moe_status launch(const CUtensorMap &a0, const CUtensorMap &b0, const CUtensorMap &a1,
+                  const CUtensorMap &b1, const FfnParams &p, int64_t max_tiles, cudaStream_t st) {
   int64_t grid = moe_host::sm_count();
   if (max_tiles < grid) grid = max_tiles;
   if (grid < 1) return MOE_OK;
-  grouped_ffn_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(ma, mb, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, grouped_ffn_kernel, a0, b0, a1, b1, p) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return moe_host::launch_status();
 }
 
@@ -562,7 +719,8 @@ moe_status check_ffn_args(const uint16_t *x_perm, int64_t n_rows, const int32_t 
     return MOE_ERR_UNSUPPORTED;
   if ((int64_t)E * 2 * I * (int64_t)H / 64 >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (!seg_offsets || !seg_expert || !w_gate_up || !w_down) return MOE_ERR_INVALID_ARG;
-  if (moe_status s = moe_host::check_ws(ws, ws_bytes, moe::kStatusBytes)) return s;
+  if (moe_status s = moe_host::check_ws(ws, ws_bytes, kReadyOff + (size_t)S * sizeof(int32_t)))
+    return s;
   if (n_rows == 0) return MOE_OK;
   if (!x_perm || !h || !y_perm) return MOE_ERR_INVALID_ARG;
   if (!moe_host::aligned16(x_perm) || !moe_host::aligned16(h) || !moe_host::aligned16(y_perm) ||
@@ -594,38 +752,43 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t m_tiles_max = (n_rows + kBM - 1) / kBM + S;  // sum of ceil(count/128)
-  int32_t *status = moe_host::status_ptr(ws);
+  int32_t *ready = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kReadyOff);
+  if (cudaMemsetAsync(ready, 0, (size_t)S * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
 
-  FfnParams p1{};
-  p1.seg_offsets = seg_offsets;
-  p1.seg_expert = seg_expert;
-  p1.S = S;
-  p1.E = E;
-  p1.n_rows = (int32_t)n_rows;
-  p1.K = H;
-  p1.n_blocks = I / 128;
-  p1.b_rows_per_expert = 2 * I;
-  p1.b_nblk_stride = 128;
-  p1.b_second_off = I;
-  p1.out = h;
-  p1.out_ld = I;
-  p1.out_nblk_stride = 128;
-  p1.mode = 0;
-  p1.b_packed = packed ? 1 : 0;
-  p1.status = status;
-  if (moe_status s = launch(m_x, m_wgu, p1, m_tiles_max * p1.n_blocks, st)) return s;
-
-  FfnParams p2 = p1;
-  p2.K = I;
-  p2.n_blocks = H / 256;
-  p2.b_rows_per_expert = H;
-  p2.b_nblk_stride = 256;
-  p2.b_second_off = 128;
-  p2.out = y_perm;
-  p2.out_ld = H;
-  p2.out_nblk_stride = 256;
-  p2.mode = 1;
-  return launch(m_h, m_wd, p2, m_tiles_max * p2.n_blocks, st);
+  FfnParams p{};
+  p.seg_offsets = seg_offsets;
+  p.seg_expert = seg_expert;
+  p.S = S;
+  p.E = E;
+  p.n_rows = (int32_t)n_rows;
+  p.b_packed = packed ? 1 : 0;
+  p.n_phases = 2;
+  p.ready = ready;
+  p.status = moe_host::status_ptr(ws);
+  p.pf_depth = prefetch_depth();
+  Phase &g = p.ph[0];  // gate/up + SwiGLU -> h
+  g.b_packed_ptr = packed ? reinterpret_cast<const uint8_t *>(w_gate_up) : nullptr;
+  g.K = H;
+  g.n_blocks = I / 128;
+  g.b_rows_per_expert = 2 * I;
+  g.b_nblk_stride = 128;
+  g.b_second_off = I;
+  g.out = h;
+  g.out_ld = I;
+  g.out_nblk_stride = 128;
+  g.mode = 0;
+  Phase &d = p.ph[1];  // down -> y_perm
+  d.K = I;
+  d.n_blocks = H / 256;
+  d.b_rows_per_expert = H;
+  d.b_nblk_stride = 256;
+  d.b_second_off = 128;
+  d.out = y_perm;
+  d.out_ld = H;
+  d.out_nblk_stride = 256;
+  d.mode = 1;
+  d.b_packed_ptr = packed ? reinterpret_cast<const uint8_t *>(w_down) : nullptr;
+  return launch(m_x, m_wgu, m_h, m_wd, p, m_tiles_max * (g.n_blocks + d.n_blocks), st);
 }
 
 }  // namespace

@@ -140,3 +140,54 @@ class MoELayer:
     def check(self, stream=None):
         """Raise MoeError if any kernel recorded a device-side error."""
         moe.moe_check_device_status(self.ws, stream)
+
+
+class HostPipeline:
+    """Steps fed from pinned host memory with the copies overlapped.
+
+    Step i copies its inputs host->device on one stream, runs the layer on a
+    second, and copies its output back on a third; `depth` sets of device
+    input/output buffers let step i+1's input copy and step i-1's output copy
+    run while step i computes.  Events order the three streams; the host
+    never waits inside submit().
+    """
+
+    def __init__(self, layer: MoELayer, T: int, E: int, depth: int = 2, device="cuda"):
+        dev = torch.device(device)
+        self.layer, self.depth = layer, depth
+        self.h2d = torch.cuda.Stream(device=dev)
+        self.comp = torch.cuda.Stream(device=dev)
+        self.d2h = torch.cuda.Stream(device=dev)
+        self.bufs = [dict(logits=torch.empty(T, E, dtype=torch.float32, device=dev),
+                          x=torch.empty(T, layer.H, dtype=torch.bfloat16, device=dev),
+                          y=torch.empty(T, layer.H, dtype=torch.bfloat16, device=dev))
+                     for _ in range(depth)]
+        ev = lambda: [torch.cuda.Event() for _ in range(depth)]
+        self.ev_in, self.ev_comp, self.ev_out = ev(), ev(), ev()
+        self.used = [False] * depth
+        self.i = 0
+
+    def submit(self, logits_host: torch.Tensor, x_host: torch.Tensor, y_host: torch.Tensor):
+        s = self.i % self.depth
+        b = self.bufs[s]
+        if self.used[s]:
+            self.h2d.wait_event(self.ev_comp[s])     # the inputs' last reader is done
+        with torch.cuda.stream(self.h2d):
+            b["logits"].copy_(logits_host, non_blocking=True)
+            b["x"].copy_(x_host, non_blocking=True)
+        self.ev_in[s].record(self.h2d)
+        self.comp.wait_event(self.ev_in[s])
+        if self.used[s]:
+            self.comp.wait_event(self.ev_out[s])     # the output's last copy is done
+        self.layer.forward(b["logits"], b["x"], b["y"], self.comp)
+        self.ev_comp[s].record(self.comp)
+        self.d2h.wait_event(self.ev_comp[s])
+        with torch.cuda.stream(self.d2h):
+            y_host.copy_(b["y"], non_blocking=True)
+        self.ev_out[s].record(self.d2h)
+        self.used[s] = True
+        self.i += 1
+
+    def synchronize(self):
+        for st in (self.h2d, self.comp, self.d2h):
+            st.synchronize()

@@ -93,7 +93,8 @@ typedef struct moe_placement {
 
 /* Bytes of device workspace needed by moe_dispatch_layout for T tokens,
  * top-k and n_slots slots (a 256-byte status block plus the scan's tile
- * flags).  Every other call needs only the status block
+ * flags); it also covers moe_grouped_ffn with up to n_slots segments.
+ * Route, permute, combine and balance need only the status block
  * (MOE_WS_STATUS_BYTES).  Returns 0 for invalid sizes. */
 #define MOE_WS_STATUS_BYTES 256
 size_t moe_workspace_size(int64_t T, int32_t k, int32_t n_slots);
@@ -210,8 +211,12 @@ moe_status moe_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
  *  h          device bf16 [n_rows, I] (intermediate, written)
  *  y_perm     device bf16 [n_rows, H]
  *  Rows outside every segment are left unwritten.  Uses tcgen05 tensor
- *  cores with TMA-fed shared memory and TMEM accumulators.
- *  Limits: H % 256 == 0, I % 128 == 0, S <= 1024, n_rows < 2^31.
+ *  cores with TMA-fed shared memory and TMEM accumulators; both GEMMs run
+ *  in one cooperative launch, a segment's down-projection tiles starting
+ *  as soon as all its gate/up tiles have stored h.
+ *  ws: at least 512 + 4*S bytes (moe_workspace_size(T, k, S) is enough).
+ *  Limits: H % 256 == 0, I % 128 == 0, S <= 1024, n_rows < 2^31,
+ *  E*2I*H/64 < 2^31.
  *  Device errors: MOE_ERR_DEVICE_INDEX (expert id), MOE_ERR_DEVICE_TIMEOUT. */
 moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_offsets,
                            const int32_t *seg_expert, int32_t S, int32_t E,

@@ -298,7 +298,7 @@ def _ffn_case(w, offsets, seg_expert, dev="cuda"):
     wd = wl.make_w_down(w, dev)
     h = torch.full((n_rows, w.I), float("nan"), dtype=torch.bfloat16, device=dev)
     yp = torch.full((n_rows, w.H), float("nan"), dtype=torch.bfloat16, device=dev)
-    ws = m.new_workspace(1, 1, 1)
+    ws = m.new_workspace(1, 1, len(seg_expert))
     offs_t = torch.tensor(offsets, dtype=torch.int32, device=dev)
     exp_t = torch.tensor(seg_expert, dtype=torch.int32, device=dev)
     m.moe_grouped_ffn(xp, offs_t, exp_t, wgu, wd, h, yp, ws)
@@ -348,7 +348,7 @@ def test_packed_ffn_is_bit_identical_to_plain(H, I, counts):
     want_gu = wgu.view(E, 2, NB1, 128, nk1, 64).permute(0, 2, 4, 1, 3, 5).reshape(E, 2 * I, H)
     want_d = wd.view(E, NB2, 2, 128, nk2, 64).permute(0, 1, 4, 2, 3, 5).reshape(E, H, I)
     assert torch.equal(pgu, want_gu) and torch.equal(pd, want_d)
-    ws = m.new_workspace(1, 1, 1)
+    ws = m.new_workspace(1, 1, len(counts))
     outs = []
     for fn, a, b in ((m.moe_grouped_ffn, wgu, wd), (m.moe_grouped_ffn_packed, pgu, pd)):
         h = torch.zeros(n, I, dtype=torch.bfloat16, device="cuda")
