@@ -50,6 +50,36 @@ def load_peaks():
                     source="fallback")
 
 
+# ------------------------------------------------------------------ ncu traffic
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "grouped_ffn_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "grouped_ffn_gb300", "csrc", f)
+                  for f in ("grouped_ffn.cu", "common.cuh")]
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes (read + write) per grouped-FFN launch from the committed ncu
+    capture, or None if there is none for this workload or the kernel source
+    changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_sha256") != kernel_source_hash():
+        return None
+    w = rec.get("workloads", {}).get(workload)
+    return None if w is None else int(w["dram_bytes_read"]) + int(w["dram_bytes_write"])
+
+
 # ------------------------------------------------------------------ dist
 def dist_setup(n_gpus):
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -261,7 +291,9 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "tensor", "achieved": g["flops"] / (g_ms * 1e-3) / 1e12,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(w.name)
+    roof["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, " +
+                              os.path.relpath(TRAFFIC_FILE, ROOT)) if roof["traffic"] else None
     roof["kernel"] = "grouped_ffn_kernel (gate/up + down launches)"
     roof["peak_source"] = peaks["source"] + (" sustained" if roof["bound"] == "tensor" else "")
     roof["algorithmic_bytes_per_step"] = g["bytes"]

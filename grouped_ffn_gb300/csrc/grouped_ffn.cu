@@ -71,7 +71,7 @@ struct __align__(8) Bars {
 constexpr size_t kBarsOff = (size_t)kStages * kStageBytes;
 constexpr size_t kMiscOff = kBarsOff + sizeof(Bars);
 constexpr size_t kSegOff = kMiscOff + 16;
-constexpr size_t kSmemBytes = kSegOff + (size_t)(3 * kMaxSegs + 2) * 4 + 1024;
+constexpr size_t kSmemBytes = kSegOff + (size_t)(4 * kMaxSegs + 3) * 4 + 1024;
 
 // One GEMM phase: gate/up with the SwiGLU epilogue (mode 0) or down (mode 1).
 struct Phase {
@@ -83,7 +83,6 @@ struct Phase {
   int32_t out_ld;
   int32_t out_nblk_stride;    // output column step per n-block (128 or 256)
   int32_t mode;               // 0 gate/up + SwiGLU, 1 down
-  const uint8_t *b_packed_ptr;  // packed weights (L2 prefetch addresses), or null
 };
 
 struct FfnParams {
@@ -93,8 +92,8 @@ struct FfnParams {
   int32_t b_packed;   // B in the tile-contiguous layout (see moe_pack_expert_weights)
   int32_t n_phases;   // 2: phase 1 reads what phase 0 writes, in the same launch
   int32_t *ready;     // [S] finished phase-0 tiles per segment (zeroed by the host)
+  int32_t interleave; // merge multi-tile and one-tile segments' tiles (see decode)
   int32_t *status;
-  int32_t pf_depth;   // weight k-blocks prefetched into L2 ahead of the smem ring
   Phase ph[2];
 };
 
@@ -175,11 +174,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
 // Orders generic-proxy global writes/reads with async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Bulk prefetch of a contiguous global range into L2 (no smem, no barrier).
-__device__ __forceinline__ void prefetch_l2(const void *gptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ int32_t ld_acquire_s32(const int32_t *p) {
@@ -297,19 +291,50 @@ struct TileInfo {
   int ph, s, n_blk, m_blk;
 };
 
-// Tiles [0, T0) are phase 0, [T0, T0 + T1) phase 1; each phase is ordered
-// (segment, n-block, m-block).
-__device__ __forceinline__ TileInfo decode(int64_t t, int64_t T0, const int32_t *tile_prefix,
-                                           int S, int NB0, int NB1) {
+// Tiles [0, T0) are phase 0, [T0, T0 + T1) phase 1.  Within a phase two
+// streams are merged in proportion to their lengths (u -> hot if
+// floor((u+1) Lh / L) > floor(u Lh / L)): the "hot" stream holds segments
+// with two or more 128-row tiles, whose weight tiles are re-read from L2 and
+// so lean on the tensor cores; the "cold" stream holds one-tile segments,
+// which stream fresh weights from HBM.  Each stream is ordered (segment,
+// n-block, m-block), so a segment's A rows and a weight tile's m-blocks stay
+// close in time, while every wave of CTAs mixes both kinds of work.
+__device__ __forceinline__ TileInfo decode(int64_t t, int64_t T0, const int32_t *pre_h,
+                                           const int32_t *pre_c, int S, int NB0, int NB1,
+                                           int64_t Mh, int64_t Mc) {
   TileInfo ti;
-  if (t < T0) {
-    ti.ph = 0;
-    decode_tile(t, tile_prefix, S, NB0, ti.s, ti.n_blk, ti.m_blk);
-  } else {
-    ti.ph = 1;
-    decode_tile(t - T0, tile_prefix, S, NB1, ti.s, ti.n_blk, ti.m_blk);
-  }
+  ti.ph = t < T0 ? 0 : 1;
+  const int64_t u = ti.ph ? t - T0 : t;
+  const int NB = ti.ph ? NB1 : NB0;
+  const int64_t Lh = Mh * NB, L = (Mh + Mc) * NB;
+  const int64_t hb = u * Lh / L;
+  if ((u + 1) * Lh / L > hb)
+    decode_tile(hb, pre_h, S, NB, ti.s, ti.n_blk, ti.m_blk);
+  else
+    decode_tile(u - hb, pre_c, S, NB, ti.s, ti.n_blk, ti.m_blk);
   return ti;
+}
+
+// In-place exclusive scan of a[0..n) by one warp (lane L owns a chunk);
+// a[n] receives the total.
+__device__ __forceinline__ void warp_exclusive_scan(int32_t *a, int n, int lane) {
+  const int per = (n + 31) / 32;
+  const int lo = lane * per, hi = min(n, lo + per);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) sum += a[i];
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int run = incl - sum;
+  for (int i = lo; i < hi; ++i) {
+    const int c = a[i];
+    a[i] = run;
+    run += c;
+  }
+  if (lane == 31) a[n] = incl;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -326,8 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the epilogue's shared go/stop decision, one per accumulator buffer
   volatile int32_t *epi_ok = reinterpret_cast<int32_t *>(smem + kMiscOff + 8);
   int32_t *seg_off = reinterpret_cast<int32_t *>(smem + kSegOff);  // [S+1]
-  int32_t *tile_prefix = seg_off + (kMaxSegs + 1);                 // [S+1]
-  int32_t *seg_exp = tile_prefix + (kMaxSegs + 1);                 // [S]
+  int32_t *pre_h = seg_off + (kMaxSegs + 1);  // [S+1] m-tiles before s, multi-tile segments
+  int32_t *pre_c = pre_h + (kMaxSegs + 1);    // [S+1] m-tiles before s, one-tile segments
+  int32_t *seg_exp = pre_c + (kMaxSegs + 1);  // [S]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t kid = p.ph[0].mode == 0 ? moe::K_FFN_GATE_UP : moe::K_FFN_DOWN;
@@ -361,35 +387,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, s, kid);
       mt = 0;
     }
-    tile_prefix[s] = mt;
+    const bool hot = p.interleave && mt >= 2;
+    pre_h[s] = hot ? mt : 0;
+    pre_c[s] = hot ? 0 : mt;
   }
   __syncthreads();
-  if (warp == 0) {  // exclusive scan of the m-tile counts; lane L owns a chunk
-    const int per = (p.S + 31) / 32;
-    const int lo = lane * per, hi = min(p.S, lo + per);
-    int sum = 0;
-    for (int s = lo; s < hi; ++s) sum += tile_prefix[s];
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    int run = incl - sum;
-    for (int s = lo; s < hi; ++s) {
-      const int c = tile_prefix[s];
-      tile_prefix[s] = run;
-      run += c;
-    }
-    if (lane == 31) tile_prefix[p.S] = incl;
-  }
+  if (warp == 0) warp_exclusive_scan(pre_h, p.S, lane);
+  if (warp == 2) warp_exclusive_scan(pre_c, p.S, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int NB0 = p.ph[0].n_blocks;
   const int NB1 = p.n_phases > 1 ? p.ph[1].n_blocks : 0;
-  const int64_t mtot = tile_prefix[p.S];
+  const int64_t Mh = pre_h[p.S], Mc = pre_c[p.S];
+  const int64_t mtot = Mh + Mc;
   const int64_t T0 = mtot * NB0;
   const int64_t total = T0 + mtot * NB1;
 
@@ -402,41 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmap_a1);
         prefetch_tmap(&tmap_b1);
       }
-      // L2 prefetch cursor: runs pf_depth weight k-blocks (32 KiB each,
-      // contiguous in the packed layout) ahead of the TMA loads, across tile
-      // boundaries, so more DRAM requests are in flight than the smem ring
-      // alone allows.  Weights are constant: no ordering is needed.
-      const bool do_pf = p.b_packed && p.pf_depth > 0;
-      int64_t pf_t = blockIdx.x;
-      int pf_kb = 0, pf_nk = 0;
-      const uint8_t *pf_base = nullptr;
-      auto pf_tile = [&]() {
-        if (pf_t >= total) return;
-        const TileInfo pi = decode(pf_t, T0, tile_prefix, p.S, NB0, NB1);
-        const Phase &PP = p.ph[pi.ph];
-        pf_nk = PP.K / kBK;
-        const int nb = pi.ph ? NB1 : NB0;
-        pf_base = PP.b_packed_ptr +
-                  (size_t)((int64_t)(seg_exp[pi.s] * nb + pi.n_blk) * pf_nk) * (2 * kBHalfBytes);
-      };
-      auto pf_next = [&]() {
-        if (pf_t >= total) return;
-        prefetch_l2(pf_base + (size_t)pf_kb * (2 * kBHalfBytes), 2 * kBHalfBytes);
-        if (++pf_kb == pf_nk) {
-          pf_kb = 0;
-          pf_t += gridDim.x;
-          pf_tile();
-        }
-      };
-      if (do_pf) {
-        pf_tile();
-        for (int i = 0; i < p.pf_depth; ++i) pf_next();
-      }
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = decode(t, T0, tile_prefix, p.S, NB0, NB1);
+        const TileInfo ti = decode(t, T0, pre_h, pre_c, p.S, NB0, NB1, Mh, Mc);
         const Phase &P = p.ph[ti.ph];
         const CUtensorMap *ma = ti.ph ? &tmap_a1 : &tmap_a0;
         const CUtensorMap *mb = ti.ph ? &tmap_b1 : &tmap_b0;
@@ -444,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nk = P.K / kBK;
         if (ti.ph == 1) {
           // every phase-0 tile of this segment must have stored its h rows
-          const int need = (tile_prefix[ti.s + 1] - tile_prefix[ti.s]) * NB0;
+          const int need =
+              (pre_h[ti.s + 1] - pre_h[ti.s] + pre_c[ti.s + 1] - pre_c[ti.s]) * NB0;
           if (ld_acquire_s32(p.ready + ti.s) < need) {
             const uint64_t t0 = moe::global_timer_ns();
             while (ld_acquire_s32(p.ready + ti.s) < need) {
@@ -492,7 +475,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             stage = 0;
             phase ^= 1u;
           }
-          if (do_pf) pf_next();
         }
       }
       for (int i = 0; i < kStages; ++i)  // own copies land before the CTA exits
@@ -542,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode(t, T0, tile_prefix, p.S, NB0, NB1);
+      const TileInfo ti = decode(t, T0, pre_h, pre_c, p.S, NB0, NB1, Mh, Mc);
       const Phase &P = p.ph[ti.ph];
       const int row = seg_off[ti.s] + ti.m_blk * kBM + r_in;
       const bool valid = row < min(seg_off[ti.s + 1], p.n_rows);
@@ -641,15 +623,14 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Weight k-blocks prefetched into L2 ahead of the TMA loads (packed layout
-// only).  MOE_FFN_PREFETCH_DEPTH overrides the default, for tuning.
-int prefetch_depth() {
-  static int depth = [] {
-    const char *e = getenv("MOE_FFN_PREFETCH_DEPTH");
-    int d = e ? atoi(e) : 0;
-    return d < 0 ? 0 : (d > 64 ? 64 : d);
+// Tile order: 1 (default) merges multi-tile and one-tile segments (see
+// decode); MOE_FFN_INTERLEAVE=0 keeps plain segment order, for comparison.
+int interleave_tiles() {
+  static int v = [] {
+    const char *e = getenv("MOE_FFN_INTERLEAVE");
+    return (e && e[0] == '0') ? 0 : 1;
   }();
-  return depth;
+  return v;
 }
 
 bool ensure_smem_attr() {
@@ -765,9 +746,8 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   p.n_phases = 2;
   p.ready = ready;
   p.status = moe_host::status_ptr(ws);
-  p.pf_depth = prefetch_depth();
+  p.interleave = interleave_tiles();
   Phase &g = p.ph[0];  // gate/up + SwiGLU -> h
-  g.b_packed_ptr = packed ? reinterpret_cast<const uint8_t *>(w_gate_up) : nullptr;
   g.K = H;
   g.n_blocks = I / 128;
   g.b_rows_per_expert = 2 * I;
@@ -787,7 +767,6 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   d.out_ld = H;
   d.out_nblk_stride = 256;
   d.mode = 1;
-  d.b_packed_ptr = packed ? reinterpret_cast<const uint8_t *>(w_down) : nullptr;
   return launch(m_x, m_wgu, m_h, m_wd, p, m_tiles_max * (g.n_blocks + d.n_blocks), st);
 }
 

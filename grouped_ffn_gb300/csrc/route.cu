@@ -13,8 +13,11 @@
 // IEEE values (so -0 == +0 and ties go to the lower id).
 //
 // GB300 issues fp64 at a small fraction of the fp32 rate, so fp64 is used
-// only where a floating value decides an integer: each lane computes its own
-// group's score (the fp64 sum of fp64 sigmoids), all groups in parallel.
+// only where a floating value decides an integer, and only when needed:
+// group scores (the fp64 sum of fp64 sigmoids, by definition) are first
+// computed in fp32, one group per lane; the kept set is provably the fp64
+// one unless the fp32 margin at the cut is within the fp32 error bound, and
+// only then does the warp recompute the scores in fp64.
 // Weights are fp32: the softmax exponent l_j - l_max is split error-free
 // (TwoSum) into hi + lo and exp(hi + lo) = expf(hi) * (1 + lo); the k terms
 // are summed with a TwoSum-compensated butterfly; one IEEE division.  The
@@ -68,6 +71,69 @@ __device__ __forceinline__ void warp_argmax(const float (&v)[VPL], uint32_t mask
 
 constexpr int kMaxGroupTopn = 8;
 
+__device__ __forceinline__ float sigmoid32(float x) {
+  return __frcp_rn(__fadd_rn(1.0f, expf(-x)));
+}
+
+__device__ __forceinline__ float sigmoid_of(float x, float) { return sigmoid32(x); }
+__device__ __forceinline__ double sigmoid_of(float x, double) { return sigmoid64(x); }
+
+// Lane g returns group g's score: the sum, in descending order, of the
+// sigmoids (in precision F) of the group's top_n largest logits.
+template <int VPL, typename F>
+__device__ F group_score(const float (&v)[VPL], uint32_t avail, int lane, int n_groups, int gsz,
+                         int top_n) {
+  F mine = (F)0;
+  for (int g = 0; g < n_groups; ++g) {
+    uint32_t gmask = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (((avail >> i) & 1u) && (lane + 32 * i) / gsz == g) gmask |= 1u << i;
+    for (int r = 0; r < top_n; ++r) {
+      float bv;
+      int bid;
+      warp_argmax<VPL>(v, gmask, lane, bv, bid);
+      if (lane == g) mine = mine + sigmoid_of(bv, (F)0);
+      if ((bid & 31) == lane) gmask &= ~(1u << (bid >> 5));
+    }
+  }
+  return mine;
+}
+
+// Bit mask of the n_sel best groups (lane g holds group g's score; ties to
+// the lower id), with the score of the last one kept and of the best one
+// left out (-inf if none).
+template <typename F>
+__device__ __forceinline__ uint32_t select_groups(F my_score, bool valid, int lane, int n_sel,
+                                                  F &last_kept, F &best_dropped) {
+  bool free_ = valid;
+  uint32_t kept = 0;
+  last_kept = (F)0;
+  best_dropped = -(F)INFINITY;
+  for (int r = 0; r <= n_sel; ++r) {
+    F bs = free_ ? my_score : (F)0;
+    int bg = free_ ? lane : INT_MAX;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const F os = __shfl_xor_sync(0xffffffffu, bs, off);
+      const int og = __shfl_xor_sync(0xffffffffu, bg, off);
+      if (og != INT_MAX && (bg == INT_MAX || os > bs || (os == bs && og < bg))) {
+        bs = os;
+        bg = og;
+      }
+    }
+    if (bg == INT_MAX) break;  // no group left
+    if (r == n_sel) {
+      best_dropped = bs;
+      break;
+    }
+    kept |= 1u << bg;
+    last_kept = bs;
+    if (lane == bg) free_ = false;
+  }
+  return kept;
+}
+
 // s + e == a + b exactly (round-to-nearest, no overflow).
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
   s = __fadd_rn(a, b);
@@ -114,52 +180,26 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
     }
 
     if (a.n_groups > 1) {
-      // Group score: fp64 sum of the sigmoids of the group's group_topn
-      // largest logits, taken in descending order.  Lane g collects group
-      // g's values, then every lane scores its own group in parallel.
-      float gv[kMaxGroupTopn];
-#pragma unroll
-      for (int r = 0; r < kMaxGroupTopn; ++r) gv[r] = 0.0f;
-      for (int g = 0; g < a.n_groups; ++g) {
-        uint32_t gmask = 0;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i)
-          if (((avail >> i) & 1u) && (lane + 32 * i) / gsz == g) gmask |= 1u << i;
-#pragma unroll
-        for (int r = 0; r < kMaxGroupTopn; ++r) {
-          if (r < a.group_topn) {
-            float bv;
-            int bid;
-            warp_argmax<VPL>(v, gmask, lane, bv, bid);
-            if (lane == g) gv[r] = bv;
-            if ((bid & 31) == lane) gmask &= ~(1u << (bid >> 5));
-          }
-        }
-      }
-      double my_gscore = 0.0;
-      if (lane < a.n_groups) {
-#pragma unroll
-        for (int r = 0; r < kMaxGroupTopn; ++r)
-          if (r < a.group_topn) my_gscore += sigmoid64(gv[r]);
-      }
-      // Keep the topk_groups best groups (score descending, id ascending).
-      bool gfree = lane < a.n_groups;
-      uint32_t kept = 0;
-      for (int r = 0; r < a.topk_groups; ++r) {
-        double bs = gfree ? my_gscore : 0.0;
-        int bg = gfree ? lane : INT_MAX;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          double os = __shfl_xor_sync(0xffffffffu, bs, off);
-          int og = __shfl_xor_sync(0xffffffffu, bg, off);
-          bool take = og != INT_MAX && (bg == INT_MAX || os > bs || (os == bs && og < bg));
-          if (take) {
-            bs = os;
-            bg = og;
-          }
-        }
-        kept |= 1u << bg;
-        if (lane == bg) gfree = false;
+      // Group score: the sum of the sigmoids of the group's group_topn
+      // largest logits, taken in descending order; lane g accumulates group
+      // g's.  Keep the topk_groups best groups (score descending, id
+      // ascending).  The fp32 scores satisfy |s32 - s64| <= eps (expf within
+      // 2 ulp, one rounding each for 1 + e, the reciprocal and every add).
+      // If the last kept group beats the best dropped one by more than 2 eps
+      // the fp64 selection is the same set; otherwise the warp recomputes
+      // the scores in fp64 and selects again.
+      const bool gvalid = lane < a.n_groups;
+      const float my_g32 = group_score<VPL, float>(v, avail, lane, a.n_groups, gsz, a.group_topn);
+      float last_kept, best_dropped;
+      uint32_t kept = select_groups<float>(my_g32, gvalid, lane, a.topk_groups, last_kept,
+                                           best_dropped);
+      const float n = (float)a.group_topn;
+      const float eps = n * 2e-7f + (n - 1.0f) * n * 6e-8f;
+      if (a.topk_groups < a.n_groups && !(last_kept - best_dropped > 4.0f * eps)) {
+        const double my_g64 =
+            group_score<VPL, double>(v, avail, lane, a.n_groups, gsz, a.group_topn);
+        double l64, b64;
+        kept = select_groups<double>(my_g64, gvalid, lane, a.topk_groups, l64, b64);
       }
 #pragma unroll
       for (int i = 0; i < VPL; ++i)

@@ -133,6 +133,32 @@ def test_route_group_limited_small_groups():
         np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
 
 
+def test_route_group_limited_near_ties_decided_in_fp64():
+    """Groups whose scores differ by less than fp32 can resolve: the kernel
+    must fall back to the fp64 definition and agree with the oracle, and
+    exact ties must go to the lower group id."""
+    rng = np.random.default_rng(21)
+    E, n_groups, gsz, T = 64, 8, 8, 512
+    lg = np.full((T, E), -6.0, np.float32)
+    one = np.float32(1.0)
+    for t in range(T):
+        a, b = rng.choice(n_groups, size=2, replace=False)
+        ulps = int(rng.integers(0, 4))             # 0 = exact tie
+        lg[t, a * gsz:a * gsz + 2] = [one, one]
+        hi = one
+        for _ in range(ulps):
+            hi = np.nextafter(hi, np.float32(2.0))
+        lg[t, b * gsz:b * gsz + 2] = [one, hi]
+        lg[t, rng.integers(0, E)] += np.float32(rng.uniform(-1e-3, 0.0))   # noise elsewhere
+    w = wl.Workload("nt", 0, T=T, H=8, E=E, k=2, I=8, R=1, ranks_per_node=1,
+                    score_fn=wl.SCORE_SIGMOID, n_groups=n_groups, topk_groups=1, group_topn=2)
+    ids, wts = gpu_route(w, torch.from_numpy(lg).cuda())
+    rid, rw, margin = oracle_route(w, lg)
+    assert margin < 1e-7                           # the cases really are near ties
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
+
+
 # ------------------------------------------------------------------ layout + balance
 @pytest.mark.parametrize("name,zipf", [(n, None) for n in ALL] +
                          [("replica", s) for s in (0.0, 0.5, 1.5)])
