@@ -184,15 +184,22 @@ def dispatch_layout(topk_ids: np.ndarray, pl) -> Dict[str, np.ndarray]:
     order, append each to its slot's list, concatenate the lists.
     """
     T, k = topk_ids.shape
+    A = T * k
+    slot = np.array([choose_slot(int(topk_ids[a // k, a % k]), a // k, pl) for a in range(A)],
+                    dtype=np.int32)
+    return dispatch_layout_from_slots(topk_ids, slot, pl)
+
+
+def dispatch_layout_from_slots(topk_ids: np.ndarray, slot: np.ndarray, pl) -> Dict[str, np.ndarray]:
+    """The same packing when each assignment's slot is already chosen (for
+    example by route_replicas_waterfill)."""
+    T, k = topk_ids.shape
     S = pl.n_slots
     A = T * k
-    slot = np.empty(A, dtype=np.int32)
+    slot = np.asarray(slot, dtype=np.int32)
     lists = [[] for _ in range(S)]
     for a in range(A):
-        t = a // k
-        s = choose_slot(int(topk_ids[t, a % k]), t, pl)
-        slot[a] = s
-        lists[s].append(a)
+        lists[int(slot[a])].append(a)
     seg_counts = np.array([len(l) for l in lists], dtype=np.int32)
     seg_offsets = np.zeros(S + 1, dtype=np.int32)
     seg_offsets[1:] = np.cumsum(seg_counts)
@@ -380,3 +387,131 @@ def moe_layer_tokens(tokens, logits, x_bits, w_gate_up, w_down, pl, route_cfg,
             acc = acc + w32[i, j] * ye[0]
         out[i] = bf16_round(acc)
     return out
+
+
+# ------------------------------------------------------------------ replica routing
+def replica_bounds(D: int, n: int, c_num: int, c_den: int):
+    """Integer load targets and bounds for one expert's n replicas.
+
+    [Zepp] Section 4.1 (Eq. 1): q_j is the expert's total demand divided
+    evenly over its replicas, and each replica's load must stay within
+    C * q_j of it; Section 5 rounds these to integers.  Reading: the
+    integer even split q_p = floor(D/n) + (p < D mod n), slack
+    floor(C * D / n) with C = c_num / c_den, bounds q_p -+ slack (lower
+    bound at least 0).  sum(lo) <= D <= sum(hi) always holds."""
+    base, rem = divmod(D, n)
+    q = [base + (1 if p < rem else 0) for p in range(n)]
+    slack = (c_num * D) // (c_den * n)
+    lo = [max(0, qp - slack) for qp in q]
+    hi = [qp + slack for qp in q]
+    return q, lo, hi
+
+
+def waterfill_expert(demand, rep_ranks, ranks_per_node, c_num, c_den):
+    """Greedy water-filling of one expert's demand over its replicas.
+
+    [Zepp] Section 5, "Routing": replicas on the source GPU are considered
+    first, then other GPUs of the same node, then remote nodes; each
+    allocation is limited by the receiving replica's remaining capacity
+    while reserving enough unassigned demand for the other replicas' lower
+    bounds.  Sources are taken in ascending rank, replicas in ascending
+    rank within each pass.  A fourth pass places any demand the reserve
+    rule held back: first into replicas still below their lower bound, then
+    into any replica with capacity (this always completes: see the design
+    notes).
+
+    demand: dict rank -> count; rep_ranks: ascending ranks of the replicas.
+    Returns (allocations, loads, lo, hi) with allocations a dict
+    rank -> list of (replica position, count) in the order made.
+    """
+    n = len(rep_ranks)
+    D = sum(demand.values())
+    _, lo, hi = replica_bounds(D, n, c_num, c_den)
+    load = [0] * n
+    left = dict(demand)
+    alloc = {i: [] for i in demand}
+    U = D
+    node = lambda r: r // ranks_per_node
+
+    def give(i, p, x):
+        nonlocal U
+        if x <= 0:
+            return
+        left[i] -= x
+        load[p] += x
+        U -= x
+        alloc[i].append((p, x))
+
+    def allow(p):
+        others = sum(max(0, lo[q] - load[q]) for q in range(n) if q != p)
+        return max(0, min(hi[p] - load[p], U - others))
+
+    sources = sorted(demand)
+    passes = [lambda i, r: r == i,
+              lambda i, r: r != i and node(r) == node(i),
+              lambda i, r: node(r) != node(i)]
+    for in_pass in passes:
+        for i in sources:
+            for p in range(n):
+                if left[i] > 0 and in_pass(i, rep_ranks[p]):
+                    give(i, p, min(left[i], allow(p)))
+    for i in sources:
+        for p in range(n):
+            if left[i] > 0 and lo[p] - load[p] > 0:
+                give(i, p, min(left[i], lo[p] - load[p]))
+        for p in range(n):
+            if left[i] > 0:
+                give(i, p, min(left[i], hi[p] - load[p]))
+    assert U == 0
+    return alloc, load, lo, hi
+
+
+def locality_order(i: int, rep_ranks, ranks_per_node: int):
+    """Replica positions in the order source rank i prefers them: its own
+    GPU, then its node (ascending rank), then remote (ascending rank)."""
+    node = lambda r: r // ranks_per_node
+    n = len(rep_ranks)
+    return ([p for p in range(n) if rep_ranks[p] == i] +
+            [p for p in range(n) if rep_ranks[p] != i and node(rep_ranks[p]) == node(i)] +
+            [p for p in range(n) if node(rep_ranks[p]) != node(i)])
+
+
+def route_replicas_waterfill(topk_ids: np.ndarray, pl, c_num: int, c_den: int):
+    """Locality-preferred choice of the replica serving each assignment
+    ([Zepp] Section 4.1 "Locality-preferred token routing" and Section 5).
+
+    Per expert with several replicas: demand d_i = assignments of that
+    expert whose token lives on rank i; the water-filling above fixes how
+    many of rank i's assignments each replica serves (M[i][p]); rank i's
+    assignments, in ascending order, then fill those destinations in its
+    locality order (own GPU, own node, remote; ascending rank within each).  Experts
+    with one replica keep it.  Returns (slot [A] int32, inter_node count)."""
+    T, k = topk_ids.shape
+    A = T * k
+    ids = topk_ids.reshape(-1)
+    src = np.array([int(pl.token_src_rank[a // k]) if pl.token_src_rank is not None
+                    else (a // k) % pl.n_ranks for a in range(A)])
+    slot = np.empty(A, dtype=np.int32)
+    for e in range(pl.n_experts):
+        reps = [int(s) for s in pl.rep_slots[pl.rep_offsets[e]:pl.rep_offsets[e + 1]]]
+        mine = np.nonzero(ids == e)[0]
+        if len(reps) == 1:
+            slot[mine] = reps[0]
+            continue
+        rep_ranks = [int(pl.slot_rank[s]) for s in reps]
+        demand = {}
+        for a in mine:
+            demand[int(src[a])] = demand.get(int(src[a]), 0) + 1
+        alloc, _, _, _ = waterfill_expert(demand, rep_ranks, pl.ranks_per_node, c_num, c_den)
+        for i, lst in alloc.items():
+            count = [0] * len(reps)                          # M[i][p]
+            for p, x in lst:
+                count[p] += x
+            rows = [a for a in mine if src[a] == i]          # ascending assignment order
+            pos = 0
+            for p in locality_order(i, rep_ranks, pl.ranks_per_node):
+                slot[rows[pos:pos + count[p]]] = reps[p]
+                pos += count[p]
+    node_of = lambda r: r // pl.ranks_per_node
+    inter = int(sum(node_of(int(pl.slot_rank[slot[a]])) != node_of(int(src[a])) for a in range(A)))
+    return slot, inter
