@@ -209,23 +209,18 @@ def run_ours(args, world, rank, local):
                      w_gate_up=wgu, w_down=wd, max_tokens=w.T, score_fn=w.score_fn,
                      n_groups=w.n_groups, topk_groups=w.topk_groups, group_topn=w.group_topn,
                      shared_w_gate_up=sgu, shared_w_down=sd, device=dev,
-                     packed=not args.unpacked)
+                     packed=not args.unpacked, replica_relax=parse_relax(args.replica_relax))
     y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    # per-stage events, recorded on the launching stream
     names = ["route", "layout", "permute", "grouped_ffn"] + (["shared_ffn"] if w.shared_I else []) \
         + ["combine", "balance"]
+    ffn_stages = ["grouped_ffn"] + (["shared_ffn"] if w.shared_I else [])
     K, W = args.steps, args.warmup
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    ET = lambda: torch.cuda.Event(enable_timing=True)
 
-    def step(i=None):
-        if i is None:
-            layer.forward(logits, x, y, stream)
-            return
-        marks = iter(ev[i][1:])
-        ev[i][0].record(stream)
-        layer.forward(logits, x, y, stream, mark=lambda n: next(marks).record(stream))
+    def step(marks=None):
+        layer.forward(logits, x, y, stream, mark=marks)
 
     with torch.cuda.stream(stream):
         for _ in range(W):
@@ -233,7 +228,24 @@ def run_ours(args, world, rank, local):
     stream.synchronize()
     layer.check(stream)
 
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Timed region: K whole steps.  The only events inside it bracket the
+    # grouped-FFN launches (their duration feeds the roofline); the other
+    # stages run back to back with programmatic dependent launch.
+    ffn_ev = [[ET() for _ in range(2 * len(ffn_stages))] for _ in range(K)]
+
+    def timed_marks(i):
+        evs = ffn_ev[i]
+        slot = {"permute": 0, "grouped_ffn": 1}
+        if w.shared_I:
+            slot.update({"grouped_ffn": 1, "shared_ffn": 3})
+        def mark(name):
+            if name in slot:
+                evs[slot[name]].record(stream)
+                if name == "grouped_ffn" and w.shared_I:
+                    evs[2].record(stream)
+        return mark
+
+    start, end = ET(), ET()
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
@@ -241,7 +253,7 @@ def run_ours(args, world, rank, local):
         start.record(stream)
         with torch.cuda.stream(stream):
             for i in range(K):
-                step(i)
+                step(timed_marks(i))
         end.record(stream)
         stream.synchronize()
     torch.cuda.synchronize()
@@ -250,9 +262,22 @@ def run_ours(args, world, rank, local):
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
     layer.check(stream)
+    ffn_ms = {n: float(np.mean([ffn_ev[i][2 * j].elapsed_time(ffn_ev[i][2 * j + 1])
+                                for i in range(K)])) for j, n in enumerate(ffn_stages)}
 
-    stage_ms = {n: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)]))
+    # Stage breakdown (not the headline): a separate pass with an event
+    # after every stage; events between kernels also break their overlap.
+    n_bd = min(K, 10)
+    bd_ev = [[ET() for _ in range(len(names) + 1)] for _ in range(n_bd)]
+    with torch.cuda.stream(stream):
+        for i in range(n_bd):
+            it = iter(bd_ev[i][1:])
+            bd_ev[i][0].record(stream)
+            step(lambda n, it=it: next(it).record(stream))
+    stream.synchronize()
+    stage_ms = {n: float(np.mean([bd_ev[i][j].elapsed_time(bd_ev[i][j + 1]) for i in range(n_bd)]))
                 for j, n in enumerate(names)}
+    stage_ms.update(ffn_ms)   # the FFN figures come from the timed region
 
     e2e = None
     if not args.no_e2e:
@@ -321,6 +346,10 @@ def run_ours(args, world, rank, local):
         "balancedness": float(layer.balancedness.item()),
         "clocks": clocks.summary(),
     }
+    if w.hot_experts > 0:
+        out["replica_zipf_sweep"] = replica_sweep(w, dev, parse_relax(args.replica_relax) or (1, 10))
+        out["config"]["replica_routing"] = ("waterfill C=" + args.replica_relax) \
+            if args.replica_relax else "fixed rule (own node, else t mod copies)"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, pl, logits, x, wgu, wd, sgu, sd, args.cpu_seconds)
     return out
@@ -353,6 +382,52 @@ def run_e2e(layer, logits, x, y, stream, world, K, W):
     layer.check(pipe.comp)
     assert torch.equal(y_h, y.cpu()), "end-to-end output differs from the device-resident run"
     return {"unit": "tokens/s", "ms_per_step": e2e_ms, "copies": "overlapped (3 streams, 2 buffers)"}
+
+
+def parse_relax(text):
+    """'1/10' -> (1, 10); '' -> None (fixed replica rule)."""
+    if not text:
+        return None
+    num, _, den = text.partition("/")
+    return int(num), int(den or 1)
+
+
+def replica_sweep(w, dev, relax):
+    """Balancedness and inter-node assignments at each Zipf exponent of the
+    sweep, for the fixed replica rule and for water-filling routing (route +
+    layout only; the FFN result does not depend on the copy chosen)."""
+    from grouped_ffn_gb300 import moe
+    pl = wl.make_placement(w)
+    pl_dev = moe.DevicePlacement.from_tables(pl, dev)
+    out = []
+    A, S, R = w.A, pl.n_slots, w.R
+    i32 = lambda n: torch.empty(n, dtype=torch.int32, device=dev)
+    ws = moe.new_workspace(w.T, w.k, S, device=dev, n_experts=w.E, n_ranks=R)
+    bal = torch.empty(1, dtype=torch.float64, device=dev)
+    mx, tot = i32(1), torch.empty(1, dtype=torch.int64, device=dev)
+    for z in wl.REPLICA_ZIPF_SWEEP:
+        wz = w.with_zipf(z)
+        logits = wl.make_logits(wz, dev)
+        ids, wts = i32(A).view(w.T, w.k), torch.empty(w.T, w.k, dtype=torch.float32, device=dev)
+        moe.moe_route(logits, moe.RouteCfg(w.score_fn, w.k, w.n_groups, w.topk_groups,
+                                           w.group_topn), ids, wts)
+        rec = {"zipf_s": z}
+        slot, counts, offs, dest, src, rc = i32(A), i32(S), i32(S + 1), i32(A), i32(A), i32(R)
+        moe.moe_dispatch_layout(ids, pl_dev, slot, counts, offs, dest, src, rc, ws)
+        moe.moe_balance_stats(rc, bal, mx, tot)
+        node = pl_dev.slot_rank[slot.long()] // w.ranks_per_node
+        tok_node = (torch.arange(A, device=dev) // w.k % R) // w.ranks_per_node
+        rec["fixed_rule"] = {"balancedness": float(bal.item()), "max_rank_load": int(mx.item()),
+                             "inter_node": int((node != tok_node).sum().item())}
+        inter = i32(1)
+        moe.moe_route_replicas(ids, pl_dev, relax[0], relax[1], slot, inter, ws)
+        moe.moe_dispatch_layout_routed(ids, slot, pl_dev, counts, offs, dest, src, rc, ws)
+        moe.moe_balance_stats(rc, bal, mx, tot)
+        moe.moe_check_device_status(ws)
+        rec["waterfill"] = {"relax_C": relax[0] / relax[1], "balancedness": float(bal.item()),
+                            "max_rank_load": int(mx.item()), "inter_node": int(inter.item())}
+        out.append(rec)
+    return out
 
 
 def workload_from_args(args) -> wl.Workload:
@@ -513,6 +588,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--replica-relax", default="",
+                    help="choose replicas by water-filling with load bounds C, e.g. 1/10")
     ap.add_argument("--unpacked", action="store_true",
                     help="stream the expert weights in their plain [E,2I,H]/[E,H,I] layout")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")

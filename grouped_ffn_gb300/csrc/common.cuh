@@ -27,6 +27,13 @@ enum KernelId : int32_t {
 //   [2] KernelId of the reporter
 constexpr size_t kStatusBytes = MOE_WS_STATUS_BYTES;
 
+// Workspace map (bytes): [0, 256) status block; [256, 256 + 4 * 1024) the
+// grouped FFN's per-segment readiness counters; [4352, 4608) the layout's
+// tile ticket; [4608, ...) the layout's look-back flags.
+constexpr size_t kFfnReadyOff = kStatusBytes;
+constexpr size_t kLayoutTicketOff = kFfnReadyOff + 4 * 1024;
+constexpr size_t kLayoutFlagsOff = kLayoutTicketOff + 256;
+
 // Bounded waits give up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -63,6 +70,14 @@ __device__ __forceinline__ uint4 ld_stream_u4(const uint4 *p) {
   return v;
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have finished and their writes are visible (a no-op when the kernel was
+// launched without the attribute), and let the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace moe
 
 // ---------------------------------------------------------------- host side
@@ -77,6 +92,26 @@ int sm_count();
 
 // Maps the last CUDA launch error to a status.
 inline moe_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Launch with programmatic stream serialization: the kernel may begin while
+// its predecessor on the stream drains; it calls moe::pdl_wait() before
+// touching anything the predecessor writes.
+template <typename... KArgs, typename... Args>
+inline moe_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -51,8 +51,8 @@ constexpr int kStageBytes = kABytes + 2 * kBHalfBytes;
 constexpr int kMaxSegs = 1024;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-// Workspace: status block, then (from byte 512) one readiness counter per segment.
-constexpr size_t kReadyOff = 512;
+// Workspace: one readiness counter per segment at moe::kFfnReadyOff.
+constexpr size_t kReadyOff = moe::kFfnReadyOff;
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),

@@ -46,11 +46,20 @@ struct LayoutArgs {
   int32_t k, E, S, R, rpn;
   const int32_t *slot_expert, *slot_rank, *rep_offsets, *rep_slots, *token_src_rank;
   int32_t *slot, *seg_counts, *seg_offsets, *dest_row, *src_assign, *rank_counts;
-  uint32_t *tile_flags;  // [n_tiles][S]
+  uint32_t *tile_flags;  // [n_tiles][K]
   int32_t *ticket;
   int32_t *status;
   int32_t n_tiles;
+  int32_t K;                // keys counted by the scan (S in slot modes)
+  const int32_t *slot_in;   // kModeSlots: the chosen slot of each assignment
+  const int32_t *rkey;      // kModeKeys: [E] replicated-expert index or -1
+  int32_t *key_totals;      // kModeKeys: [K] assignments per key
 };
+
+// What the scan counts and ranks: the slot given by the fixed replica rule,
+// a slot chosen beforehand (routed layout), or the (replicated expert,
+// source rank) key of replica routing.
+enum ScanMode { kModeRule = 0, kModeSlots = 1, kModeKeys = 2 };
 
 // Placement tables cached in shared memory by every layout CTA.
 struct PlacementCache {
@@ -94,36 +103,43 @@ __device__ int choose_slot(const LayoutArgs &p, const PlacementCache &c, int64_t
 }
 
 // Dynamic shared memory of layout_scan_kernel, in 32-bit words.
-inline size_t layout_smem_words(int S, int R, int E) {
-  return (size_t)(kWarps + 2) * S + R + (E + 1) + 3 * (size_t)S;
+inline size_t layout_smem_words(int S, int R, int E, int K) {
+  return (size_t)(kWarps + 2) * K + R + (E + 1) + 3 * (size_t)S + E;
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
   extern __shared__ int32_t smem[];
-  int32_t *whist = smem;                       // [kWarps][S]: counts, then warp offsets
-  int32_t *tile_prefix = smem + kWarps * p.S;  // [S]
-  int32_t *tile_agg = tile_prefix + p.S;       // [S]
-  int32_t *rload = tile_agg + p.S;             // [R], last tile only
+  const int K = p.K;
+  int32_t *whist = smem;                       // [kWarps][K]: counts, then warp offsets
+  int32_t *tile_prefix = smem + kWarps * K;    // [K]
+  int32_t *tile_agg = tile_prefix + K;         // [K]
+  int32_t *rload = tile_agg + K;               // [R], last tile only
   int32_t *c_rep_offsets = rload + p.R;        // [E+1]
   int32_t *c_rep_slots = c_rep_offsets + p.E + 1;  // [S]
   int32_t *c_slot_expert = c_rep_slots + p.S;      // [S]
   int32_t *c_slot_rank = c_slot_expert + p.S;      // [S]
+  int32_t *c_rkey = c_slot_rank + p.S;             // [E], kModeKeys
   __shared__ int32_t s_tile;
 
+  moe::pdl_wait();
+  moe::pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) s_tile = atomicAdd(p.ticket, 1);
-  for (int i = tid; i < kWarps * p.S; i += kThreads) whist[i] = 0;
+  for (int i = tid; i < kWarps * K; i += kThreads) whist[i] = 0;
   for (int i = tid; i <= p.E; i += kThreads) c_rep_offsets[i] = p.rep_offsets[i];
   for (int i = tid; i < p.S; i += kThreads) {
     c_rep_slots[i] = p.rep_slots[i];
     c_slot_expert[i] = p.slot_expert[i];
     c_slot_rank[i] = p.slot_rank[i];
   }
+  if (MODE == kModeKeys)
+    for (int i = tid; i < p.E; i += kThreads) c_rkey[i] = p.rkey[i];
   __syncthreads();
   const int tile = s_tile;
   const PlacementCache cache{c_rep_offsets, c_rep_slots, c_slot_expert, c_slot_rank};
 
-  // ---- slots of this warp's 256 assignments (all loads issued together)
+  // ---- keys of this warp's 256 assignments (all loads issued together)
   const int64_t base = (int64_t)tile * kTileA + (int64_t)warp * kPerWarp;
   int ids[kRounds];
 #pragma unroll
@@ -135,7 +151,34 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
     const int64_t a = base + r * 32 + lane;
-    my_slot[r] = (a < p.A) ? choose_slot(p, cache, a, ids[r]) : -1;
+    int s = -1;
+    if (a < p.A) {
+      const int e = ids[r];
+      if (MODE == kModeRule) {
+        s = choose_slot(p, cache, a, e);
+      } else if (MODE == kModeSlots) {
+        s = __ldg(p.slot_in + a);
+        if (e < 0 || e >= p.E) {
+          moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, (int32_t)a, moe::K_LAYOUT_SCAN);
+          s = -1;
+        } else if (s < 0 || s >= p.S || cache.slot_expert[s] != e) {
+          moe::report_error(p.status, MOE_ERR_PLACEMENT, (int32_t)a, moe::K_LAYOUT_SCAN);
+          s = -1;
+        }
+      } else {  // kModeKeys: only experts with several replicas are keyed
+        if (e < 0 || e >= p.E) {
+          moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, (int32_t)a, moe::K_LAYOUT_SCAN);
+        } else if (c_rkey[e] >= 0) {
+          const int64_t t = a / p.k;
+          const int src = p.token_src_rank ? p.token_src_rank[t] : (int)(t % p.R);
+          if (src < 0 || src >= p.R)
+            moe::report_error(p.status, MOE_ERR_PLACEMENT, (int32_t)a, moe::K_LAYOUT_SCAN);
+          else
+            s = c_rkey[e] * p.R + src;
+        }
+      }
+    }
+    my_slot[r] = s;
   }
 
   // ---- stable rank of each assignment inside its warp's 256-run
@@ -144,24 +187,24 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
     const int s = my_slot[r];
     const uint32_t peers = __match_any_sync(0xffffffffu, s);
     const int leader = __ffs(peers) - 1;
-    const int before = (s >= 0) ? whist[warp * p.S + s] : 0;
+    const int before = (s >= 0) ? whist[warp * K + s] : 0;
     __syncwarp();
-    if (s >= 0 && lane == leader) whist[warp * p.S + s] = before + __popc(peers);
+    if (s >= 0 && lane == leader) whist[warp * K + s] = before + __popc(peers);
     __syncwarp();
     my_rank[r] = before + __popc(peers & ((1u << lane) - 1u));
   }
   __syncthreads();
 
-  // ---- per slot: warp offsets, tile aggregate, decoupled look-back
-  for (int s = tid; s < p.S; s += kThreads) {
+  // ---- per key: warp offsets, tile aggregate, decoupled look-back
+  for (int s = tid; s < K; s += kThreads) {
     int run = 0;
     for (int w = 0; w < kWarps; ++w) {
-      const int c = whist[w * p.S + s];
-      whist[w * p.S + s] = run;
+      const int c = whist[w * K + s];
+      whist[w * K + s] = run;
       run += c;
     }
     tile_agg[s] = run;
-    uint32_t *my_flag = p.tile_flags + (size_t)tile * p.S + s;
+    uint32_t *my_flag = p.tile_flags + (size_t)tile * K + s;
     int prefix = 0;
     bool ok = true;
     if (tile == 0) {
@@ -170,7 +213,7 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
       moe::st_relaxed_u32(my_flag, kFlagAgg | (uint32_t)run);
       const uint64_t t0 = moe::global_timer_ns();
       for (int j = tile - 1; j >= 0;) {
-        const uint32_t f = moe::ld_relaxed_u32(p.tile_flags + (size_t)j * p.S + s);
+        const uint32_t f = moe::ld_relaxed_u32(p.tile_flags + (size_t)j * K + s);
         const uint32_t flag = f & ~kValMask;
         if (flag == 0) {
           if (moe::global_timer_ns() - t0 > moe::kWaitLimitNs) {
@@ -195,19 +238,23 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
   }
   __syncthreads();
 
-  // ---- partial destination rows (seg_offsets added by the finalize kernel)
+  // ---- partial ranks (slot modes: seg_offsets added by the finalize kernel)
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
     const int64_t a = base + r * 32 + lane;
     if (a < p.A) {
       const int s = my_slot[r];
-      p.slot[a] = s;
-      p.dest_row[a] = (s >= 0) ? tile_prefix[s] + whist[warp * p.S + s] + my_rank[r] : -1;
+      if (MODE == kModeRule) p.slot[a] = s;
+      p.dest_row[a] = (s >= 0) ? tile_prefix[s] + whist[warp * K + s] + my_rank[r] : -1;
     }
   }
 
   // ---- the last tile knows the totals
   if (tile != p.n_tiles - 1) return;
+  if (MODE == kModeKeys) {
+    for (int s = tid; s < K; s += kThreads) p.key_totals[s] = tile_prefix[s] + tile_agg[s];
+    return;
+  }
   int32_t *tot = whist;  // reuse: [S] totals
   __syncthreads();
   for (int s = tid; s < p.S; s += kThreads) {
@@ -251,11 +298,20 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
   for (int r = tid; r < p.R; r += kThreads) p.rank_counts[r] = rload[r];
 }
 
+// Adds seg_offsets to the partial ranks and writes the inverse permutation;
+// then clears the scan's ticket and look-back flags, so the next call on
+// this workspace finds them zero without a separate memset.
 __global__ void layout_finalize_kernel(LayoutArgs p) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t a = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; a < p.A; a += stride) {
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t n_flags = (int64_t)p.n_tiles * p.K;
+  for (int64_t i = i0; i < n_flags; i += stride) p.tile_flags[i] = 0u;
+  if (i0 == 0) *p.ticket = 0;
+  for (int64_t a = i0; a < p.A; a += stride) {
     const int s = p.slot[a];
-    if (s < 0) continue;
+    if (s < 0 || p.dest_row[a] < 0) continue;
     const int d = p.dest_row[a] + p.seg_offsets[s];
     if (d < 0 || d >= p.A) {
       moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, (int32_t)a, moe::K_LAYOUT_FINALIZE);
@@ -269,8 +325,190 @@ __global__ void layout_finalize_kernel(LayoutArgs p) {
 
 inline int64_t n_tiles_for(int64_t A) { return A > 0 ? (A + kTileA - 1) / kTileA : 0; }
 
-constexpr size_t kTicketOff = moe::kStatusBytes;      // 256
-constexpr size_t kFlagsOff = moe::kStatusBytes + 256;  // 512
+// ---------------------------------------------------------------- replica routing
+// "Zepp", Section 4.1 (Eq. 1) and Section 5 "Routing": per expert with
+// several replicas, a greedy water-filling decides how many of each source
+// rank's assignments each replica serves, preferring the source's own GPU,
+// then its node, then remote nodes, within integer load bounds around the
+// even split; a source's assignments then take those destinations in
+// ascending order.
+constexpr int kMaxRep = 16;      // replicas of one expert
+constexpr int kMaxKeys = 1024;   // (replicated experts) x ranks
+
+struct RouteArgs {
+  int32_t E, S, R, rpn, Kx;  // Kx = S - E bounds the number of replicated experts
+  int32_t c_num, c_den;
+  const int32_t *rep_offsets, *rep_slots, *slot_rank;
+  int32_t *rkey;         // [E] replicated-expert index or -1
+  int32_t *repl_expert;  // [Kx]
+  int32_t *n_repl;       // [1]
+  const int32_t *key_totals;  // [Kx * R] demand d[c][i]
+  int32_t *left;         // [Kx * R] scratch
+  int32_t *M;            // [Kx * R * kMaxRep] assignments of source i served by replica p
+  int32_t *inter_node;   // [1] output
+  int32_t *status;
+};
+
+// Index the experts that have several replicas (one warp).
+__global__ void route_prep_kernel(RouteArgs r) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x >= 32) return;
+  int base = 0;
+  for (int e0 = 0; e0 < r.E; e0 += 32) {
+    const int e = e0 + lane;
+    int n = 0;
+    if (e < r.E) n = r.rep_offsets[e + 1] - r.rep_offsets[e];
+    bool rep = n >= 2;
+    if (rep && n > kMaxRep) {
+      moe::report_error(r.status, MOE_ERR_PLACEMENT, e, moe::K_LAYOUT_SCAN);
+      rep = false;
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, rep);
+    const int idx = base + __popc(m & ((1u << lane) - 1u));
+    if (rep && idx >= r.Kx) {
+      moe::report_error(r.status, MOE_ERR_PLACEMENT, e, moe::K_LAYOUT_SCAN);
+      rep = false;
+    }
+    if (e < r.E) r.rkey[e] = rep ? idx : -1;
+    if (rep) r.repl_expert[idx] = e;
+    base += __popc(m);
+  }
+  if (lane == 0) {
+    *r.n_repl = min(base, r.Kx);
+    *r.inter_node = 0;
+  }
+}
+
+// One thread per replicated expert: the water-filling of its demand.
+__global__ void route_waterfill_kernel(RouteArgs r) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= *r.n_repl) return;
+  const int e = r.repl_expert[c];
+  const int off = r.rep_offsets[e];
+  const int n = r.rep_offsets[e + 1] - off;
+  int rank_of[kMaxRep];
+  int lo[kMaxRep], hi[kMaxRep], load[kMaxRep];
+  const int32_t *d = r.key_totals + (size_t)c * r.R;
+  int32_t *left = r.left + (size_t)c * r.R;
+  int32_t *M = r.M + (size_t)c * r.R * kMaxRep;
+  int64_t D = 0;
+  for (int i = 0; i < r.R; ++i) {
+    left[i] = d[i];
+    D += d[i];
+    for (int q = 0; q < kMaxRep; ++q) M[i * kMaxRep + q] = 0;
+  }
+  const int base = (int)(D / n), rem = (int)(D % n);
+  const int slack = (int)(((int64_t)r.c_num * D) / ((int64_t)r.c_den * n));
+  for (int q = 0; q < kMaxRep; ++q) {
+    if (q < n) {
+      rank_of[q] = r.slot_rank[r.rep_slots[off + q]];
+      const int qq = base + (q < rem ? 1 : 0);
+      lo[q] = max(0, qq - slack);
+      hi[q] = qq + slack;
+      load[q] = 0;
+    }
+  }
+  int64_t U = D;
+  auto deficit_total = [&]() {
+    int64_t t = 0;
+    for (int q = 0; q < n; ++q) t += max(0, lo[q] - load[q]);
+    return t;
+  };
+  auto give = [&](int i, int q, int64_t x) {
+    if (x <= 0) return;
+    left[i] -= (int)x;
+    load[q] += (int)x;
+    U -= x;
+    M[i * kMaxRep + q] += (int)x;
+  };
+  // passes 1-3: own GPU, own node, remote; each capped by capacity and by
+  // the demand the other replicas' lower bounds still need
+  for (int pass = 0; pass < 3; ++pass) {
+    for (int i = 0; i < r.R; ++i) {
+      for (int q = 0; q < n && left[i] > 0; ++q) {
+        const int rq = rank_of[q];
+        const bool same_node = rq / r.rpn == i / r.rpn;
+        const bool in_pass = pass == 0 ? rq == i : (pass == 1 ? (rq != i && same_node) : !same_node);
+        if (!in_pass) continue;
+        const int64_t others = deficit_total() - max(0, lo[q] - load[q]);
+        const int64_t allow = min((int64_t)(hi[q] - load[q]), U - others);
+        give(i, q, min((int64_t)left[i], max((int64_t)0, allow)));
+      }
+    }
+  }
+  // pass 4: what the reserve rule held back, deficits first
+  for (int i = 0; i < r.R; ++i) {
+    for (int q = 0; q < n && left[i] > 0; ++q)
+      if (lo[q] > load[q]) give(i, q, min(left[i], lo[q] - load[q]));
+    for (int q = 0; q < n && left[i] > 0; ++q) give(i, q, min(left[i], hi[q] - load[q]));
+  }
+  if (U != 0) moe::report_error(r.status, MOE_ERR_PLACEMENT, e, moe::K_LAYOUT_SCAN);
+}
+
+// Per assignment: the replica its rank within (expert, source) falls into,
+// walking the source's locality order; counts inter-node assignments and
+// clears the scan's ticket and flags for the next call.
+__global__ void route_assign_kernel(RouteArgs r, LayoutArgs p, int32_t *slot) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t n_flags = (int64_t)p.n_tiles * p.K;
+  int inter = 0;
+  for (int64_t a = i0; a < p.A; a += stride) {
+    const int e = p.topk_ids[a];
+    if (e < 0 || e >= p.E) {
+      slot[a] = -1;
+      continue;
+    }
+    const int64_t t = a / p.k;
+    const int src = p.token_src_rank ? p.token_src_rank[t] : (int)(t % p.R);
+    const int off = r.rep_offsets[e];
+    const int n = r.rep_offsets[e + 1] - off;
+    int s = -1;
+    if (n == 1) {
+      s = r.rep_slots[off];
+    } else if (r.rkey[e] >= 0 && src >= 0 && src < p.R) {
+      const int rank = slot[a];  // rank within (expert, source), from the scan
+      const int32_t *M = r.M + ((size_t)r.rkey[e] * p.R + src) * kMaxRep;
+      int cum = 0;
+      for (int pass = 0; pass < 3 && s < 0; ++pass) {
+        for (int q = 0; q < n; ++q) {
+          const int rq = r.slot_rank[r.rep_slots[off + q]];
+          const bool same_node = rq / p.rpn == src / p.rpn;
+          const bool in_pass =
+              pass == 0 ? rq == src : (pass == 1 ? (rq != src && same_node) : !same_node);
+          if (!in_pass) continue;
+          cum += M[q];
+          if (rank >= 0 && rank < cum) {
+            s = r.rep_slots[off + q];
+            break;
+          }
+        }
+      }
+    }
+    if (s < 0) {
+      moe::report_error(p.status, MOE_ERR_PLACEMENT, (int32_t)a, moe::K_LAYOUT_FINALIZE);
+    } else if (r.slot_rank[s] / p.rpn != src / p.rpn) {
+      ++inter;
+    }
+    slot[a] = s;
+  }
+  for (int64_t i = i0; i < n_flags; i += stride) p.tile_flags[i] = 0u;
+  if (i0 == 0) *p.ticket = 0;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) inter += __shfl_xor_sync(0xffffffffu, inter, off);
+  if ((threadIdx.x & 31) == 0 && inter) atomicAdd(r.inter_node, inter);
+}
+
+
+
+constexpr size_t kTicketOff = moe::kLayoutTicketOff;
+constexpr size_t kFlagsOff = moe::kLayoutFlagsOff;
 
 }  // namespace
 
@@ -303,8 +541,8 @@ extern "C" moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t n_tiles = std::max<int64_t>(n_tiles_for(A), 1);
   char *wsb = static_cast<char *>(ws);
-  if (cudaMemsetAsync(wsb + kTicketOff, 0, need - kTicketOff, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  // The ticket and flags are zero on entry: moe_workspace_init clears them
+  // once and every call's finalize kernel clears them again after use.
 
   LayoutArgs p{};
   p.topk_ids = topk_ids;
@@ -330,22 +568,20 @@ extern "C" moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, in
   p.status = moe_host::status_ptr(ws);
   p.n_tiles = (int32_t)n_tiles;
 
-  const size_t smem = layout_smem_words(p.S, p.R, p.E) * sizeof(int32_t);
+  p.K = p.S;
+  const size_t smem = layout_smem_words(p.S, p.R, p.E, p.K) * sizeof(int32_t);
   if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(layout_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(layout_scan_kernel<kModeRule>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  layout_scan_kernel<<<(unsigned)n_tiles, kThreads, smem, st>>>(p);
-  if (moe_status s = moe_host::launch_status()) return s;
-  if (A > 0) {
-    int64_t blocks = (A + 255) / 256;
-    const int64_t cap = (int64_t)moe_host::sm_count() * 8;
-    if (blocks > cap) blocks = cap;
-    layout_finalize_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
-    if (moe_status s = moe_host::launch_status()) return s;
-  }
-  return MOE_OK;
+  if (moe_status s = moe_host::launch_pdl(layout_scan_kernel<kModeRule>, dim3((unsigned)n_tiles),
+                                          dim3(kThreads), smem, st, p))
+    return s;
+  int64_t blocks = (std::max<int64_t>(A, n_tiles * p.K) + 255) / 256;
+  const int64_t cap = (int64_t)moe_host::sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  return moe_host::launch_pdl(layout_finalize_kernel, dim3((unsigned)blocks), dim3(256), 0, st, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -442,13 +678,14 @@ extern "C" moe_status moe_dispatch_layout_noalloc(const int32_t *topk_ids, int64
   p.status = status;
   p.n_tiles = (int32_t)n_tiles;
 
-  const size_t smem = layout_smem_words(p.S, p.R, p.E) * sizeof(int32_t);
+  p.K = p.S;
+  const size_t smem = layout_smem_words(p.S, p.R, p.E, p.K) * sizeof(int32_t);
   if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(layout_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(layout_scan_kernel<kModeRule>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  layout_scan_kernel<<<(unsigned)n_tiles, kThreads, smem, st>>>(p);
+  layout_scan_kernel<kModeRule><<<(unsigned)n_tiles, kThreads, smem, st>>>(p);
   if (moe_status s = moe_host::launch_status()) return s;
   if (A > 0) {
     int64_t blocks = (A + 255) / 256;
@@ -458,4 +695,168 @@ extern "C" moe_status moe_dispatch_layout_noalloc(const int32_t *topk_ids, int64
     if (moe_status s = moe_host::launch_status()) return s;
   }
   return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+namespace {
+
+size_t route_ws_words_after_flags(int32_t E, int32_t S, int32_t R) {
+  const size_t Kx = (size_t)(S > E ? S - E : 0);
+  // key totals, rkey, replicated experts, count, left, M
+  return Kx * R + (size_t)E + Kx + 1 + Kx * R + Kx * R * kMaxRep;
+}
+
+moe_status fill_layout_args(LayoutArgs &p, const int32_t *topk_ids, int64_t T, int32_t k,
+                            const moe_placement *pl, void *ws) {
+  p = LayoutArgs{};
+  p.topk_ids = topk_ids;
+  p.A = T * (int64_t)k;
+  p.k = k;
+  p.E = pl->n_experts;
+  p.S = pl->n_slots;
+  p.R = pl->n_ranks;
+  p.rpn = pl->ranks_per_node;
+  p.slot_expert = pl->slot_expert;
+  p.slot_rank = pl->slot_rank;
+  p.rep_offsets = pl->rep_offsets;
+  p.rep_slots = pl->rep_slots;
+  p.token_src_rank = pl->token_src_rank;
+  char *wsb = static_cast<char *>(ws);
+  p.tile_flags = reinterpret_cast<uint32_t *>(wsb + kFlagsOff);
+  p.ticket = reinterpret_cast<int32_t *>(wsb + kTicketOff);
+  p.status = moe_host::status_ptr(ws);
+  p.n_tiles = (int32_t)std::max<int64_t>(n_tiles_for(p.A), 1);
+  return MOE_OK;
+}
+
+moe_status check_placement(const moe_placement *pl, int64_t T, int32_t k) {
+  if (pl == nullptr || T < 0 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (T * (int64_t)k >= (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  if (pl->n_experts < 1 || pl->n_slots < 1 || pl->n_ranks < 1 || pl->ranks_per_node < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (pl->n_slots > kMaxSlots || pl->n_ranks > kMaxRanks || pl->n_experts > kMaxExperts)
+    return MOE_ERR_UNSUPPORTED;
+  if (!pl->slot_expert || !pl->slot_rank || !pl->rep_offsets || !pl->rep_slots)
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" size_t moe_route_replicas_workspace_size(int64_t T, int32_t k, int32_t n_experts,
+                                                    int32_t n_slots, int32_t n_ranks) {
+  if (T < 0 || k < 1 || n_experts < 1 || n_slots < 1 || n_ranks < 1) return 0;
+  const int64_t Kx = n_slots > n_experts ? n_slots - n_experts : 0;
+  // flags sized for the routing keys and for the slots of a following
+  // layout call on the same workspace, so neither reaches the scratch tail
+  const int64_t K = std::max<int64_t>(std::max<int64_t>(Kx * n_ranks, 1), n_slots);
+  const int64_t tiles = std::max<int64_t>(n_tiles_for(T * (int64_t)k), 1);
+  return kFlagsOff + (size_t)(tiles * K) * sizeof(uint32_t) +
+         route_ws_words_after_flags(n_experts, n_slots, n_ranks) * sizeof(int32_t);
+}
+
+extern "C" moe_status moe_route_replicas(const int32_t *topk_ids, int64_t T, int32_t k,
+                                         const moe_placement *pl, int32_t c_num, int32_t c_den,
+                                         int32_t *slot, int32_t *inter_node, void *ws,
+                                         size_t ws_bytes, void *stream) {
+  if (moe_status s = check_placement(pl, T, k)) return s;
+  if (c_num < 0 || c_den < 1 || !inter_node) return MOE_ERR_INVALID_ARG;
+  const int64_t A = T * (int64_t)k;
+  if (A > 0 && (!topk_ids || !slot)) return MOE_ERR_INVALID_ARG;
+  const int Kx = pl->n_slots > pl->n_experts ? pl->n_slots - pl->n_experts : 0;
+  if ((int64_t)Kx * pl->n_ranks > kMaxKeys) return MOE_ERR_UNSUPPORTED;
+  const size_t need = moe_route_replicas_workspace_size(T, k, pl->n_experts, pl->n_slots,
+                                                        pl->n_ranks);
+  if (moe_status s = moe_host::check_ws(ws, ws_bytes, need)) return s;
+
+  LayoutArgs p;
+  fill_layout_args(p, topk_ids, T, k, pl, ws);
+  p.K = std::max(Kx * pl->n_ranks, 1);
+  const int64_t flag_words = (int64_t)p.n_tiles * std::max(p.K, p.S);
+  int32_t *tail = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kFlagsOff +
+                                              (size_t)flag_words * sizeof(uint32_t));
+  RouteArgs r{};
+  r.E = p.E;
+  r.S = p.S;
+  r.R = p.R;
+  r.rpn = p.rpn;
+  r.Kx = Kx;
+  r.c_num = c_num;
+  r.c_den = c_den;
+  r.rep_offsets = pl->rep_offsets;
+  r.rep_slots = pl->rep_slots;
+  r.slot_rank = pl->slot_rank;
+  int32_t *key_totals = tail;
+  r.key_totals = key_totals;
+  r.rkey = key_totals + (size_t)Kx * p.R;
+  r.repl_expert = r.rkey + p.E;
+  r.n_repl = r.repl_expert + Kx;
+  r.left = r.n_repl + 1;
+  r.M = r.left + (size_t)Kx * p.R;
+  r.inter_node = inter_node;
+  r.status = p.status;
+  p.rkey = r.rkey;
+  p.key_totals = key_totals;
+  p.dest_row = slot;  // the scan leaves each assignment's rank within its key here
+  p.slot = nullptr;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (moe_status s = moe_host::launch_pdl(route_prep_kernel, dim3(1), dim3(32), 0, st, r)) return s;
+  if (A > 0 && Kx > 0) {
+    const size_t smem = layout_smem_words(p.S, p.R, p.E, p.K) * sizeof(int32_t);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(layout_scan_kernel<kModeKeys>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (moe_status s = moe_host::launch_pdl(layout_scan_kernel<kModeKeys>, dim3((unsigned)p.n_tiles),
+                                            dim3(kThreads), smem, st, p))
+      return s;
+    if (moe_status s = moe_host::launch_pdl(route_waterfill_kernel, dim3((Kx + 63) / 64), dim3(64),
+                                            0, st, r))
+      return s;
+  }
+  int64_t blocks = (std::max<int64_t>(A, (int64_t)p.n_tiles * p.K) + 255) / 256;
+  const int64_t cap = (int64_t)moe_host::sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return moe_host::launch_pdl(route_assign_kernel, dim3((unsigned)blocks), dim3(256), 0, st, r, p,
+                              slot);
+}
+
+extern "C" moe_status moe_dispatch_layout_routed(const int32_t *topk_ids, const int32_t *slot_in,
+                                                 int64_t T, int32_t k, const moe_placement *pl,
+                                                 int32_t *seg_counts, int32_t *seg_offsets,
+                                                 int32_t *dest_row, int32_t *src_assign,
+                                                 int32_t *rank_counts, void *ws, size_t ws_bytes,
+                                                 void *stream) {
+  if (moe_status s = check_placement(pl, T, k)) return s;
+  const int64_t A = T * (int64_t)k;
+  if (!seg_counts || !seg_offsets || !rank_counts) return MOE_ERR_INVALID_ARG;
+  if (A > 0 && (!topk_ids || !slot_in || !dest_row || !src_assign)) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_workspace_size(T, k, pl->n_slots);
+  if (moe_status s = moe_host::check_ws(ws, ws_bytes, need)) return s;
+
+  LayoutArgs p;
+  fill_layout_args(p, topk_ids, T, k, pl, ws);
+  p.K = p.S;
+  p.slot_in = slot_in;
+  p.slot = const_cast<int32_t *>(slot_in);  // read by the finalize kernel only
+  p.seg_counts = seg_counts;
+  p.seg_offsets = seg_offsets;
+  p.dest_row = dest_row;
+  p.src_assign = src_assign;
+  p.rank_counts = rank_counts;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t smem = layout_smem_words(p.S, p.R, p.E, p.K) * sizeof(int32_t);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(layout_scan_kernel<kModeSlots>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (moe_status s = moe_host::launch_pdl(layout_scan_kernel<kModeSlots>, dim3((unsigned)p.n_tiles),
+                                          dim3(kThreads), smem, st, p))
+    return s;
+  int64_t blocks = (std::max<int64_t>(A, (int64_t)p.n_tiles * p.K) + 255) / 256;
+  const int64_t cap = (int64_t)moe_host::sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  return moe_host::launch_pdl(layout_finalize_kernel, dim3((unsigned)blocks), dim3(256), 0, st, p);
 }

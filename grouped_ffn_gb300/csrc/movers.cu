@@ -23,6 +23,8 @@ constexpr int kUnroll = 4;
 __global__ void __launch_bounds__(kMoverThreads) permute_kernel(
     const uint4 *__restrict__ x, int64_t T, int H8, int k, const int32_t *__restrict__ dest_row,
     uint4 *__restrict__ xp, int64_t A, int32_t *status) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     const uint4 *src = x + t * H8;
     const int32_t *dr = dest_row + t * k;
@@ -72,6 +74,8 @@ __global__ void __launch_bounds__(kMoverThreads) combine_kernel(
     const uint4 *__restrict__ yp, const int32_t *__restrict__ dest_row,
     const float *__restrict__ topk_w, int64_t T, int k, int H8, const uint4 *__restrict__ shared,
     uint4 *__restrict__ y, int64_t A, int32_t *status) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     int32_t r[KMAX];
     float w[KMAX];
@@ -121,6 +125,8 @@ __global__ void __launch_bounds__(kMoverThreads) combine_kernel(
 
 __global__ void balance_kernel(const int32_t *__restrict__ rc, int R, double *bal, int32_t *mx,
                                int64_t *total) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
   __shared__ long long s_tot[32];
   __shared__ int s_max[32];
   long long tsum = 0;
@@ -171,10 +177,10 @@ extern "C" moe_status moe_permute(const uint16_t *x, int64_t T, int32_t H, int32
   if (!moe_host::aligned16(x) || !moe_host::aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
   if (moe_status s = moe_host::check_ws(ws, ws_bytes, moe::kStatusBytes)) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  permute_kernel<<<mover_grid(T), kMoverThreads, 0, st>>>(
-      reinterpret_cast<const uint4 *>(x), T, H / 8, k, dest_row, reinterpret_cast<uint4 *>(x_perm),
-      T * (int64_t)k, moe_host::status_ptr(ws));
-  return moe_host::launch_status();
+  return moe_host::launch_pdl(permute_kernel, dim3(mover_grid(T)), dim3(kMoverThreads), 0, st,
+                              reinterpret_cast<const uint4 *>(x), T, H / 8, k, dest_row,
+                              reinterpret_cast<uint4 *>(x_perm), T * (int64_t)k,
+                              moe_host::status_ptr(ws));
 }
 
 extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *dest_row,
@@ -195,16 +201,15 @@ extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *dest_ro
   uint4 *yo = reinterpret_cast<uint4 *>(y);
   const int64_t A = T * (int64_t)k;
   int32_t *status = moe_host::status_ptr(ws);
-  const unsigned g = mover_grid(T);
+  const dim3 g(mover_grid(T)), b(kMoverThreads);
+  const int H8 = H / 8;
   if (k <= 2)
-    combine_kernel<2><<<g, kMoverThreads, 0, st>>>(yp, dest_row, topk_w, T, k, H / 8, sh, yo, A, status);
-  else if (k <= 4)
-    combine_kernel<4><<<g, kMoverThreads, 0, st>>>(yp, dest_row, topk_w, T, k, H / 8, sh, yo, A, status);
-  else if (k <= 8)
-    combine_kernel<8><<<g, kMoverThreads, 0, st>>>(yp, dest_row, topk_w, T, k, H / 8, sh, yo, A, status);
-  else
-    combine_kernel<16><<<g, kMoverThreads, 0, st>>>(yp, dest_row, topk_w, T, k, H / 8, sh, yo, A, status);
-  return moe_host::launch_status();
+    return moe_host::launch_pdl(combine_kernel<2>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, status);
+  if (k <= 4)
+    return moe_host::launch_pdl(combine_kernel<4>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, status);
+  if (k <= 8)
+    return moe_host::launch_pdl(combine_kernel<8>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, status);
+  return moe_host::launch_pdl(combine_kernel<16>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, status);
 }
 
 extern "C" moe_status moe_balance_stats(const int32_t *rank_counts, int32_t R, double *balancedness,
@@ -213,7 +218,6 @@ extern "C" moe_status moe_balance_stats(const int32_t *rank_counts, int32_t R, d
   (void)ws;
   (void)ws_bytes;
   if (R < 1 || !rank_counts || !balancedness || !max_count || !total) return MOE_ERR_INVALID_ARG;
-  balance_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(rank_counts, R, balancedness,
-                                                                     max_count, total);
-  return moe_host::launch_status();
+  return moe_host::launch_pdl(balance_kernel, dim3(1), dim3(256), 0, static_cast<cudaStream_t>(stream),
+                              rank_counts, R, balancedness, max_count, total);
 }

@@ -81,14 +81,14 @@ __device__ __forceinline__ double sigmoid_of(float x, double) { return sigmoid64
 // Lane g returns group g's score: the sum, in descending order, of the
 // sigmoids (in precision F) of the group's top_n largest logits.
 template <int VPL, typename F>
-__device__ F group_score(const float (&v)[VPL], uint32_t avail, int lane, int n_groups, int gsz,
-                         int top_n) {
+__device__ F group_score(const float (&v)[VPL], uint32_t avail, int lane, int n_groups,
+                         const int (&gid)[VPL], int top_n) {
   F mine = (F)0;
   for (int g = 0; g < n_groups; ++g) {
     uint32_t gmask = 0;
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
-      if (((avail >> i) & 1u) && (lane + 32 * i) / gsz == g) gmask |= 1u << i;
+      if (((avail >> i) & 1u) && gid[i] == g) gmask |= 1u << i;
     for (int r = 0; r < top_n; ++r) {
       float bv;
       int bid;
@@ -159,10 +159,15 @@ template <int VPL>
 __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits, int64_t T,
                                                     int E, RouteArgs a, int32_t *__restrict__ ids,
                                                     float *__restrict__ w) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int gsz = a.n_groups > 1 ? E / a.n_groups : E;
+  int gid[VPL];  // group of this lane's element i (constant for the whole launch)
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) gid[i] = (lane + 32 * i) / gsz;
 
   for (int64_t t = warp0; t < T; t += nwarps) {
     const float *row = logits + t * E;
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
       // the fp64 selection is the same set; otherwise the warp recomputes
       // the scores in fp64 and selects again.
       const bool gvalid = lane < a.n_groups;
-      const float my_g32 = group_score<VPL, float>(v, avail, lane, a.n_groups, gsz, a.group_topn);
+      const float my_g32 = group_score<VPL, float>(v, avail, lane, a.n_groups, gid, a.group_topn);
       float last_kept, best_dropped;
       uint32_t kept = select_groups<float>(my_g32, gvalid, lane, a.topk_groups, last_kept,
                                            best_dropped);
@@ -197,13 +202,13 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
       const float eps = n * 2e-7f + (n - 1.0f) * n * 6e-8f;
       if (a.topk_groups < a.n_groups && !(last_kept - best_dropped > 4.0f * eps)) {
         const double my_g64 =
-            group_score<VPL, double>(v, avail, lane, a.n_groups, gsz, a.group_topn);
+            group_score<VPL, double>(v, avail, lane, a.n_groups, gid, a.group_topn);
         double l64, b64;
         kept = select_groups<double>(my_g64, gvalid, lane, a.topk_groups, l64, b64);
       }
 #pragma unroll
       for (int i = 0; i < VPL; ++i)
-        if (!((kept >> ((lane + 32 * i) / gsz)) & 1u)) avail &= ~(1u << i);
+        if (!((kept >> gid[i]) & 1u)) avail &= ~(1u << i);
     }
 
     // Top-k: lane j keeps the j-th selection.
@@ -247,7 +252,8 @@ void launch_route(const float *logits, int64_t T, int E, RouteArgs a, int32_t *i
   const int64_t cap = (int64_t)moe_host::sm_count() * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  route_kernel<VPL><<<(unsigned)blocks, threads, 0, st>>>(logits, T, E, a, ids, w);
+  moe_host::launch_pdl(route_kernel<VPL>, dim3((unsigned)blocks), dim3(threads), 0, st, logits, T, E,
+                       a, ids, w);
 }
 
 }  // namespace

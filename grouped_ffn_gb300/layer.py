@@ -24,7 +24,10 @@ class MoELayer:
                  topk_groups: int = 1, group_topn: int = 1,
                  shared_w_gate_up: Optional[torch.Tensor] = None,
                  shared_w_down: Optional[torch.Tensor] = None, device="cuda",
-                 packed: bool = True):
+                 packed: bool = True, replica_relax: Optional[tuple] = None):
+        """replica_relax=(c_num, c_den) chooses each assignment's replica by
+        locality-preferred water-filling with load bounds C = c_num/c_den
+        (moe_route_replicas); None keeps the fixed replica rule."""
         self.H, self.I, self.E, self.k = H, I, E, k
         self.placement = placement
         self.packed = packed
@@ -57,7 +60,9 @@ class MoELayer:
         self.balancedness = torch.empty(1, dtype=torch.float64, device=dev)
         self.max_count = torch.empty(1, **i32)
         self.total = torch.empty(1, dtype=torch.int64, device=dev)
-        self.ws = moe.new_workspace(max_tokens, k, S, device=dev)
+        self.ws = moe.new_workspace(max_tokens, k, S, device=dev, n_experts=E, n_ranks=R)
+        self.replica_relax = replica_relax
+        self.inter_node = torch.zeros(1, **i32)
         if shared_w_gate_up is not None:
             self.shared_I = shared_w_gate_up.shape[1] // 2
             self.shared_h = torch.empty(max_tokens, self.shared_I, **bf)
@@ -66,9 +71,11 @@ class MoELayer:
             self._shared_offsets = {}
         else:
             self.shared_I = 0
-        # per step: route, layout scan + finalize, permute, 2 FFN, combine,
-        # balance (+2 shared FFN); packing happens once, here
-        self.launches_per_step = 8 + (2 if shared_w_gate_up is not None else 0)
+        # per step: route, layout scan + finalize, permute, FFN, combine,
+        # balance (+1 shared FFN, +4 replica routing: prep, key scan,
+        # water-fill, assign); packing happens once, here
+        self.launches_per_step = 7 + (1 if shared_w_gate_up is not None else 0) + \
+            (4 if replica_relax is not None else 0)
 
     @staticmethod
     def _pack(w_gate_up, w_down):
@@ -102,9 +109,16 @@ class MoELayer:
         ids, w = self.topk_ids[:T], self.topk_w[:T]
         moe.moe_route(logits, self.cfg, ids, w, self.ws, stream)
         mark("route")
-        moe.moe_dispatch_layout(ids, self.placement, self.slot[:A], self.seg_counts,
-                                self.seg_offsets, self.dest_row[:A], self.src_assign[:A],
-                                self.rank_counts, self.ws, stream)
+        if self.replica_relax is None:
+            moe.moe_dispatch_layout(ids, self.placement, self.slot[:A], self.seg_counts,
+                                    self.seg_offsets, self.dest_row[:A], self.src_assign[:A],
+                                    self.rank_counts, self.ws, stream)
+        else:
+            moe.moe_route_replicas(ids, self.placement, *self.replica_relax, self.slot[:A],
+                                   self.inter_node, self.ws, stream)
+            moe.moe_dispatch_layout_routed(ids, self.slot[:A], self.placement, self.seg_counts,
+                                           self.seg_offsets, self.dest_row[:A],
+                                           self.src_assign[:A], self.rank_counts, self.ws, stream)
         mark("layout")
         moe.moe_permute(x, self.k, self.dest_row[:A], self.x_perm[:A], self.ws, stream)
         mark("permute")

@@ -65,6 +65,11 @@ _SIGNATURES = {
                                            _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_layout_noalloc": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC),
                                                    _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_route_replicas_workspace_size": (_SZ, [_I64, _I32, _I32, _I32, _I32]),
+    "moe_route_replicas": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC), _I32, _I32,
+                                          _P, _P, _P, _SZ, _P]),
+    "moe_dispatch_layout_routed": (ctypes.c_int, [_P, _P, _I64, _I32, ctypes.POINTER(PlacementC),
+                                                  _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _I32, _I32,
                                        _P, _P, _P, _SZ, _P]),
@@ -125,9 +130,14 @@ def moe_workspace_size(T: int, k: int, n_slots: int) -> int:
     return int(lib().moe_workspace_size(T, k, n_slots))
 
 
-def new_workspace(T: int, k: int, n_slots: int, device=None, stream=None) -> torch.Tensor:
-    """Allocate (torch) and zero a workspace for calls on up to T tokens."""
+def new_workspace(T: int, k: int, n_slots: int, device=None, stream=None,
+                  n_experts: int = 0, n_ranks: int = 0) -> torch.Tensor:
+    """Allocate (torch) and zero a workspace for calls on up to T tokens
+    (large enough for replica routing too when n_experts and n_ranks are
+    given)."""
     n = max(moe_workspace_size(T, k, n_slots), WS_STATUS_BYTES)
+    if n_experts and n_ranks:
+        n = max(n, moe_route_replicas_workspace_size(T, k, n_experts, n_slots, n_ranks))
     ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
     moe_workspace_init(ws, stream)
     return ws
@@ -217,6 +227,37 @@ def moe_dispatch_layout_noalloc(topk_ids, placement: DevicePlacement, slot, seg_
         _ptr(topk_ids), T, k, ctypes.byref(placement.c), _ptr(slot), _ptr(seg_counts),
         _ptr(seg_offsets), _ptr(dest_row), _ptr(src_assign), _ptr(rank_counts), _ptr(status),
         _stream(stream)))
+
+
+def moe_route_replicas_workspace_size(T: int, k: int, n_experts: int, n_slots: int,
+                                      n_ranks: int) -> int:
+    return int(lib().moe_route_replicas_workspace_size(T, k, n_experts, n_slots, n_ranks))
+
+
+def moe_route_replicas(topk_ids, placement: DevicePlacement, c_num: int, c_den: int, slot,
+                       inter_node, ws, stream=None):
+    """Locality-preferred replica choice per assignment (water-filling under
+    load bounds C = c_num / c_den); inter_node is a device int32[1]."""
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(slot, torch.int32, "slot")
+    _need(inter_node, torch.int32, "inter_node")
+    T, k = topk_ids.shape
+    _check("moe_route_replicas", lib().moe_route_replicas(
+        _ptr(topk_ids), T, k, ctypes.byref(placement.c), c_num, c_den, _ptr(slot),
+        _ptr(inter_node), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_dispatch_layout_routed(topk_ids, slot_in, placement: DevicePlacement, seg_counts,
+                               seg_offsets, dest_row, src_assign, rank_counts, ws, stream=None):
+    for n, t in (("topk_ids", topk_ids), ("slot_in", slot_in), ("seg_counts", seg_counts),
+                 ("seg_offsets", seg_offsets), ("dest_row", dest_row),
+                 ("src_assign", src_assign), ("rank_counts", rank_counts)):
+        _need(t, torch.int32, n)
+    T, k = topk_ids.shape
+    _check("moe_dispatch_layout_routed", lib().moe_dispatch_layout_routed(
+        _ptr(topk_ids), _ptr(slot_in), T, k, ctypes.byref(placement.c), _ptr(seg_counts),
+        _ptr(seg_offsets), _ptr(dest_row), _ptr(src_assign), _ptr(rank_counts), _ptr(ws),
+        ws.numel(), _stream(stream)))
 
 
 def moe_permute(x, k: int, dest_row, x_perm, ws, stream=None):

@@ -21,7 +21,10 @@
  *    contiguous.  All bf16 pointers must be 16-byte aligned.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *    call is asynchronous on that stream and never synchronises the host,
- *    except moe_check_device_status.
+ *    except moe_check_device_status.  Route, layout, permute, combine and
+ *    balance use programmatic dependent launch: each kernel may start while
+ *    its predecessor on the stream drains and waits (griddepcontrol.wait)
+ *    before reading anything.
  *  - Errors found on the host (bad sizes, NULL pointers, unsupported shapes)
  *    return a status at once and launch nothing.  Errors found on the
  *    device (an expert id or row index out of range, a bounded wait that
@@ -151,13 +154,63 @@ moe_status moe_route(const float *logits, int64_t T, int32_t E, const moe_route_
  *  Device errors: MOE_ERR_DEVICE_INDEX (expert id outside [0,E)),
  *  MOE_ERR_PLACEMENT (tables inconsistent), MOE_ERR_DEVICE_TIMEOUT.
  *  Limits: n_slots <= 1024, n_ranks <= 1024, n_experts <= 4096, T*k < 2^30.
- *  ws: moe_workspace_size(T,k,S). */
+ *  ws: moe_workspace_size(T,k,S).  The scan's ticket and flags in ws must be
+ *  zero on entry; moe_workspace_init makes them so and every call leaves
+ *  them zero again (no per-call memset). */
 moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k,
                                const moe_placement *placement, int32_t *slot,
                                int32_t *seg_counts, int32_t *seg_offsets,
                                int32_t *dest_row, int32_t *src_assign,
                                int32_t *rank_counts, void *ws, size_t ws_bytes,
                                void *stream);
+
+/* Locality-preferred replica routing under relaxed load bounds: choose,
+ * for every assignment, which copy of its expert serves it.  "Zepp",
+ * Section 4.1, "Locality-preferred token routing" (Eq. 1: keep each
+ * source's expert selections, keep each replica's load within C * q_j of
+ * its balanced share q_j, minimise inter-node traffic) and Section 5,
+ * "Routing" (greedy water-filling: the source's own GPU first, then its
+ * node, then remote nodes, each allocation limited by the replica's
+ * remaining capacity while reserving enough demand for the other replicas'
+ * lower bounds).  Readings fixed here:
+ *  - per expert with several replicas, demand d_i = its assignments whose
+ *    token lives on rank i (token_src_rank, or t mod R);
+ *  - integer targets q_p = floor(D/n) + (p < D mod n) over the replicas in
+ *    ascending rank; bounds q_p -+ floor(C*D/n), lower bound >= 0, with
+ *    C = c_num / c_den;
+ *  - sources in ascending rank; passes own GPU, own node, remote, each
+ *    over replicas in ascending rank; then a completion pass (replicas
+ *    below their lower bound first, then any with capacity);
+ *  - a source's assignments, in ascending assignment order, fill its
+ *    destinations in locality order (own GPU, own node, remote).
+ *  The refinement that consolidates a token's remote requests onto fewer
+ *  nodes is not applied.
+ *  slot        device int32 [T*k] (output): the chosen slot per assignment.
+ *  inter_node  device int32 scalar (output): assignments whose slot is on a
+ *              node other than their token's.
+ *  ws: moe_route_replicas_workspace_size(T, k, E, S, R) bytes (it also
+ *  covers moe_dispatch_layout_routed and moe_grouped_ffn on the same
+ *  workspace).  Limits: (n_slots - n_experts) * n_ranks <= 1024, at most 16
+ *  copies of an expert.  Device errors: MOE_ERR_DEVICE_INDEX,
+ *  MOE_ERR_PLACEMENT, MOE_ERR_DEVICE_TIMEOUT. */
+size_t moe_route_replicas_workspace_size(int64_t T, int32_t k, int32_t n_experts,
+                                         int32_t n_slots, int32_t n_ranks);
+moe_status moe_route_replicas(const int32_t *topk_ids, int64_t T, int32_t k,
+                              const moe_placement *placement, int32_t c_num, int32_t c_den,
+                              int32_t *slot, int32_t *inter_node, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/* moe_dispatch_layout with each assignment's slot already chosen (for
+ * example by moe_route_replicas) instead of the fixed replica rule; same
+ * outputs and passage ("14. Serving Mixture-of-Experts Models", "Follow one
+ * token", steps 1-2).  slot_in[a] must host topk_ids[a]'s expert, else
+ * MOE_ERR_PLACEMENT is recorded and the assignment is skipped. */
+moe_status moe_dispatch_layout_routed(const int32_t *topk_ids, const int32_t *slot_in, int64_t T,
+                                      int32_t k, const moe_placement *placement,
+                                      int32_t *seg_counts, int32_t *seg_offsets,
+                                      int32_t *dest_row, int32_t *src_assign,
+                                      int32_t *rank_counts, void *ws, size_t ws_bytes,
+                                      void *stream);
 
 /* moe_dispatch_layout without a workspace: for callers that cannot
  * allocate device memory when they run the layout, such as a serving engine
@@ -214,7 +267,7 @@ moe_status moe_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
  *  cores with TMA-fed shared memory and TMEM accumulators; both GEMMs run
  *  in one cooperative launch, a segment's down-projection tiles starting
  *  as soon as all its gate/up tiles have stored h.
- *  ws: at least 512 + 4*S bytes (moe_workspace_size(T, k, S) is enough).
+ *  ws: at least 256 + 4*S bytes (moe_workspace_size(T, k, S) is enough).
  *  Limits: H % 256 == 0, I % 128 == 0, S <= 1024, n_rows < 2^31,
  *  E*2I*H/64 < 2^31.
  *  Device errors: MOE_ERR_DEVICE_INDEX (expert id), MOE_ERR_DEVICE_TIMEOUT. */

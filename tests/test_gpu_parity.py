@@ -498,3 +498,82 @@ def test_shared_expert_alone_matches_dense_definition():
     m.moe_check_device_status(ws)
     rh, ry = oracle.swiglu_expert(f64(x), f64(sgu[0]), f64(sd[0]), w.shared_I)
     assert_close(f64(y), ry, "shared y")
+
+
+# ------------------------------------------------------------------ replica routing (water-filling)
+def _gpu_route_replicas(ids, pl, c):
+    m = moe()
+    pl_dev = m.DevicePlacement.from_tables(pl)
+    T, k = ids.shape
+    ws = m.new_workspace(T, k, pl.n_slots, n_experts=pl.n_experts, n_ranks=pl.n_ranks)
+    slot = torch.full((T * k,), -9, dtype=torch.int32, device="cuda")
+    inter = torch.full((1,), -9, dtype=torch.int32, device="cuda")
+    m.moe_route_replicas(ids, pl_dev, c[0], c[1], slot, inter, ws)
+    m.moe_check_device_status(ws)
+    return slot, int(inter.item()), pl_dev, ws
+
+
+@pytest.mark.parametrize("zipf,c", [(1.0, (0, 1)), (1.0, (1, 10)), (1.0, (1, 1)), (0.0, (1, 4)),
+                                    (1.5, (3, 10))])
+def test_route_replicas_parity(zipf, c):
+    w = wl.WORKLOADS["replica"].with_zipf(zipf)
+    pl = wl.make_placement(w)
+    ids, _ = gpu_route(w, wl.make_logits(w, "cuda"))
+    ids_np = ids.cpu().numpy()
+    slot, inter, pl_dev, ws = _gpu_route_replicas(ids, pl, c)
+    ref_slot, ref_inter = oracle.route_replicas_waterfill(ids_np, pl, *c)
+    assert np.array_equal(slot.cpu().numpy(), ref_slot)
+    assert inter == ref_inter
+    # the layout from these slots, on the same workspace
+    m = moe()
+    A, S, R = w.A, pl.n_slots, w.R
+    out = [torch.full((n,), -7, dtype=torch.int32, device="cuda") for n in (S, S + 1, A, A, R)]
+    m.moe_dispatch_layout_routed(ids, slot, pl_dev, *out, ws)
+    m.moe_check_device_status(ws)
+    ref = oracle.dispatch_layout_from_slots(ids_np, ref_slot, pl)
+    for key, t in zip(("seg_counts", "seg_offsets", "dest_row", "src_assign", "rank_counts"), out):
+        assert np.array_equal(t.cpu().numpy(), ref[key]), key
+
+
+def test_route_replicas_skewed_sources_and_figure6():
+    rng = np.random.default_rng(5)
+    # tokens concentrated on node 0: local replicas overflow their bounds
+    w = wl.WORKLOADS["replica"].scaled(T=3000)
+    hosts = wl.replica_hosts(w)
+    src = np.where(rng.random(w.T) < 0.7, rng.integers(0, 4, w.T), rng.integers(0, 16, w.T))
+    pl = wl.placement_from_hosts(w.E, w.R, w.ranks_per_node, hosts, token_src_rank=src)
+    ids, _ = gpu_route(w, wl.make_logits(w, "cuda"))
+    for c in [(0, 1), (1, 5), (2, 1)]:
+        slot, inter, _, _ = _gpu_route_replicas(ids, pl, c)
+        ref_slot, ref_inter = oracle.route_replicas_waterfill(ids.cpu().numpy(), pl, *c)
+        assert np.array_equal(slot.cpu().numpy(), ref_slot) and inter == ref_inter
+    # the "Zepp" Figure 6 scenario
+    R, rpn = 8, 2
+    src = np.concatenate([np.arange(16) % R] * 2)
+    pl = wl.placement_from_hosts(2, R, rpn, [[0, 2, 4, 6], [1, 3, 5]], token_src_rank=src)
+    ids6 = torch.tensor(np.concatenate([np.zeros(16), np.ones(16)]).astype(np.int32)[:, None],
+                        device="cuda")
+    slot, inter, _, _ = _gpu_route_replicas(ids6, pl, (1, 1))
+    ref_slot, ref_inter = oracle.route_replicas_waterfill(ids6.cpu().numpy(), pl, 1, 1)
+    assert np.array_equal(slot.cpu().numpy(), ref_slot) and inter == ref_inter == 4
+
+
+def test_routed_layer_output_equals_fixed_rule_output():
+    """Copies of an expert hold the same weights and rows are independent,
+    so choosing other copies must not change the layer's output bit."""
+    from grouped_ffn_gb300 import MoELayer
+    m = moe()
+    w = wl.WORKLOADS["replica"].scaled(T=4096)
+    pl = wl.make_placement(w)
+    logits, x = wl.make_logits(w, "cuda"), wl.make_x(w, "cuda")
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    outs = []
+    for relax in (None, (1, 10)):
+        layer = MoELayer(H=w.H, I=w.I, E=w.E, k=w.k, placement=m.DevicePlacement.from_tables(pl),
+                         w_gate_up=wgu, w_down=wd, max_tokens=w.T, replica_relax=relax)
+        y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+        layer.forward(logits, x, y)
+        layer.check()
+        outs.append((y, layer.rank_counts.clone(), int(layer.inter_node.item())))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert int(outs[0][1].sum()) == int(outs[1][1].sum()) == w.A
