@@ -171,8 +171,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ algorithmic work
-def algorithmic(w: wl.Workload, seg_counts: np.ndarray, slot_expert: np.ndarray):
-    """Bytes / flops per step by stage (the per-unit figures times the units)."""
+def algorithmic(w: wl.Workload, seg_counts: np.ndarray, slot_expert: np.ndarray,
+                gather: bool = False):
+    """Bytes / flops per step by stage (the per-unit figures times the units).
+    With the gather-fused FFN the rows come from x (2H bytes per token)
+    instead of the permuted copy (2H per assignment)."""
     A, T, H, I = w.A, w.T, w.H, w.I
     active_slots = seg_counts > 0
     # weights are read once per active expert slot (replicas re-read: they
@@ -183,7 +186,7 @@ def algorithmic(w: wl.Workload, seg_counts: np.ndarray, slot_expert: np.ndarray)
         "route": dict(bytes=T * w.E * 4 + T * w.k * 8),
         "layout": dict(bytes=A * 4 * 4 + A * 4),
         "permute": dict(bytes=T * H * 2 + A * H * 2),
-        "grouped_ffn": dict(bytes=wbytes + A * H * 2 + A * I * 2 * 2 + A * H * 2,
+        "grouped_ffn": dict(bytes=wbytes + (T if gather else A) * H * 2 + A * I * 2 * 2 + A * H * 2,
                             flops=6 * A * H * I, weight_bytes=wbytes),
         "combine": dict(bytes=A * H * 2 + T * H * 2 + (T * H * 2 if w.shared_I else 0) + A * 8),
     }
@@ -209,7 +212,8 @@ def run_ours(args, world, rank, local):
                      w_gate_up=wgu, w_down=wd, max_tokens=w.T, score_fn=w.score_fn,
                      n_groups=w.n_groups, topk_groups=w.topk_groups, group_topn=w.group_topn,
                      shared_w_gate_up=sgu, shared_w_down=sd, device=dev,
-                     packed=not args.unpacked, replica_relax=parse_relax(args.replica_relax))
+                     packed=not args.unpacked, replica_relax=parse_relax(args.replica_relax),
+                     gather=args.gather)
     y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -288,11 +292,14 @@ def run_ours(args, world, rank, local):
 
     peaks = load_peaks()
     seg_counts = layer.seg_counts.cpu().numpy()
-    alg = algorithmic(w, seg_counts, pl.slot_expert)
+    alg = algorithmic(w, seg_counts, pl.slot_expert, args.gather)
     stages = {}
     for n in names:
         if n == "balance":
             stages[n] = {"us": stage_ms[n] * 1e3}
+            continue
+        if n == "permute" and args.gather:
+            stages[n] = {"us": stage_ms[n] * 1e3, "fused_into": "grouped_ffn"}
             continue
         a = alg[n]
         s = {"us": stage_ms[n] * 1e3, "gbs": a["bytes"] / (stage_ms[n] * 1e-3) / 1e9}
@@ -334,6 +341,7 @@ def run_ours(args, world, rank, local):
                    "simulated_ranks": w.R, "zipf_s": w.zipf_s, "assignments": w.A,
                    "parallelism": f"replicas{world}",
                    "weight_layout": "plain" if args.unpacked else "packed",
+                   "dispatch": "gather-fused" if args.gather else "permute",
                    "l2": "inputs larger than L2: %.2f GB of expert weights stream per step"
                          % (g["weight_bytes"] / 1e9)},
         "e2e": e2e,
@@ -341,7 +349,7 @@ def run_ours(args, world, rank, local):
         "roofline": roof,
         "stages": stages,
         "gemm_pct_bf16_peak": 100.0 * stages["grouped_ffn"]["tflops"] / peaks["bf16_tflops"],
-        "permute_pct_hbm": 100.0 * stages["permute"]["hbm_frac"],
+        "permute_pct_hbm": None if args.gather else 100.0 * stages["permute"]["hbm_frac"],
         "combine_pct_hbm": 100.0 * stages["combine"]["hbm_frac"],
         "balancedness": float(layer.balancedness.item()),
         "clocks": clocks.summary(),
@@ -588,6 +596,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gather", action="store_true",
+                    help="FFN reads rows from x through the inverse permutation (no permute)")
     ap.add_argument("--replica-relax", default="",
                     help="choose replicas by water-filling with load bounds C, e.g. 1/10")
     ap.add_argument("--unpacked", action="store_true",

@@ -71,7 +71,8 @@ struct __align__(8) Bars {
 constexpr size_t kBarsOff = (size_t)kStages * kStageBytes;
 constexpr size_t kMiscOff = kBarsOff + sizeof(Bars);
 constexpr size_t kSegOff = kMiscOff + 16;
-constexpr size_t kSmemBytes = kSegOff + (size_t)(4 * kMaxSegs + 3) * 4 + 1024;
+constexpr size_t kGidxOff = kSegOff + (size_t)(4 * kMaxSegs + 3) * 4;  // [kBM] gathered token rows
+constexpr size_t kSmemBytes = kGidxOff + kBM * 4 + 1024;
 
 // One GEMM phase: gate/up with the SwiGLU epilogue (mode 0) or down (mode 1).
 struct Phase {
@@ -93,6 +94,10 @@ struct FfnParams {
   int32_t n_phases;   // 2: phase 1 reads what phase 0 writes, in the same launch
   int32_t *ready;     // [S] finished phase-0 tiles per segment (zeroed by the host)
   int32_t interleave; // merge multi-tile and one-tile segments' tiles (see decode)
+  // Gather mode: phase 0 reads row r of a segment from x[gather_src[r] / gather_k]
+  // (token rows, gather_T of them) instead of a permuted copy.
+  const int32_t *gather_src;
+  int32_t gather_k, gather_T;
   int32_t *status;
   Phase ph[2];
 };
@@ -168,6 +173,19 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Four rows (y0..y3) of a one-row-high box at column x, into 4 consecutive
+// 128-byte rows of shared memory (same swizzle as a tiled load there).
+__device__ __forceinline__ void tma_gather4(void *smem_dst, const CUtensorMap *m, int32_t x,
+                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -406,19 +424,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t total = T0 + mtot * NB1;
 
   if (warp == 0) {
+    // ------------------------------------------------ TMA producer (lane 0;
+    // the whole warp stages gathered row indices)
+    int32_t *gidx = reinterpret_cast<int32_t *>(smem + kGidxOff);
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer
       prefetch_tmap(&tmap_a0);
       prefetch_tmap(&tmap_b0);
       if (p.n_phases > 1) {
         prefetch_tmap(&tmap_a1);
         prefetch_tmap(&tmap_b1);
       }
-      int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_par = 0;
-      bool ok = true;
-      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = decode(t, T0, pre_h, pre_c, p.S, NB0, NB1, Mh, Mc);
+    }
+    int stage = 0;
+    uint32_t phase = 0, armed = 0, armed_par = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileInfo ti = decode(t, T0, pre_h, pre_c, p.S, NB0, NB1, Mh, Mc);
+      const bool gather = p.gather_src != nullptr && ti.ph == 0;
+      if (gather) {  // token row of each of the tile's 128 rows (row 0 past the end)
+        const int row0 = seg_off[ti.s] + ti.m_blk * kBM;
+        const int row_end = min(seg_off[ti.s + 1], p.n_rows);
+        for (int j = lane; j < kBM; j += 32) {
+          int tok = 0;
+          if (row0 + j < row_end) {
+            tok = __ldg(p.gather_src + row0 + j) / p.gather_k;
+            if (tok < 0 || tok >= p.gather_T) tok = 0;
+          }
+          gidx[j] = tok;
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
         const Phase &P = p.ph[ti.ph];
         const CUtensorMap *ma = ti.ph ? &tmap_a1 : &tmap_a0;
         const CUtensorMap *mb = ti.ph ? &tmap_b1 : &tmap_b0;
@@ -444,9 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               __nanosleep(64);
             }
-            if (!ok) break;
           }
-          fence_proxy_async_global();
+          if (ok) fence_proxy_async_global();
         }
         const int e = seg_exp[ti.s];
         const int row_a = seg_off[ti.s] + ti.m_blk * kBM;
@@ -458,14 +493,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_b1 = p.b_packed ? row_b0 + 128 : row_b0 + P.b_second_off;
         const int b_x_step = p.b_packed ? 0 : kBK;
         const int b_y_step = p.b_packed ? 256 : 0;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = 0; kb < nk && ok; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.status, kid)) {
             ok = false;
             break;
           }
           uint8_t *sa = smem + (size_t)stage * kStageBytes;
           mbar_arrive_expect_tx(&bars->full[stage], kStageBytes);
-          tma_load_2d(sa, ma, kb * kBK, row_a, &bars->full[stage]);
+          if (gather) {
+#pragma unroll 4
+            for (int g = 0; g < kBM / 4; ++g)
+              tma_gather4(sa + g * 512, ma, kb * kBK, gidx[4 * g], gidx[4 * g + 1],
+                          gidx[4 * g + 2], gidx[4 * g + 3], &bars->full[stage]);
+          } else {
+            tma_load_2d(sa, ma, kb * kBK, row_a, &bars->full[stage]);
+          }
           tma_load_2d(sa + kABytes, mb, kb * b_x_step, row_b0 + kb * b_y_step, &bars->full[stage]);
           tma_load_2d(sa + kABytes + kBHalfBytes, mb, kb * b_x_step, row_b1 + kb * b_y_step,
                       &bars->full[stage]);
@@ -477,9 +519,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // lane 0 is done with gidx too
+      if (!ok) break;
+    }
+    if (lane == 0)
       for (int i = 0; i < kStages; ++i)  // own copies land before the CTA exits
         if ((armed >> i) & 1u) mbar_wait_drain(&bars->full[i], (armed_par >> i) & 1u);
-    }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
@@ -610,13 +655,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 row-major [rows, cols] map with a 64-column x 128-row box.
-bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+// 2-D bf16 row-major [rows, cols] map with a 64-column x box_rows box
+// (128 for tiled loads, 1 for tile::gather4).
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
+              uint32_t box_rows = 128) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, 128};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -710,10 +757,15 @@ moe_status check_ffn_args(const uint16_t *x_perm, int64_t n_rows, const int32_t 
   return MOE_OK;
 }
 
+// gather_src == nullptr: x_perm holds the n_rows dispatched rows.  Otherwise
+// x_perm is the token matrix x [gather_T, H] and dispatched row r is token
+// gather_src[r] / gather_k (read with tile::gather4, no permuted copy).
 moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_offsets,
                    const int32_t *seg_expert, int32_t S, int32_t E, const uint16_t *w_gate_up,
                    const uint16_t *w_down, int32_t H, int32_t I, uint16_t *h, uint16_t *y_perm,
-                   void *ws, size_t ws_bytes, void *stream, bool packed) {
+                   void *ws, size_t ws_bytes, void *stream, bool packed,
+                   const int32_t *gather_src = nullptr, int32_t gather_k = 1,
+                   int64_t gather_T = 0) {
   if (moe_status s = check_ffn_args(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up,
                                     w_down, H, I, h, y_perm, ws, ws_bytes))
     return s;
@@ -725,7 +777,9 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   const uint64_t gu_cols = packed ? (uint64_t)kBK : (uint64_t)H;
   const uint64_t d_rows = packed ? (uint64_t)E * H * I / kBK : (uint64_t)E * H;
   const uint64_t d_cols = packed ? (uint64_t)kBK : (uint64_t)I;
-  if (!make_map(&m_x, x_perm, (uint64_t)n_rows, (uint64_t)H) ||
+  const bool ok_x = gather_src ? make_map(&m_x, x_perm, (uint64_t)gather_T, (uint64_t)H, 1)
+                               : make_map(&m_x, x_perm, (uint64_t)n_rows, (uint64_t)H);
+  if (!ok_x ||
       !make_map(&m_wgu, w_gate_up, gu_rows, gu_cols) ||
       !make_map(&m_h, h, (uint64_t)n_rows, (uint64_t)I) ||
       !make_map(&m_wd, w_down, d_rows, d_cols))
@@ -747,6 +801,9 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   p.ready = ready;
   p.status = moe_host::status_ptr(ws);
   p.interleave = interleave_tiles();
+  p.gather_src = gather_src;
+  p.gather_k = gather_k;
+  p.gather_T = (int32_t)gather_T;
   Phase &g = p.ph[0];  // gate/up + SwiGLU -> h
   g.K = H;
   g.n_blocks = I / 128;
@@ -789,6 +846,19 @@ extern "C" moe_status moe_grouped_ffn_packed(const uint16_t *x_perm, int64_t n_r
                                              size_t ws_bytes, void *stream) {
   return run_ffn(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up_packed, w_down_packed, H,
                  I, h, y_perm, ws, ws_bytes, stream, true);
+}
+
+extern "C" moe_status moe_grouped_ffn_gather(const uint16_t *x, int64_t T, int32_t k,
+                                             const int32_t *src_assign, int64_t n_rows,
+                                             const int32_t *seg_offsets, const int32_t *seg_expert,
+                                             int32_t S, int32_t E, const uint16_t *w_gate_up_packed,
+                                             const uint16_t *w_down_packed, int32_t H, int32_t I,
+                                             uint16_t *h, uint16_t *y_perm, void *ws,
+                                             size_t ws_bytes, void *stream) {
+  if (T < 0 || k < 1 || (n_rows > 0 && (!src_assign || T == 0))) return MOE_ERR_INVALID_ARG;
+  if (T >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  return run_ffn(x, n_rows, seg_offsets, seg_expert, S, E, w_gate_up_packed, w_down_packed, H, I,
+                 h, y_perm, ws, ws_bytes, stream, true, src_assign, k, T);
 }
 
 extern "C" moe_status moe_pack_expert_weights(const uint16_t *w_gate_up, const uint16_t *w_down,

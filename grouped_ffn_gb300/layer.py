@@ -24,10 +24,16 @@ class MoELayer:
                  topk_groups: int = 1, group_topn: int = 1,
                  shared_w_gate_up: Optional[torch.Tensor] = None,
                  shared_w_down: Optional[torch.Tensor] = None, device="cuda",
-                 packed: bool = True, replica_relax: Optional[tuple] = None):
+                 packed: bool = True, replica_relax: Optional[tuple] = None,
+                 gather: bool = False):
         """replica_relax=(c_num, c_den) chooses each assignment's replica by
         locality-preferred water-filling with load bounds C = c_num/c_den
-        (moe_route_replicas); None keeps the fixed replica rule."""
+        (moe_route_replicas); None keeps the fixed replica rule.
+        gather=True reads the FFN's rows straight from x through the
+        inverse permutation (moe_grouped_ffn_gather): no permute step."""
+        if gather and not packed:
+            raise ValueError("gather mode streams packed weights")
+        self.gather = gather
         self.H, self.I, self.E, self.k = H, I, E, k
         self.placement = placement
         self.packed = packed
@@ -54,7 +60,7 @@ class MoELayer:
         self.dest_row = torch.empty(A, **i32)
         self.src_assign = torch.empty(A, **i32)
         self.rank_counts = torch.empty(R, **i32)
-        self.x_perm = torch.empty(A, H, **bf)
+        self.x_perm = torch.empty(0 if gather else A, H, **bf)
         self.h = torch.empty(A, I, **bf)
         self.y_perm = torch.empty(A, H, **bf)
         self.balancedness = torch.empty(1, dtype=torch.float64, device=dev)
@@ -75,7 +81,7 @@ class MoELayer:
         # balance (+1 shared FFN, +4 replica routing: prep, key scan,
         # water-fill, assign); packing happens once, here
         self.launches_per_step = 7 + (1 if shared_w_gate_up is not None else 0) + \
-            (4 if replica_relax is not None else 0)
+            (4 if replica_relax is not None else 0) - (1 if gather else 0)
 
     @staticmethod
     def _pack(w_gate_up, w_down):
@@ -120,10 +126,16 @@ class MoELayer:
                                            self.seg_offsets, self.dest_row[:A],
                                            self.src_assign[:A], self.rank_counts, self.ws, stream)
         mark("layout")
-        moe.moe_permute(x, self.k, self.dest_row[:A], self.x_perm[:A], self.ws, stream)
-        mark("permute")
-        self._ffn(self.x_perm[:A], self.seg_offsets, self.placement.slot_expert,
-                  self.w_gate_up, self.w_down, self.h[:A], self.y_perm[:A], self.ws, stream)
+        if self.gather:
+            mark("permute")
+            moe.moe_grouped_ffn_gather(x, self.k, self.src_assign[:A], self.seg_offsets,
+                                       self.placement.slot_expert, self.w_gate_up, self.w_down,
+                                       self.h[:A], self.y_perm[:A], self.ws, stream)
+        else:
+            moe.moe_permute(x, self.k, self.dest_row[:A], self.x_perm[:A], self.ws, stream)
+            mark("permute")
+            self._ffn(self.x_perm[:A], self.seg_offsets, self.placement.slot_expert,
+                      self.w_gate_up, self.w_down, self.h[:A], self.y_perm[:A], self.ws, stream)
         mark("grouped_ffn")
         shared = None
         if self.shared_I:

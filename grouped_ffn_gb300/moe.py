@@ -75,6 +75,8 @@ _SIGNATURES = {
                                        _P, _P, _P, _SZ, _P]),
     "moe_grouped_ffn_packed": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _I32, _I32,
                                               _P, _P, _P, _SZ, _P]),
+    "moe_grouped_ffn_gather": (ctypes.c_int, [_P, _I64, _I32, _P, _I64, _P, _P, _I32, _I32, _P,
+                                              _P, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "moe_pack_expert_weights": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "moe_balance_stats": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -307,6 +309,29 @@ def moe_grouped_ffn_packed(x_perm, seg_offsets, seg_expert, w_gate_up_packed, w_
     _check("moe_grouped_ffn_packed", lib().moe_grouped_ffn_packed(
         _ptr(x_perm), n_rows, _ptr(seg_offsets), _ptr(seg_expert), S, E, _ptr(w_gate_up_packed),
         _ptr(w_down_packed), H, I, _ptr(h), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_grouped_ffn_gather(x, k: int, src_assign, seg_offsets, seg_expert, w_gate_up_packed,
+                           w_down_packed, h, y_perm, ws, stream=None):
+    """The grouped FFN reading its gate/up rows straight from x through
+    src_assign (TMA gather), with packed weights; no permuted copy."""
+    for n, t in (("x", x), ("w_gate_up_packed", w_gate_up_packed),
+                 ("w_down_packed", w_down_packed), ("h", h), ("y_perm", y_perm)):
+        _bf16(t, n)
+    _need(src_assign, torch.int32, "src_assign")
+    _need(seg_offsets, torch.int32, "seg_offsets")
+    _need(seg_expert, torch.int32, "seg_expert")
+    T, H = x.shape
+    n_rows = y_perm.shape[0]
+    E, two_i, H2 = w_gate_up_packed.shape
+    I = two_i // 2
+    if H2 != H or tuple(w_down_packed.shape) != (E, H, I) or tuple(h.shape) != (n_rows, I) \
+            or src_assign.numel() < n_rows:
+        raise ValueError("moe_grouped_ffn_gather: inconsistent shapes")
+    _check("moe_grouped_ffn_gather", lib().moe_grouped_ffn_gather(
+        _ptr(x), T, k, _ptr(src_assign), n_rows, _ptr(seg_offsets), _ptr(seg_expert),
+        seg_expert.numel(), E, _ptr(w_gate_up_packed), _ptr(w_down_packed), H, I, _ptr(h),
+        _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_pack_expert_weights(w_gate_up, w_down, w_gate_up_packed, w_down_packed, stream=None):

@@ -302,6 +302,24 @@ moe_status moe_grouped_ffn_packed(const uint16_t *x_perm, int64_t n_rows,
                                   uint16_t *h, uint16_t *y_perm, void *ws, size_t ws_bytes,
                                   void *stream);
 
+/* moe_grouped_ffn_packed without the permuted copy: dispatched row r of
+ * the gate/up GEMM is read straight from token row src_assign[r] / k of x
+ * with TMA tile::gather4 loads (four rows per instruction), so moe_permute
+ * and x_perm are not needed.  "Mixture-of-Experts Inference", "Optimized
+ * kernels for MoE" (a fused MoE kernel combines token permutation with the
+ * expert GEMMs); "Zepp", Section 5, "Transport" (expert GEMMs select their
+ * rows through gather indices instead of repacking).  Results are bit-
+ * identical to permute + moe_grouped_ffn_packed.
+ *  x          device bf16 [T, H]; src_assign device int32 [n_rows] (from
+ *             moe_dispatch_layout); other arguments as moe_grouped_ffn_packed. */
+moe_status moe_grouped_ffn_gather(const uint16_t *x, int64_t T, int32_t k,
+                                  const int32_t *src_assign, int64_t n_rows,
+                                  const int32_t *seg_offsets, const int32_t *seg_expert,
+                                  int32_t S, int32_t E, const uint16_t *w_gate_up_packed,
+                                  const uint16_t *w_down_packed, int32_t H, int32_t I,
+                                  uint16_t *h, uint16_t *y_perm, void *ws, size_t ws_bytes,
+                                  void *stream);
+
 /* Combine: y[t] = bf16(acc) with acc = shared[t] (or 0) and, for j = 0..k-1
  * in order, acc = fmaf(topk_w[t,j], y_perm[dest_row[t*k+j]], acc) in fp32.
  * "14. Serving Mixture-of-Experts Models", "Follow one token", step 4 (the

@@ -577,3 +577,63 @@ def test_routed_layer_output_equals_fixed_rule_output():
         outs.append((y, layer.rank_counts.clone(), int(layer.inter_node.item())))
     assert torch.equal(outs[0][0], outs[1][0])
     assert int(outs[0][1].sum()) == int(outs[1][1].sum()) == w.A
+
+
+# ------------------------------------------------------------------ gather-fused FFN (no permute)
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "group_limited", "replica"])
+def test_gather_layer_is_bit_identical_to_permuted_layer(name):
+    """Reading the FFN's rows straight from x through the inverse
+    permutation (TMA gather) must reproduce the permuted path bit for bit:
+    h, the expert outputs and the layer output."""
+    from grouped_ffn_gb300 import MoELayer
+    m = moe()
+    w = wl.WORKLOADS[name]
+    if name == "group_limited":
+        w = w.scaled(T=1024)
+    pl = wl.make_placement(w)
+    logits, x = wl.make_logits(w, "cuda"), wl.make_x(w, "cuda")
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    sgu, sd = wl.make_shared_weights(w, "cuda")
+    res = []
+    for gather in (False, True):
+        layer = MoELayer(H=w.H, I=w.I, E=w.E, k=w.k, placement=m.DevicePlacement.from_tables(pl),
+                         w_gate_up=wgu, w_down=wd, max_tokens=w.T, score_fn=w.score_fn,
+                         n_groups=w.n_groups, topk_groups=w.topk_groups, group_topn=w.group_topn,
+                         shared_w_gate_up=sgu, shared_w_down=sd, gather=gather)
+        y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+        layer.forward(logits, x, y)
+        layer.check()
+        res.append((layer.h[:w.A].clone(), layer.y_perm[:w.A].clone(), y))
+        del layer
+    for a, b in zip(res[0], res[1]):
+        assert torch.equal(a, b)
+
+
+def test_gather_ffn_ragged_segments_match_oracle():
+    """Small ragged case compared in full with the oracle, rows read through
+    a shuffled inverse permutation."""
+    m = moe()
+    H, I, k, T = 512, 384, 2, 400
+    counts = [130, 1, 0, 257, 128, 75, 209]
+    E = len(counts) + 1
+    w = wl.Workload("gath", 77, T=T, H=H, E=E, k=k, I=I, R=1, ranks_per_node=1)
+    A = sum(counts)
+    assert A == T * k
+    g = torch.Generator(device="cuda").manual_seed(17)
+    x = torch.randn(T, H, generator=g, device="cuda").to(torch.bfloat16)
+    src = torch.randperm(A, generator=g, device="cuda").to(torch.int32)
+    offs = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32, device="cuda")
+    se = torch.tensor([(3 * s + 1) % E for s in range(len(counts))], dtype=torch.int32, device="cuda")
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    pgu, pd = torch.empty_like(wgu), torch.empty_like(wd)
+    m.moe_pack_expert_weights(wgu, wd, pgu, pd)
+    h = torch.empty(A, I, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(A, H, dtype=torch.bfloat16, device="cuda")
+    ws = m.new_workspace(1, 1, len(counts))
+    m.moe_grouped_ffn_gather(x, k, src, offs, se, pgu, pd, h, y, ws)
+    m.moe_check_device_status(ws)
+    rows = f64(x)[src.cpu().numpy() // k]
+    rh, ry = oracle.grouped_ffn(rows, offs.cpu().numpy(), se.cpu().numpy(),
+                                oracle.bf16_bits_to_f64(bits(wgu)), oracle.bf16_bits_to_f64(bits(wd)), I)
+    assert_close(f64(h), rh, "h (gather)")
+    assert_close(f64(y), ry, "y_perm (gather)")
