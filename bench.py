@@ -283,6 +283,27 @@ def run_ours(args, world, rank, local):
                 for j, n in enumerate(names)}
     stage_ms.update(ffn_ms)   # the FFN figures come from the timed region
 
+    # Merge (simulated): inter-node dispatch messages before / after merge
+    # and the pre-reducing combine timed like the plain one (not in the step)
+    msgs = torch.zeros(2, dtype=torch.int32, device=dev)
+    y_m = torch.empty_like(y)
+    shared_arg = layer.shared_y[:w.T] if w.shared_I else None
+    mev = [ET() for _ in range(2)]
+    with torch.cuda.stream(stream):
+        for i in range(3 + K):
+            if i == 3:
+                mev[0].record(stream)
+            moe.moe_combine_merged(layer.y_perm[:w.A], layer.dest_row[:w.A], layer.topk_w[:w.T],
+                                   layer.slot[:w.A], layer.placement, y_m, msgs, layer.ws,
+                                   shared_arg, stream)
+        mev[1].record(stream)
+    stream.synchronize()
+    layer.check(stream)
+    merge = {"inter_node_assignments": int(msgs[0].item()),
+             "inter_node_messages_after_merge": int(msgs[1].item()),
+             "bytes_saved_per_step": (int(msgs[0].item()) - int(msgs[1].item())) * w.H * 2 * 2,
+             "combine_merged_us": mev[0].elapsed_time(mev[1]) / K * 1e3}
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(layer, logits, x, y, stream, world, K, W)
@@ -352,6 +373,7 @@ def run_ours(args, world, rank, local):
         "permute_pct_hbm": None if args.gather else 100.0 * stages["permute"]["hbm_frac"],
         "combine_pct_hbm": 100.0 * stages["combine"]["hbm_frac"],
         "balancedness": float(layer.balancedness.item()),
+        "merge": merge,
         "clocks": clocks.summary(),
     }
     if w.hot_experts > 0:

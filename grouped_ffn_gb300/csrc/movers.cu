@@ -123,6 +123,110 @@ __global__ void __launch_bounds__(kMoverThreads) combine_kernel(
   }
 }
 
+// Combine with node-local pre-reduction ("Zepp", Section 4.2, "Merge";
+// Algorithm 1's PreReduce and Reduce), simulated on one GPU: the weighted
+// outputs of a token's experts on one node are summed there (fp32 fmaf in
+// j order) and returned as one bf16 partial; the source adds the partials
+// in ascending node order onto the shared output (or 0) and rounds once.
+// Also counts the step's inter-node dispatch messages before merge (remote
+// assignments) and after it (distinct remote nodes per token).
+template <int KMAX>
+__global__ void __launch_bounds__(kMoverThreads) combine_merged_kernel(
+    const uint4 *__restrict__ yp, const int32_t *__restrict__ dest_row,
+    const float *__restrict__ topk_w, const int32_t *__restrict__ slot,
+    const int32_t *__restrict__ slot_rank, const int32_t *__restrict__ token_src_rank, int S,
+    int R, int rpn, int64_t T, int k, int H8, const uint4 *__restrict__ shared,
+    uint4 *__restrict__ y, int64_t A, int32_t *messages, int32_t *status) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    int32_t r[KMAX], nd[KMAX];
+    float w[KMAX];
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      nd[j] = 0x7fffffff;
+      if (j < k) {
+        r[j] = __ldg(dest_row + t * k + j);
+        w[j] = __ldg(topk_w + t * k + j);
+        const int s = __ldg(slot + t * k + j);
+        if (r[j] < 0 || r[j] >= A || s < 0 || s >= S) {
+          ok = false;
+        } else {
+          nd[j] = __ldg(slot_rank + s) / rpn;
+        }
+      }
+    }
+    if (!ok) {
+      if (threadIdx.x == 0)
+        moe::report_error(status, MOE_ERR_DEVICE_INDEX, (int32_t)t, moe::K_COMBINE);
+      continue;
+    }
+    if (threadIdx.x == 0) {
+      const int src = token_src_rank ? token_src_rank[t] : (int)(t % R);
+      const int sn = src / rpn;
+      int before = 0, after = 0;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k && nd[j] != sn) {
+          ++before;
+          bool first = true;
+          for (int i = 0; i < j; ++i)
+            if (nd[i] == nd[j]) first = false;
+          if (first) ++after;
+        }
+      }
+      if (before) {
+        atomicAdd(messages, before);
+        atomicAdd(messages + 1, after);
+      }
+    }
+    for (int c = threadIdx.x; c < H8; c += kMoverThreads) {
+      uint4 v[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) v[j] = moe::ld_stream_u4(yp + (int64_t)r[j] * H8 + c);
+      float acc[8];
+      if (shared) {
+        const uint4 sv = moe::ld_stream_u4(shared + t * H8 + c);
+        const uint32_t u[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = __uint_as_float(u[i] << 16);
+          acc[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      }
+      int prev = -1;
+      for (;;) {  // destination nodes in ascending order
+        int n = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (j < k && nd[j] > prev && nd[j] < n) n = nd[j];
+        if (n == 0x7fffffff) break;
+        float part[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (j < k && nd[j] == n) bf16x8_fma(v[j], w[j], part);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          acc[i] = __fadd_rn(acc[i], __bfloat162float(__float2bfloat16_rn(part[i])));
+        prev = n;
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      y[t * H8 + c] = o;
+    }
+  }
+}
+
 __global__ void balance_kernel(const int32_t *__restrict__ rc, int R, double *bal, int32_t *mx,
                                int64_t *total) {
   moe::pdl_wait();
@@ -220,4 +324,43 @@ extern "C" moe_status moe_balance_stats(const int32_t *rank_counts, int32_t R, d
   if (R < 1 || !rank_counts || !balancedness || !max_count || !total) return MOE_ERR_INVALID_ARG;
   return moe_host::launch_pdl(balance_kernel, dim3(1), dim3(256), 0, static_cast<cudaStream_t>(stream),
                               rank_counts, R, balancedness, max_count, total);
+}
+
+extern "C" moe_status moe_combine_merged(const uint16_t *y_perm, const int32_t *dest_row,
+                                         const float *topk_w, const int32_t *slot,
+                                         const moe_placement *pl, int64_t T, int32_t k, int32_t H,
+                                         const uint16_t *shared, uint16_t *y, int32_t *messages,
+                                         void *ws, size_t ws_bytes, void *stream) {
+  if (T < 0 || H < 1 || k < 1 || !pl || !messages) return MOE_ERR_INVALID_ARG;
+  if (H % 8 != 0 || k > 16) return MOE_ERR_UNSUPPORTED;
+  if (pl->n_slots < 1 || pl->n_ranks < 1 || pl->ranks_per_node < 1 || !pl->slot_rank)
+    return MOE_ERR_INVALID_ARG;
+  if (moe_status s = moe_host::check_ws(ws, ws_bytes, moe::kStatusBytes)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(messages, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (T == 0) return MOE_OK;
+  if (!y_perm || !dest_row || !topk_w || !slot || !y) return MOE_ERR_INVALID_ARG;
+  if (!moe_host::aligned16(y_perm) || !moe_host::aligned16(y) ||
+      (shared && !moe_host::aligned16(shared)))
+    return MOE_ERR_INVALID_ARG;
+  const uint4 *yp = reinterpret_cast<const uint4 *>(y_perm);
+  const uint4 *sh = reinterpret_cast<const uint4 *>(shared);
+  uint4 *yo = reinterpret_cast<uint4 *>(y);
+  const int64_t A = T * (int64_t)k;
+  int32_t *status = moe_host::status_ptr(ws);
+  const dim3 g(mover_grid(T)), b(kMoverThreads);
+  const int H8 = H / 8;
+  const int S = pl->n_slots, R = pl->n_ranks, rpn = pl->ranks_per_node;
+  const int32_t *sr = pl->slot_rank, *tsr = pl->token_src_rank;
+  if (k <= 2)
+    return moe_host::launch_pdl(combine_merged_kernel<2>, g, b, 0, st, yp, dest_row, topk_w, slot, sr,
+                                tsr, S, R, rpn, T, k, H8, sh, yo, A, messages, status);
+  if (k <= 4)
+    return moe_host::launch_pdl(combine_merged_kernel<4>, g, b, 0, st, yp, dest_row, topk_w, slot, sr,
+                                tsr, S, R, rpn, T, k, H8, sh, yo, A, messages, status);
+  if (k <= 8)
+    return moe_host::launch_pdl(combine_merged_kernel<8>, g, b, 0, st, yp, dest_row, topk_w, slot, sr,
+                                tsr, S, R, rpn, T, k, H8, sh, yo, A, messages, status);
+  return moe_host::launch_pdl(combine_merged_kernel<16>, g, b, 0, st, yp, dest_row, topk_w, slot, sr,
+                              tsr, S, R, rpn, T, k, H8, sh, yo, A, messages, status);
 }

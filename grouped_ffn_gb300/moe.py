@@ -79,6 +79,8 @@ _SIGNATURES = {
                                               _P, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "moe_pack_expert_weights": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "moe_combine_merged": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(PlacementC), _I64, _I32,
+                                          _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_balance_stats": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_version": (ctypes.c_char_p, []),
@@ -362,6 +364,23 @@ def moe_combine(y_perm, dest_row, topk_w, y, ws, shared=None, stream=None):
     _check("moe_combine", lib().moe_combine(_ptr(y_perm), _ptr(dest_row), _ptr(topk_w), T, k, H,
                                             _ptr(shared), _ptr(y), _ptr(ws), ws.numel(),
                                             _stream(stream)))
+
+
+def moe_combine_merged(y_perm, dest_row, topk_w, slot, placement: DevicePlacement, y, messages,
+                       ws, shared=None, stream=None):
+    """Combine with node-local pre-reduction; messages (device int32[2])
+    receives the inter-node dispatch messages before and after merge."""
+    _bf16(y_perm, "y_perm")
+    _bf16(y, "y")
+    if shared is not None:
+        _bf16(shared, "shared")
+    for n, t in (("dest_row", dest_row), ("slot", slot), ("messages", messages)):
+        _need(t, torch.int32, n)
+    _need(topk_w, torch.float32, "topk_w")
+    T, k = topk_w.shape
+    _check("moe_combine_merged", lib().moe_combine_merged(
+        _ptr(y_perm), _ptr(dest_row), _ptr(topk_w), _ptr(slot), ctypes.byref(placement.c), T, k,
+        y.shape[1], _ptr(shared), _ptr(y), _ptr(messages), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_balance_stats(rank_counts, balancedness, max_count, total, ws=None, stream=None):

@@ -333,6 +333,26 @@ moe_status moe_combine(const uint16_t *y_perm, const int32_t *dest_row, const fl
                        int64_t T, int32_t k, int32_t H, const uint16_t *shared, uint16_t *y,
                        void *ws, size_t ws_bytes, void *stream);
 
+/* Combine with node-local pre-reduction, the combine side of "Zepp"'s
+ * merge (Section 4.2, "Merge": the weighted expert outputs of one token on
+ * one node are accumulated there and only that partial sum returns;
+ * Algorithm 1's PreReduce and Reduce), simulated on one GPU.  Per token and
+ * element: for each destination node n of its k assignments, in ascending
+ * node order, part_n = bf16(fmaf chain over that node's assignments in j
+ * order, from 0) -- the bf16 payload that would cross the network; then
+ * acc = shared[t] (or 0), acc += part_n in node order, y = bf16(acc).
+ * Also counts the step's inter-node dispatch messages (Section 3.2,
+ * "Redundant Tokens"): messages[0] = assignments whose copy is on another
+ * node than their token, messages[1] = distinct (token, remote node) pairs,
+ * i.e. the transfers left after merge.
+ *  slot     device int32 [T*k]: each assignment's slot (moe_dispatch_layout).
+ *  messages device int32 [2] (output, cleared by the call).
+ *  Other arguments as moe_combine.  Limits: H % 8 == 0, k <= 16. */
+moe_status moe_combine_merged(const uint16_t *y_perm, const int32_t *dest_row, const float *topk_w,
+                              const int32_t *slot, const moe_placement *placement, int64_t T,
+                              int32_t k, int32_t H, const uint16_t *shared, uint16_t *y,
+                              int32_t *messages, void *ws, size_t ws_bytes, void *stream);
+
 /* Balancedness of one step: mean per-rank load over the busiest rank's
  * load, total / (R * max) in fp64; 1.0 when total is 0.  "14. Serving
  * Mixture-of-Experts Models", "The slowest expert sets the pace" (loads

@@ -515,3 +515,62 @@ def route_replicas_waterfill(topk_ids: np.ndarray, pl, c_num: int, c_den: int):
     node_of = lambda r: r // pl.ranks_per_node
     inter = int(sum(node_of(int(pl.slot_rank[slot[a]])) != node_of(int(src[a])) for a in range(A)))
     return slot, inter
+
+
+# ------------------------------------------------------------------ merge (simulated)
+def dispatch_messages(slot: np.ndarray, pl, T: int, k: int):
+    """Inter-node dispatch transfers of one step, before and after merge
+    ([Zepp] Section 3.2 "Redundant Tokens" and Section 4.2 "Merge": a token
+    whose experts share a remote node crosses the network once).  Returns
+    (remote assignments, unique (token, remote node) pairs)."""
+    before, pairs = 0, set()
+    for a in range(T * k):
+        t = a // k
+        src = int(pl.token_src_rank[t]) if pl.token_src_rank is not None else t % pl.n_ranks
+        dn = int(pl.slot_rank[int(slot[a])]) // pl.ranks_per_node
+        if dn != src // pl.ranks_per_node:
+            before += 1
+            pairs.add((t, dn))
+    return before, len(pairs)
+
+
+def combine_merged_fma32(y_perm_bits, dest_row, topk_w32, node, shared_bits=None):
+    """Combine with node-local pre-reduction; see oracle_combine_merged_fma32
+    in fma_combine.c for the order of operations.  bf16 bit patterns in and
+    out; node[a] is assignment a's destination node."""
+    T, k = topk_w32.shape
+    H = y_perm_bits.shape[1]
+    yp = np.ascontiguousarray(y_perm_bits, dtype=np.uint16)
+    dr = np.ascontiguousarray(dest_row, dtype=np.int32)
+    w = np.ascontiguousarray(topk_w32, dtype=np.float32)
+    nd = np.ascontiguousarray(node, dtype=np.int32)
+    sh = None if shared_bits is None else np.ascontiguousarray(shared_bits, dtype=np.uint16)
+    out = np.empty((T, H), dtype=np.uint16)
+    lib = _fma()
+    if not hasattr(lib, "_merged_ready"):
+        lib.oracle_combine_merged_fma32.restype = None
+        lib.oracle_combine_merged_fma32.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+        lib._merged_ready = True
+    lib.oracle_combine_merged_fma32(yp.ctypes.data, dr.ctypes.data, w.ctypes.data, nd.ctypes.data,
+                                    None if sh is None else sh.ctypes.data, T, k, H,
+                                    out.ctypes.data)
+    return out
+
+
+def combine_merged_f64(y_perm, dest_row, topk_w, node, shared=None):
+    """The same pre-reduction in fp64 with the bf16 rounding of each node's
+    partial sum kept (it is the transferred payload); bf16 result."""
+    T, k = topk_w.shape
+    out = np.zeros((T, y_perm.shape[1]))
+    for t in range(T):
+        acc = np.zeros(y_perm.shape[1]) if shared is None else shared[t].astype(np.float64)
+        for n in sorted(set(int(v) for v in node[t * k:(t + 1) * k])):
+            part = np.zeros(y_perm.shape[1])
+            for j in range(k):
+                if int(node[t * k + j]) == n:
+                    part = part + float(topk_w[t, j]) * y_perm[dest_row[t * k + j]]
+            acc = acc + bf16_round(part)
+        out[t] = bf16_round(acc)
+    return out

@@ -42,3 +42,44 @@ void oracle_combine_fma32(const uint16_t *y_perm, const int32_t *dest_row,
     }
   }
 }
+
+/* The combine with node-local pre-reduction ("Zepp", Section 4.2, "Merge":
+ * the weighted expert outputs of one token on one node are summed there
+ * and only that partial sum returns; Algorithm 1's PreReduce and Reduce).
+ * Per token and element: for each destination node n in ascending order,
+ * part_n = bf16(fmaf chain over its assignments j in ascending order,
+ * from 0); then acc = shared[t] (or 0), acc = acc + part_n over the nodes in
+ * ascending order, out = bf16(acc).  node[t*k + j] is assignment j's
+ * destination node. */
+void oracle_combine_merged_fma32(const uint16_t *y_perm, const int32_t *dest_row,
+                                 const float *topk_w, const int32_t *node,
+                                 const uint16_t *shared, int64_t T, int32_t k, int32_t H,
+                                 uint16_t *out) {
+  for (int64_t t = 0; t < T; ++t) {
+    const int32_t *nd = node + t * k;
+    for (int32_t h = 0; h < H; ++h) {
+      float acc = shared ? bf16_to_f32(shared[t * (int64_t)H + h]) : 0.0f;
+      int32_t prev = -2147483647 - 1;
+      for (;;) {
+        /* next node id above prev among this token's assignments */
+        int32_t n = 2147483647;
+        int found = 0;
+        for (int32_t j = 0; j < k; ++j)
+          if (nd[j] > prev && nd[j] <= n) {
+            n = nd[j];
+            found = 1;
+          }
+        if (!found) break;
+        float part = 0.0f;
+        for (int32_t j = 0; j < k; ++j) {
+          if (nd[j] != n) continue;
+          int64_t row = dest_row[t * k + j];
+          part = fmaf(topk_w[t * k + j], bf16_to_f32(y_perm[row * H + h]), part);
+        }
+        acc = acc + bf16_to_f32(f32_to_bf16(part));
+        prev = n;
+      }
+      out[t * (int64_t)H + h] = f32_to_bf16(acc);
+    }
+  }
+}

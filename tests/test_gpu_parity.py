@@ -637,3 +637,49 @@ def test_gather_ffn_ragged_segments_match_oracle():
                                 oracle.bf16_bits_to_f64(bits(wgu)), oracle.bf16_bits_to_f64(bits(wd)), I)
     assert_close(f64(h), rh, "h (gather)")
     assert_close(f64(y), ry, "y_perm (gather)")
+
+
+# ------------------------------------------------------------------ merge: node-local pre-reduction
+@pytest.mark.parametrize("name", ["decode", "group_limited", "replica"])
+def test_combine_merged_bit_exact_and_message_counts(name):
+    m = moe()
+    w = wl.WORKLOADS[name]
+    if name == "group_limited":
+        w = w.scaled(T=1024, H=1024)
+    pl = wl.make_placement(w)
+    pl_dev = m.DevicePlacement.from_tables(pl)
+    ids, wts = gpu_route(w, wl.make_logits(w, "cuda"))
+    lay = gpu_layout(ids, pl_dev, w.T, w.k)
+    g = torch.Generator(device="cuda").manual_seed(w.index)
+    yp = torch.randn(w.A, w.H, generator=g, device="cuda").to(torch.bfloat16)
+    sh = torch.randn(w.T, w.H, generator=g, device="cuda").to(torch.bfloat16) if w.shared_I else None
+    y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    msgs = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    ws = m.new_workspace(w.T, w.k, pl.n_slots)
+    dr = torch.from_numpy(lay["dest_row"]).cuda()
+    slot = torch.from_numpy(lay["slot"]).cuda()
+    m.moe_combine_merged(yp, dr, wts, slot, pl_dev, y, msgs, ws, sh)
+    m.moe_check_device_status(ws)
+    node = pl.slot_rank[lay["slot"]] // pl.ranks_per_node
+    ref = oracle.combine_merged_fma32(bits(yp), lay["dest_row"], wts.cpu().numpy(), node,
+                                      None if sh is None else bits(sh))
+    assert np.array_equal(bits(y), ref)
+    assert tuple(msgs.tolist()) == oracle.dispatch_messages(lay["slot"], pl, w.T, w.k)
+
+
+def test_combine_merged_figure4_counts():
+    m = moe()
+    pl = wl.placement_from_hosts(3, 2, 1, [[1], [1], [0]], token_src_rank=np.array([0]))
+    pl_dev = m.DevicePlacement.from_tables(pl)
+    ids = torch.tensor([[0, 1, 2]], dtype=torch.int32, device="cuda")
+    lay = gpu_layout(ids, pl_dev, 1, 3)
+    yp = torch.ones(3, 8, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(1, 8, dtype=torch.bfloat16, device="cuda")
+    msgs = torch.zeros(2, dtype=torch.int32, device="cuda")
+    ws = m.new_workspace(1, 3, pl.n_slots)
+    m.moe_combine_merged(yp, torch.from_numpy(lay["dest_row"]).cuda(),
+                         torch.full((1, 3), 0.25, device="cuda"),
+                         torch.from_numpy(lay["slot"]).cuda(), pl_dev, y, msgs, ws)
+    m.moe_check_device_status(ws)
+    assert msgs.tolist() == [2, 1]
+    assert torch.equal(y.float(), torch.full((1, 8), 0.75, device="cuda"))
