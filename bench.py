@@ -223,14 +223,26 @@ def run_ours(args, world, rank, local):
     K, W = args.steps, args.warmup
     ET = lambda: torch.cuda.Event(enable_timing=True)
 
+    graph = None
+
     def step(marks=None):
-        layer.forward(logits, x, y, stream, mark=marks)
+        if graph is not None and marks is None:
+            graph.replay()
+        else:
+            layer.forward(logits, x, y, stream, mark=marks)
 
     with torch.cuda.stream(stream):
         for _ in range(W):
             step()
     stream.synchronize()
     layer.check(stream)
+    if args.graph:
+        # the whole step as one CUDA graph; replays run on `stream`
+        with torch.cuda.stream(stream):
+            graph = layer.capture(logits, x, y)
+            for _ in range(W):
+                graph.replay()
+        stream.synchronize()
 
     # Timed region: K whole steps.  The only events inside it bracket the
     # grouped-FFN launches (their duration feeds the roofline); the other
@@ -257,7 +269,7 @@ def run_ours(args, world, rank, local):
         start.record(stream)
         with torch.cuda.stream(stream):
             for i in range(K):
-                step(timed_marks(i))
+                step(None if graph is not None else timed_marks(i))
         end.record(stream)
         stream.synchronize()
     torch.cuda.synchronize()
@@ -266,8 +278,9 @@ def run_ours(args, world, rank, local):
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
     layer.check(stream)
-    ffn_ms = {n: float(np.mean([ffn_ev[i][2 * j].elapsed_time(ffn_ev[i][2 * j + 1])
-                                for i in range(K)])) for j, n in enumerate(ffn_stages)}
+    ffn_ms = {} if graph is not None else {
+        n: float(np.mean([ffn_ev[i][2 * j].elapsed_time(ffn_ev[i][2 * j + 1]) for i in range(K)]))
+        for j, n in enumerate(ffn_stages)}
 
     # Stage breakdown (not the headline): a separate pass with an event
     # after every stage; events between kernels also break their overlap.
@@ -363,6 +376,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas{world}",
                    "weight_layout": "plain" if args.unpacked else "packed",
                    "dispatch": "gather-fused" if args.gather else "permute",
+                   "launch": "cuda-graph replay" if args.graph else "stream (PDL)",
                    "l2": "inputs larger than L2: %.2f GB of expert weights stream per step"
                          % (g["weight_bytes"] / 1e9)},
         "e2e": e2e,
@@ -618,6 +632,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the step as CUDA-graph replays (FFN roofline from the breakdown pass)")
     ap.add_argument("--gather", action="store_true",
                     help="FFN reads rows from x through the inverse permutation (no permute)")
     ap.add_argument("--replica-relax", default="",

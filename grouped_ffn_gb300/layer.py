@@ -150,6 +150,23 @@ class MoELayer:
         mark("balance")
         return y
 
+    def capture(self, logits: torch.Tensor, x: torch.Tensor, y: torch.Tensor):
+        """Record one whole step (every kernel of forward) as a CUDA graph
+        over these fixed buffers and return it; graph.replay() then reruns
+        the step on whatever the buffers hold, with one launch from the
+        host.  Segment sizes never reach the host, so the dynamic
+        contiguous layout needs no padding to be replayable.  Call forward
+        once first (per-device set-up happens on the first call)."""
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        stream = torch.cuda.Stream(device=y.device)
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                self.forward(logits, x, y, torch.cuda.current_stream())
+        torch.cuda.current_stream().wait_stream(stream)
+        return graph
+
     def forward_host(self, logits_host: torch.Tensor, x_host: torch.Tensor,
                      y_host: torch.Tensor, logits_dev: torch.Tensor, x_dev: torch.Tensor,
                      y_dev: torch.Tensor, stream=None):

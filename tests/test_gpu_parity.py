@@ -683,3 +683,42 @@ def test_combine_merged_figure4_counts():
     m.moe_check_device_status(ws)
     assert msgs.tolist() == [2, 1]
     assert torch.equal(y.float(), torch.full((1, 8), 0.75, device="cuda"))
+
+
+# ------------------------------------------------------------------ whole step as a CUDA graph
+@pytest.mark.parametrize("name", ["decode", "group_limited", "replica"])
+def test_graph_replay_matches_eager(name):
+    """The step records into one CUDA graph (cooperative FFN, programmatic
+    dependent launches, memsets) and its replays reproduce the eager step
+    bit for bit, including after the inputs change in place."""
+    from grouped_ffn_gb300 import MoELayer
+    m = moe()
+    w = wl.WORKLOADS[name]
+    if name == "group_limited":
+        w = w.scaled(T=512, E=64, R=16, H=1024, I=256, shared_I=256)
+    pl = wl.make_placement(w)
+    logits, x = wl.make_logits(w, "cuda"), wl.make_x(w, "cuda")
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    sgu, sd = wl.make_shared_weights(w, "cuda")
+    layer = MoELayer(H=w.H, I=w.I, E=w.E, k=w.k, placement=m.DevicePlacement.from_tables(pl),
+                     w_gate_up=wgu, w_down=wd, max_tokens=w.T, score_fn=w.score_fn,
+                     n_groups=w.n_groups, topk_groups=w.topk_groups, group_topn=w.group_topn,
+                     shared_w_gate_up=sgu, shared_w_down=sd)
+    y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    layer.forward(logits, x, y)
+    eager = y.clone()
+    graph = layer.capture(logits, x, y)
+    y.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    layer.check()
+    assert torch.equal(y, eager)
+    # new inputs in the same buffers: replay equals a fresh eager step
+    g = torch.Generator(device="cuda").manual_seed(99)
+    logits.copy_(torch.randn(logits.shape, generator=g, device="cuda"))
+    x.copy_(torch.randn(x.shape, generator=g, device="cuda").to(torch.bfloat16))
+    graph.replay()
+    y_graph = y.clone()
+    layer.forward(logits, x, y)
+    torch.cuda.synchronize()
+    assert torch.equal(y_graph, y)
