@@ -213,16 +213,179 @@ def dispatch_layout_from_slots(topk_ids: np.ndarray, slot: np.ndarray, pl) -> Di
                 dest_row=dest_row, src_assign=src_assign, rank_counts=rank_counts)
 
 
+def dispatch_layout_masked(topk_ids: np.ndarray, pl, cap: int,
+                           slot: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """Fixed-capacity ("masked") layout: every slot owns `cap` rows whatever
+    its load, so the buffers and launches have the same shape every step
+    ([MoEInf] "Communication pressure", prefill and decode kernel layouts:
+    decode pads tokens into fixed-size masked layouts so that one captured
+    CUDA graph can be replayed; [MoE14] "Capacity, padding, and the drop
+    decision": a fixed per-expert capacity, and assignments beyond it are
+    dropped, their output for the layer being zero).
+
+    Slot s owns rows [s*cap, (s+1)*cap).  Walking the assignments in order,
+    the first `cap` of slot s take rows s*cap, s*cap+1, ...; later ones are
+    dropped (dest_row -1).  Returns slot, seg_counts (the demand, before
+    dropping), masked_m (rows used: min(demand, cap)), dest_row,
+    src_assign [S*cap] (-1 on unused rows), rank_counts (rows each rank
+    executes: the sum of its slots' masked_m) and n_dropped."""
+    T, k = topk_ids.shape
+    S = pl.n_slots
+    A = T * k
+    if slot is None:
+        slot = np.array([choose_slot(int(topk_ids[a // k, a % k]), a // k, pl) for a in range(A)],
+                        dtype=np.int32)
+    slot = np.asarray(slot, dtype=np.int32)
+    seg_counts = np.zeros(S, dtype=np.int32)
+    dest_row = np.full(A, -1, dtype=np.int32)
+    src_assign = np.full(S * cap, -1, dtype=np.int32)
+    for a in range(A):
+        s = int(slot[a])
+        pos = int(seg_counts[s])
+        seg_counts[s] += 1
+        if pos < cap:
+            dest_row[a] = s * cap + pos
+            src_assign[s * cap + pos] = a
+    masked_m = np.minimum(seg_counts, cap).astype(np.int32)
+    rank_counts = np.zeros(pl.n_ranks, dtype=np.int32)
+    for s in range(S):
+        rank_counts[int(pl.slot_rank[s])] += masked_m[s]
+    n_dropped = int(seg_counts.sum() - masked_m.sum())
+    return dict(slot=slot, seg_counts=seg_counts, masked_m=masked_m, dest_row=dest_row,
+                src_assign=src_assign, rank_counts=rank_counts, n_dropped=n_dropped)
+
+
+def grouped_ffn_masked(x_perm: np.ndarray, cap: int, masked_m: np.ndarray,
+                       seg_expert: np.ndarray, w_gate_up, w_down, I: int):
+    """The grouped FFN on a fixed-capacity layout: slot s runs expert
+    seg_expert[s] on its rows [s*cap, s*cap + masked_m[s]); other rows are
+    padding and come back as zero here.  Same per-row definition as
+    grouped_ffn."""
+    S = len(masked_m)
+    H = x_perm.shape[1]
+    h_out = np.zeros((S * cap, I))
+    y_out = np.zeros((S * cap, H))
+    for s in range(S):
+        m = int(masked_m[s])
+        if m == 0:
+            continue
+        r0 = s * cap
+        e = int(seg_expert[s])
+        h, y = swiglu_expert(x_perm[r0:r0 + m], np.asarray(w_gate_up[e], np.float64),
+                             np.asarray(w_down[e], np.float64), I)
+        h_out[r0:r0 + m] = h
+        y_out[r0:r0 + m] = y
+    return h_out, y_out
+
+
 # ------------------------------------------------------------------ permute
-def permute(x: np.ndarray, dest_row: np.ndarray, k: int) -> np.ndarray:
+def permute(x: np.ndarray, dest_row: np.ndarray, k: int,
+            n_rows: Optional[int] = None) -> np.ndarray:
     """x_perm[dest_row[t*k+j]] = x[t] ([MoE14] "Price one dispatch": every
     assignment carries one copy of its token's hidden row).  Works on any
-    dtype, so bf16 bit patterns are moved unchanged."""
+    dtype, so bf16 bit patterns are moved unchanged.  n_rows: rows of the
+    output (default T*k); an assignment with dest_row -1 was dropped by a
+    fixed-capacity layout and moves nothing.  Rows no assignment lands on
+    are zero here (the GPU leaves them unwritten)."""
     T = x.shape[0]
-    out = np.empty((T * k,) + x.shape[1:], dtype=x.dtype)
+    out = np.zeros((T * k if n_rows is None else n_rows,) + x.shape[1:], dtype=x.dtype)
     for a in range(T * k):
-        out[dest_row[a]] = x[a // k]
+        if dest_row[a] >= 0:
+            out[dest_row[a]] = x[a // k]
     return out
+
+
+# ------------------------------------------------------------------ FP8 dispatch
+# [MoEInf] "Communication pressure": token activations can be quantized, for
+# example to FP8, before dispatch, to shrink what the all-to-all moves.
+# Readings: OCP FP8 E4M3 ("e4m3fn": 1 sign, 4 exponent bits with bias 7, 3
+# mantissa bits, no infinities, S.1111.111 is NaN, largest finite 448);
+# one scale per (token, 128 consecutive channels); the scale is the power of
+# two 2^e with the smallest e such that the block's largest magnitude is at
+# most 448 * 2^e (so x / 2^e is exact and only the rounding to E4M3 loses
+# information), e clamped to [-126, 127], and e = 0 for an all-zero block;
+# codes are x / 2^e rounded to the nearest E4M3 value, ties to the even
+# code.  The receiver restores bf16(code_value * 2^e).
+FP8_BLOCK = 128
+E4M3_MAX = 448.0
+
+
+def e4m3_value(code) -> np.ndarray:
+    """E4M3 codes (uint8) -> fp64 values, from the bit fields: exponent
+    field 0 is subnormal (m/8 * 2^-6), otherwise (1 + m/8) * 2^(E-7); the
+    two NaN codes map to nan."""
+    c = np.asarray(code, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    E = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(E == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(E.astype(np.float64) - 7))
+    out = sign * mag
+    return np.where((c & 0x7F) == 0x7F, np.nan, out)
+
+
+_E4M3_POS = e4m3_value(np.arange(0x7F))   # the 127 finite non-negative values, ascending
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """fp64 values with |v| <= 448 -> the E4M3 code of the nearest value,
+    ties to the even code (the one whose lowest mantissa bit is 0).  Found
+    by search in the table of all finite values, so no bit trick is
+    involved.  The sign bit is kept for zero results (-0 -> 0x80)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    if np.any(a > E4M3_MAX) or np.any(np.isnan(v)):
+        raise ValueError("e4m3_encode: value outside [-448, 448]")
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 0x7E)
+    lo = np.clip(hi - 1, 0, 0x7E)
+    d_lo = a - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(v), code | 0x80, code).astype(np.uint8)
+
+
+def fp8_block_exponent(amax: float) -> int:
+    """Smallest integer e with amax <= 448 * 2^e, clamped to [-126, 127];
+    0 when amax is 0.  Exact: candidates are checked with exact power-of-two
+    scaling (ldexp) in fp64."""
+    amax = float(amax)
+    if amax == 0.0:
+        return 0
+    e = int(np.ceil(np.log2(amax / E4M3_MAX)))
+    while amax > np.ldexp(E4M3_MAX, e):
+        e += 1
+    while amax <= np.ldexp(E4M3_MAX, e - 1):
+        e -= 1
+    return int(min(max(e, -126), 127))
+
+
+def quantize_fp8_blocks(x_bits: np.ndarray):
+    """bf16 rows (uint16 [T, H], H a multiple of 128) -> (codes uint8 [T, H],
+    scales fp32 [T, H/128] holding 2^e).  Per block: e from the largest
+    magnitude, codes = e4m3_encode(x / 2^e)."""
+    x = bf16_bits_to_f64(x_bits)
+    T, H = x.shape
+    nb = H // FP8_BLOCK
+    codes = np.empty((T, H), dtype=np.uint8)
+    scales = np.empty((T, nb), dtype=np.float32)
+    for t in range(T):
+        for b in range(nb):
+            blk = x[t, b * FP8_BLOCK:(b + 1) * FP8_BLOCK]
+            e = fp8_block_exponent(np.max(np.abs(blk)))
+            codes[t, b * FP8_BLOCK:(b + 1) * FP8_BLOCK] = e4m3_encode(np.ldexp(blk, -e))
+            scales[t, b] = np.float32(np.ldexp(1.0, e))
+    return codes, scales
+
+
+def dequantize_fp8_blocks(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """(codes [n, H], scales [n, H/128]) -> bf16 bit patterns [n, H] of
+    bf16(code_value * scale), rounded to nearest, ties to even."""
+    vals = e4m3_value(codes) * np.repeat(np.asarray(scales, np.float64), FP8_BLOCK, axis=1)
+    # below 2^-126 bf16 is subnormal: a fixed step of 2^-133, ties to even
+    tiny = np.abs(vals) < 2.0 ** -126
+    rounded = np.where(tiny, np.ldexp(np.rint(np.ldexp(vals, 133)), -133),
+                       bf16_round(np.where(tiny, 1.0, vals)))
+    return f64_to_bf16_bits(rounded)
 
 
 # ------------------------------------------------------------------ expert FFN
@@ -281,13 +444,18 @@ def combine_f64(y_perm: np.ndarray, dest_row: np.ndarray, topk_w: np.ndarray,
     "Follow one token", step 4; [Zepp] Section 2: outputs aggregated at each
     token's source), plus the shared expert's output with weight one
     ([MoEInf] "MoE architecture recap": shared experts see every token).
-    fp64 accumulation, bf16 result.  tokens: optional subset."""
+    fp64 accumulation, bf16 result.  tokens: optional subset.  An
+    assignment dropped by a fixed-capacity layout (dest_row -1) adds
+    nothing ([MoE14] "Capacity, padding, and the drop decision": a dropped
+    token's output for the layer is zero)."""
     T, k = topk_w.shape
     ts = np.arange(T) if tokens is None else np.asarray(tokens)
     out = np.zeros((len(ts), y_perm.shape[1]))
     for i, t in enumerate(ts):
         acc = np.zeros(y_perm.shape[1]) if shared is None else shared[t].astype(np.float64)
         for j in range(k):
+            if dest_row[t * k + j] < 0:      # dropped: its output is zero
+                continue
             acc = acc + float(topk_w[t, j]) * y_perm[dest_row[t * k + j]]
         out[i] = bf16_round(acc)
     return out
@@ -324,7 +492,8 @@ def combine_fma32(y_perm_bits: np.ndarray, dest_row: np.ndarray, topk_w32: np.nd
     acc = shared (or 0); for j = 0..k-1: acc = fmaf(w[t,j], y, acc); result
     bf16 (nearest, ties to even).  Inputs/outputs are bf16 bit patterns
     (uint16).  This fixes one valid rounding order so that a stage fed the
-    same y_perm can be compared bit for bit."""
+    same y_perm can be compared bit for bit.  Terms with dest_row -1
+    (dropped assignments) are skipped."""
     T, k = topk_w32.shape
     H = y_perm_bits.shape[1]
     yp = np.ascontiguousarray(y_perm_bits, dtype=np.uint16)

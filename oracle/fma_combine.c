@@ -6,8 +6,11 @@
  * and are summed with the router weights.  Per output element:
  *     acc = shared[t] (or 0);  for j = 0..k-1: acc = fmaf(w[t,j], y_j, acc);
  *     out = bf16(acc)  (round to nearest, ties to even)
- * where y_j is row dest_row[t*k+j] of the expert outputs.  bf16 values are
- * passed as their 16-bit patterns.  Shares no code with the CUDA library. */
+ * where y_j is row dest_row[t*k+j] of the expert outputs; a term whose
+ * dest_row is -1 (an assignment dropped by a fixed-capacity layout, whose
+ * output is zero: same chapter, "Capacity, padding, and the drop
+ * decision") is skipped.  bf16 values are passed as their 16-bit patterns.
+ * Shares no code with the CUDA library. */
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -36,6 +39,7 @@ void oracle_combine_fma32(const uint16_t *y_perm, const int32_t *dest_row,
       float acc = shared ? bf16_to_f32(shared[t * (int64_t)H + h]) : 0.0f;
       for (int32_t j = 0; j < k; ++j) {
         int64_t row = dest_row[t * k + j];
+        if (row < 0) continue; /* dropped by a fixed-capacity layout: adds nothing */
         acc = fmaf(topk_w[t * k + j], bf16_to_f32(y_perm[row * H + h]), acc);
       }
       out[t * (int64_t)H + h] = f32_to_bf16(acc);
