@@ -65,6 +65,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
+def mode_name(args) -> str:
+    """Non-default step variants; the committed traffic capture covers the
+    default one only."""
+    parts = [n for n, on in (("gather", args.gather), ("unpacked", args.unpacked),
+                             ("masked", bool(args.masked_cap)), ("fp8", args.fp8_dispatch),
+                             ("relax", bool(args.replica_relax))) if on]
+    return "+".join(parts)
+
+
 def measured_traffic(workload: str):
     """DRAM bytes (read + write) per grouped-FFN launch from the committed ncu
     capture, or None if there is none for this workload or the kernel source
@@ -172,24 +181,31 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ algorithmic work
 def algorithmic(w: wl.Workload, seg_counts: np.ndarray, slot_expert: np.ndarray,
-                gather: bool = False):
+                gather: bool = False, kept: int = None, fp8: bool = False):
     """Bytes / flops per step by stage (the per-unit figures times the units).
     With the gather-fused FFN the rows come from x (2H bytes per token)
-    instead of the permuted copy (2H per assignment)."""
+    instead of the permuted copy (2H per assignment).  kept: assignments
+    that run (fewer than T*k when a fixed capacity drops some).  fp8: the
+    dispatched rows carry H E4M3 bytes plus one fp32 scale per 128
+    channels, restored to bf16 by a separate pass."""
     A, T, H, I = w.A, w.T, w.H, w.I
+    K = A if kept is None else kept
     active_slots = seg_counts > 0
     # weights are read once per active expert slot (replicas re-read: they
     # are separate copies in a real deployment)
     n_active = int(active_slots.sum())
     wbytes = n_active * 6 * H * I
+    wire = H + 4 * (H // 128) if fp8 else 2 * H
     st = {
         "route": dict(bytes=T * w.E * 4 + T * w.k * 8),
         "layout": dict(bytes=A * 4 * 4 + A * 4),
-        "permute": dict(bytes=T * H * 2 + A * H * 2),
-        "grouped_ffn": dict(bytes=wbytes + (T if gather else A) * H * 2 + A * I * 2 * 2 + A * H * 2,
-                            flops=6 * A * H * I, weight_bytes=wbytes),
-        "combine": dict(bytes=A * H * 2 + T * H * 2 + (T * H * 2 if w.shared_I else 0) + A * 8),
+        "permute": dict(bytes=T * H * 2 + K * wire),
+        "grouped_ffn": dict(bytes=wbytes + (T if gather else K) * H * 2 + K * I * 2 * 2 + K * H * 2,
+                            flops=6 * K * H * I, weight_bytes=wbytes),
+        "combine": dict(bytes=K * H * 2 + T * H * 2 + (T * H * 2 if w.shared_I else 0) + A * 8),
     }
+    if fp8:
+        st["dequant"] = dict(bytes=K * wire + K * H * 2)
     if w.shared_I:
         st["shared_ffn"] = dict(bytes=6 * H * w.shared_I + T * H * 2 * 2 + T * w.shared_I * 4,
                                 flops=6 * T * H * w.shared_I, weight_bytes=6 * H * w.shared_I)
@@ -213,12 +229,14 @@ def run_ours(args, world, rank, local):
                      n_groups=w.n_groups, topk_groups=w.topk_groups, group_topn=w.group_topn,
                      shared_w_gate_up=sgu, shared_w_down=sd, device=dev,
                      packed=not args.unpacked, replica_relax=parse_relax(args.replica_relax),
-                     gather=args.gather)
+                     gather=args.gather, masked_cap=args.masked_cap or None,
+                     fp8_dispatch=args.fp8_dispatch)
     y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    names = ["route", "layout", "permute", "grouped_ffn"] + (["shared_ffn"] if w.shared_I else []) \
-        + ["combine", "balance"]
+    names = ["route", "layout", "permute"] + (["dequant"] if args.fp8_dispatch else []) + \
+        ["grouped_ffn"] + (["shared_ffn"] if w.shared_I else []) + ["combine", "balance"]
+    ffn_start = "dequant" if args.fp8_dispatch else "permute"
     ffn_stages = ["grouped_ffn"] + (["shared_ffn"] if w.shared_I else [])
     K, W = args.steps, args.warmup
     ET = lambda: torch.cuda.Event(enable_timing=True)
@@ -251,7 +269,7 @@ def run_ours(args, world, rank, local):
 
     def timed_marks(i):
         evs = ffn_ev[i]
-        slot = {"permute": 0, "grouped_ffn": 1}
+        slot = {ffn_start: 0, "grouped_ffn": 1}
         if w.shared_I:
             slot.update({"grouped_ffn": 1, "shared_ffn": 3})
         def mark(name):
@@ -297,7 +315,30 @@ def run_ours(args, world, rank, local):
     stage_ms.update(ffn_ms)   # the FFN figures come from the timed region
 
     # Merge (simulated): inter-node dispatch messages before / after merge
-    # and the pre-reducing combine timed like the plain one (not in the step)
+    # and the pre-reducing combine timed like the plain one (not in the step;
+    # contiguous layout only)
+    merge = None if args.masked_cap else run_merge(layer, w, y, stream, K)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(layer, logits, x, y, stream, world, K, W)
+        e2e["value"] = world * w.T / (e2e["ms_per_step"] * 1e-3)
+        e2e["h2d_bytes_per_step"] = logits.numel() * 4 + x.numel() * 2
+        e2e["d2h_bytes_per_step"] = y.numel() * 2
+
+    peaks = load_peaks()
+    seg_counts = layer.seg_counts.cpu().numpy()
+    dropped = int(layer.n_dropped.item()) if args.masked_cap else 0
+    alg = algorithmic(w, seg_counts, pl.slot_expert, args.gather, kept=w.A - dropped,
+                      fp8=args.fp8_dispatch)
+    return finish(args, w, pl, layer, logits, x, wgu, wd, sgu, sd, names, stage_ms, ms_step,
+                  world, rank, K, W, alg, peaks, merge, e2e, dropped, clocks, dev)
+
+
+def run_merge(layer, w, y, stream, K):
+    from grouped_ffn_gb300 import moe
+    ET = lambda: torch.cuda.Event(enable_timing=True)
+    dev = y.device
     msgs = torch.zeros(2, dtype=torch.int32, device=dev)
     y_m = torch.empty_like(y)
     shared_arg = layer.shared_y[:w.T] if w.shared_I else None
@@ -312,21 +353,15 @@ def run_ours(args, world, rank, local):
         mev[1].record(stream)
     stream.synchronize()
     layer.check(stream)
-    merge = {"inter_node_assignments": int(msgs[0].item()),
-             "inter_node_messages_after_merge": int(msgs[1].item()),
-             "bytes_saved_per_step": (int(msgs[0].item()) - int(msgs[1].item())) * w.H * 2 * 2,
-             "combine_merged_us": mev[0].elapsed_time(mev[1]) / K * 1e3}
+    return {"inter_node_assignments": int(msgs[0].item()),
+            "inter_node_messages_after_merge": int(msgs[1].item()),
+            "bytes_saved_per_step": (int(msgs[0].item()) - int(msgs[1].item())) * w.H * 2 * 2,
+            "combine_merged_us": mev[0].elapsed_time(mev[1]) / K * 1e3}
 
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(layer, logits, x, y, stream, world, K, W)
-        e2e["value"] = world * w.T / (e2e["ms_per_step"] * 1e-3)
-        e2e["h2d_bytes_per_step"] = logits.numel() * 4 + x.numel() * 2
-        e2e["d2h_bytes_per_step"] = y.numel() * 2
 
-    peaks = load_peaks()
-    seg_counts = layer.seg_counts.cpu().numpy()
-    alg = algorithmic(w, seg_counts, pl.slot_expert, args.gather)
+def finish(args, w, pl, layer, logits, x, wgu, wd, sgu, sd, names, stage_ms, ms_step, world,
+           rank, K, W, alg, peaks, merge, e2e, dropped, clocks, dev):
+    """Stage table, roofline and the JSON record of our arm."""
     stages = {}
     for n in names:
         if n == "balance":
@@ -357,7 +392,7 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "tensor", "achieved": g["flops"] / (g_ms * 1e-3) / 1e12,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(w.name)
+    roof["traffic"] = measured_traffic(w.name) if mode_name(args) == "" else None
     roof["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, " +
                               os.path.relpath(TRAFFIC_FILE, ROOT)) if roof["traffic"] else None
     roof["kernel"] = "grouped_ffn_kernel (gate/up + down launches)"
@@ -375,7 +410,11 @@ def run_ours(args, world, rank, local):
                    "simulated_ranks": w.R, "zipf_s": w.zipf_s, "assignments": w.A,
                    "parallelism": f"replicas{world}",
                    "weight_layout": "plain" if args.unpacked else "packed",
-                   "dispatch": "gather-fused" if args.gather else "permute",
+                   "dispatch": "gather-fused" if args.gather else
+                               ("fp8-e4m3 permute + dequant (128-channel power-of-two scales)"
+                                if args.fp8_dispatch else "permute"),
+                   "layout": ("fixed capacity %d rows per slot" % args.masked_cap)
+                             if args.masked_cap else "contiguous",
                    "launch": "cuda-graph replay" if args.graph else "stream (PDL)",
                    "l2": "inputs larger than L2: %.2f GB of expert weights stream per step"
                          % (g["weight_bytes"] / 1e9)},
@@ -387,6 +426,7 @@ def run_ours(args, world, rank, local):
         "permute_pct_hbm": None if args.gather else 100.0 * stages["permute"]["hbm_frac"],
         "combine_pct_hbm": 100.0 * stages["combine"]["hbm_frac"],
         "balancedness": float(layer.balancedness.item()),
+        "dropped_assignments": dropped,
         "merge": merge,
         "clocks": clocks.summary(),
     }
@@ -640,6 +680,10 @@ def main():
                     help="choose replicas by water-filling with load bounds C, e.g. 1/10")
     ap.add_argument("--unpacked", action="store_true",
                     help="stream the expert weights in their plain [E,2I,H]/[E,H,I] layout")
+    ap.add_argument("--masked-cap", type=int, default=0,
+                    help="fixed-capacity layout with this many rows per slot (0: contiguous)")
+    ap.add_argument("--fp8-dispatch", action="store_true",
+                    help="dispatch E4M3 codes + block scales, restore bf16 before the FFN")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count")
     args = ap.parse_args()

@@ -71,7 +71,7 @@ struct __align__(8) Bars {
 constexpr size_t kBarsOff = (size_t)kStages * kStageBytes;
 constexpr size_t kMiscOff = kBarsOff + sizeof(Bars);
 constexpr size_t kSegOff = kMiscOff + 16;
-constexpr size_t kGidxOff = kSegOff + (size_t)(4 * kMaxSegs + 3) * 4;  // [kBM] gathered token rows
+constexpr size_t kGidxOff = kSegOff + (size_t)(5 * kMaxSegs + 3) * 4;  // [kBM] gathered token rows
 constexpr size_t kSmemBytes = kGidxOff + kBM * 4 + 1024;
 
 // One GEMM phase: gate/up with the SwiGLU epilogue (mode 0) or down (mode 1).
@@ -98,6 +98,10 @@ struct FfnParams {
   // (token rows, gather_T of them) instead of a permuted copy.
   const int32_t *gather_src;
   int32_t gather_k, gather_T;
+  // Fixed-capacity layout: segment s is rows [s*cap, s*cap + masked_m[s])
+  // (seg_offsets unused) when masked_m is set.
+  const int32_t *masked_m;
+  int32_t cap;
   int32_t *status;
   Phase ph[2];
 };
@@ -368,10 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + kMiscOff + 4);
   // the epilogue's shared go/stop decision, one per accumulator buffer
   volatile int32_t *epi_ok = reinterpret_cast<int32_t *>(smem + kMiscOff + 8);
-  int32_t *seg_off = reinterpret_cast<int32_t *>(smem + kSegOff);  // [S+1]
+  int32_t *seg_off = reinterpret_cast<int32_t *>(smem + kSegOff);  // [S] first row of s
   int32_t *pre_h = seg_off + (kMaxSegs + 1);  // [S+1] m-tiles before s, multi-tile segments
   int32_t *pre_c = pre_h + (kMaxSegs + 1);    // [S+1] m-tiles before s, one-tile segments
   int32_t *seg_exp = pre_c + (kMaxSegs + 1);  // [S]
+  int32_t *seg_end = seg_exp + kMaxSegs;      // [S] one past the last row of s (<= n_rows)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t kid = p.ph[0].mode == 0 ? moe::K_FFN_GATE_UP : moe::K_FFN_DOWN;
@@ -393,13 +398,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  for (int s = threadIdx.x; s <= p.S; s += kThreads) seg_off[s] = p.seg_offsets[s];
-  for (int s = threadIdx.x; s < p.S; s += kThreads) seg_exp[s] = p.seg_expert[s];
-  __syncthreads();
   for (int s = threadIdx.x; s < p.S; s += kThreads) {
-    const int lo = seg_off[s];
-    const int hi = min(seg_off[s + 1], p.n_rows);
-    const int e = seg_exp[s];
+    int lo, hi;
+    if (p.masked_m != nullptr) {
+      int m = p.masked_m[s];
+      if (m < 0 || m > p.cap) {
+        moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, s, kid);
+        m = m < 0 ? 0 : p.cap;
+      }
+      lo = s * p.cap;
+      hi = lo + m;
+    } else {
+      lo = p.seg_offsets[s];
+      hi = p.seg_offsets[s + 1];
+    }
+    hi = min(hi, p.n_rows);
+    const int e = p.seg_expert[s];
+    seg_off[s] = lo;
+    seg_end[s] = hi;
+    seg_exp[s] = e;
     int mt = (hi > lo && lo >= 0) ? (hi - lo + kBM - 1) / kBM : 0;
     if (mt > 0 && (e < 0 || e >= p.E)) {
       moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, s, kid);
@@ -443,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool gather = p.gather_src != nullptr && ti.ph == 0;
       if (gather) {  // token row of each of the tile's 128 rows (row 0 past the end)
         const int row0 = seg_off[ti.s] + ti.m_blk * kBM;
-        const int row_end = min(seg_off[ti.s + 1], p.n_rows);
+        const int row_end = seg_end[ti.s];
         for (int j = lane; j < kBM; j += 32) {
           int tok = 0;
           if (row0 + j < row_end) {
@@ -572,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo ti = decode(t, T0, pre_h, pre_c, p.S, NB0, NB1, Mh, Mc);
       const Phase &P = p.ph[ti.ph];
       const int row = seg_off[ti.s] + ti.m_blk * kBM + r_in;
-      const bool valid = row < min(seg_off[ti.s + 1], p.n_rows);
+      const bool valid = row < seg_end[ti.s];
       // One thread waits for the accumulator; all 128 then act on its verdict,
       // so the named barriers below are always reached by every epilogue warp.
       if (warp == 2 && lane == 0)
@@ -765,9 +782,9 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
                    const uint16_t *w_down, int32_t H, int32_t I, uint16_t *h, uint16_t *y_perm,
                    void *ws, size_t ws_bytes, void *stream, bool packed,
                    const int32_t *gather_src = nullptr, int32_t gather_k = 1,
-                   int64_t gather_T = 0) {
-  if (moe_status s = check_ffn_args(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up,
-                                    w_down, H, I, h, y_perm, ws, ws_bytes))
+                   int64_t gather_T = 0, const int32_t *masked_m = nullptr, int32_t cap = 0) {
+  if (moe_status s = check_ffn_args(x_perm, n_rows, masked_m ? masked_m : seg_offsets, seg_expert,
+                                    S, E, w_gate_up, w_down, H, I, h, y_perm, ws, ws_bytes))
     return s;
   if (n_rows == 0) return MOE_OK;
   if (!ensure_smem_attr()) return MOE_ERR_CUDA;
@@ -804,6 +821,8 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   p.gather_src = gather_src;
   p.gather_k = gather_k;
   p.gather_T = (int32_t)gather_T;
+  p.masked_m = masked_m;
+  p.cap = cap;
   Phase &g = p.ph[0];  // gate/up + SwiGLU -> h
   g.K = H;
   g.n_blocks = I / 128;
@@ -859,6 +878,18 @@ extern "C" moe_status moe_grouped_ffn_gather(const uint16_t *x, int64_t T, int32
   if (T >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   return run_ffn(x, n_rows, seg_offsets, seg_expert, S, E, w_gate_up_packed, w_down_packed, H, I,
                  h, y_perm, ws, ws_bytes, stream, true, src_assign, k, T);
+}
+
+extern "C" moe_status moe_grouped_ffn_masked(const uint16_t *x_perm, int32_t cap,
+                                             const int32_t *masked_m, const int32_t *seg_expert,
+                                             int32_t S, int32_t E, const uint16_t *w_gate_up_packed,
+                                             const uint16_t *w_down_packed, int32_t H, int32_t I,
+                                             uint16_t *h, uint16_t *y_perm, void *ws,
+                                             size_t ws_bytes, void *stream) {
+  if (cap < 1 || S < 1 || !masked_m) return MOE_ERR_INVALID_ARG;
+  const int64_t n_rows = (int64_t)S * cap;
+  return run_ffn(x_perm, n_rows, nullptr, seg_expert, S, E, w_gate_up_packed, w_down_packed, H, I,
+                 h, y_perm, ws, ws_bytes, stream, true, nullptr, 1, 0, masked_m, cap);
 }
 
 extern "C" moe_status moe_pack_expert_weights(const uint16_t *w_gate_up, const uint16_t *w_down,

@@ -276,7 +276,8 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
       atomicAdd(&rload[r], tot[s]);
   }
   // exclusive scan of the totals by warp 0: lane L owns a contiguous chunk
-  if (warp == 0) {
+  // (the fixed-capacity layout has no offsets and passes none)
+  if (warp == 0 && p.seg_offsets != nullptr) {
     const int per = (p.S + 31) / 32;
     const int lo = lane * per, hi = min(p.S, lo + per);
     int sum = 0;
@@ -321,6 +322,64 @@ __global__ void layout_finalize_kernel(LayoutArgs p) {
     p.dest_row[a] = d;
     p.src_assign[d] = (int32_t)a;
   }
+}
+
+// Fixed-capacity ("masked") layout: slot s owns rows [s*cap, (s+1)*cap).
+// "14. Serving Mixture-of-Experts Models", "Capacity, padding, and the drop
+// decision" (a fixed per-expert capacity; what overflows is dropped and its
+// output is zero); "Mixture-of-Experts Inference", "Communication pressure"
+// (decode pads tokens into fixed-size masked layouts so that one captured
+// graph can be replayed).  The scan left each assignment's stable rank
+// within its slot in dest_row; the first `cap` of a slot keep a row, later
+// ones get -1.  Also marks unused rows in src_assign, clips the per-slot and
+// per-rank counts to what runs, counts the drops, and clears the scan's
+// ticket and flags.  Block 0 does the per-slot work.
+__global__ void layout_finalize_masked_kernel(LayoutArgs p, int32_t cap, int32_t *masked_m,
+                                              int32_t *n_dropped) {
+  __shared__ int32_t rload[kMaxRanks];
+  __shared__ int32_t dropped;
+  moe::pdl_wait();
+  moe::pdl_trigger();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t n_flags = (int64_t)p.n_tiles * p.K;
+  for (int64_t i = i0; i < n_flags; i += stride) p.tile_flags[i] = 0u;
+  if (i0 == 0) *p.ticket = 0;
+  for (int64_t a = i0; a < p.A; a += stride) {
+    const int s = p.slot[a];
+    const int pos = p.dest_row[a];
+    if (s < 0 || s >= p.S || pos < 0 || pos >= cap) {
+      p.dest_row[a] = -1;
+      continue;
+    }
+    const int d = s * cap + pos;
+    p.dest_row[a] = d;
+    p.src_assign[d] = (int32_t)a;
+  }
+  const int64_t rows = (int64_t)p.S * cap;
+  for (int64_t i = i0; i < rows; i += stride) {
+    const int s = (int)(i / cap);
+    if ((int)(i - (int64_t)s * cap) >= min(p.seg_counts[s], cap)) p.src_assign[i] = -1;
+  }
+  if (blockIdx.x != 0) return;
+  for (int r = threadIdx.x; r < p.R; r += blockDim.x) rload[r] = 0;
+  if (threadIdx.x == 0) dropped = 0;
+  __syncthreads();
+  int my_drop = 0;
+  for (int s = threadIdx.x; s < p.S; s += blockDim.x) {
+    const int c = p.seg_counts[s];
+    const int m = min(c, cap);
+    masked_m[s] = m;
+    my_drop += c - m;
+    const int r = p.slot_rank[s];
+    if (r >= 0 && r < p.R) atomicAdd(&rload[r], m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) my_drop += __shfl_xor_sync(0xffffffffu, my_drop, off);
+  if ((threadIdx.x & 31) == 0 && my_drop) atomicAdd(&dropped, my_drop);
+  __syncthreads();
+  for (int r = threadIdx.x; r < p.R; r += blockDim.x) p.rank_counts[r] = rload[r];
+  if (threadIdx.x == 0) *n_dropped = dropped;
 }
 
 inline int64_t n_tiles_for(int64_t A) { return A > 0 ? (A + kTileA - 1) / kTileA : 0; }
@@ -582,6 +641,71 @@ extern "C" moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, in
   const int64_t cap = (int64_t)moe_host::sm_count() * 8;
   if (blocks > cap) blocks = cap;
   return moe_host::launch_pdl(layout_finalize_kernel, dim3((unsigned)blocks), dim3(256), 0, st, p);
+}
+
+extern "C" moe_status moe_dispatch_layout_masked(const int32_t *topk_ids, int64_t T, int32_t k,
+                                                 const moe_placement *pl, int32_t cap,
+                                                 int32_t *slot, int32_t *seg_counts,
+                                                 int32_t *masked_m, int32_t *dest_row,
+                                                 int32_t *src_assign, int32_t *rank_counts,
+                                                 int32_t *n_dropped, void *ws, size_t ws_bytes,
+                                                 void *stream) {
+  if (pl == nullptr || T < 0 || k < 1 || cap < 1) return MOE_ERR_INVALID_ARG;
+  const int64_t A = T * (int64_t)k;
+  if (A >= (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  if (pl->n_experts < 1 || pl->n_slots < 1 || pl->n_ranks < 1 || pl->ranks_per_node < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (pl->n_slots > kMaxSlots || pl->n_ranks > kMaxRanks || pl->n_experts > kMaxExperts)
+    return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)pl->n_slots * cap >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  if (!pl->slot_expert || !pl->slot_rank || !pl->rep_offsets || !pl->rep_slots || !seg_counts ||
+      !masked_m || !rank_counts || !n_dropped || !src_assign)
+    return MOE_ERR_INVALID_ARG;
+  if (A > 0 && (!topk_ids || !slot || !dest_row)) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_workspace_size(T, k, pl->n_slots);
+  if (moe_status st = moe_host::check_ws(ws, ws_bytes, need)) return st;
+
+  LayoutArgs p{};
+  p.topk_ids = topk_ids;
+  p.A = A;
+  p.k = k;
+  p.E = pl->n_experts;
+  p.S = pl->n_slots;
+  p.R = pl->n_ranks;
+  p.rpn = pl->ranks_per_node;
+  p.slot_expert = pl->slot_expert;
+  p.slot_rank = pl->slot_rank;
+  p.rep_offsets = pl->rep_offsets;
+  p.rep_slots = pl->rep_slots;
+  p.token_src_rank = pl->token_src_rank;
+  p.slot = slot;
+  p.seg_counts = seg_counts;
+  p.seg_offsets = nullptr;  // no contiguous offsets in this layout
+  p.dest_row = dest_row;
+  p.src_assign = src_assign;
+  p.rank_counts = rank_counts;
+  char *wsb = static_cast<char *>(ws);
+  p.tile_flags = reinterpret_cast<uint32_t *>(wsb + kFlagsOff);
+  p.ticket = reinterpret_cast<int32_t *>(wsb + kTicketOff);
+  p.status = moe_host::status_ptr(ws);
+  p.n_tiles = (int32_t)std::max<int64_t>(n_tiles_for(A), 1);
+  p.K = p.S;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t smem = layout_smem_words(p.S, p.R, p.E, p.K) * sizeof(int32_t);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(layout_scan_kernel<kModeRule>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (moe_status s = moe_host::launch_pdl(layout_scan_kernel<kModeRule>, dim3((unsigned)p.n_tiles),
+                                          dim3(kThreads), smem, st, p))
+    return s;
+  const int64_t rows = (int64_t)p.S * cap;
+  int64_t blocks = (std::max<int64_t>(std::max<int64_t>(A, rows), (int64_t)p.n_tiles * p.K) + 255) / 256;
+  const int64_t lim = (int64_t)moe_host::sm_count() * 8;
+  if (blocks > lim) blocks = lim;
+  return moe_host::launch_pdl(layout_finalize_masked_kernel, dim3((unsigned)blocks), dim3(256), 0,
+                              st, p, cap, masked_m, n_dropped);
 }
 
 // ---------------------------------------------------------------------------

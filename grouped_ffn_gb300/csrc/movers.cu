@@ -20,6 +20,7 @@ namespace {
 constexpr int kMoverThreads = 128;
 constexpr int kUnroll = 4;
 
+template <bool DROP>
 __global__ void __launch_bounds__(kMoverThreads) permute_kernel(
     const uint4 *__restrict__ x, int64_t T, int H8, int k, const int32_t *__restrict__ dest_row,
     uint4 *__restrict__ xp, int64_t A, int32_t *status) {
@@ -37,8 +38,8 @@ __global__ void __launch_bounds__(kMoverThreads) permute_kernel(
       }
       for (int j = 0; j < k; ++j) {
         const int32_t r = __ldg(dr + j);
-        if (r < 0 || r >= A) {
-          if (threadIdx.x == 0 && c0 == 0)
+        if (r < 0 || r >= A) {  // DROP: -1 marks a dropped assignment
+          if (threadIdx.x == 0 && c0 == 0 && !(DROP && r == -1))
             moe::report_error(status, MOE_ERR_DEVICE_INDEX, (int32_t)(t * k + j), moe::K_PERMUTE);
           continue;
         }
@@ -73,19 +74,23 @@ template <int KMAX>
 __global__ void __launch_bounds__(kMoverThreads) combine_kernel(
     const uint4 *__restrict__ yp, const int32_t *__restrict__ dest_row,
     const float *__restrict__ topk_w, int64_t T, int k, int H8, const uint4 *__restrict__ shared,
-    uint4 *__restrict__ y, int64_t A, int32_t *status) {
+    uint4 *__restrict__ y, int64_t A, int allow_drop, int32_t *status) {
   moe::pdl_wait();
   moe::pdl_trigger();
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     int32_t r[KMAX];
     float w[KMAX];
     bool ok = true;
+    uint32_t live = 0;  // terms that take part; a dropped one (-1) adds nothing
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
         r[j] = __ldg(dest_row + t * k + j);
         w[j] = __ldg(topk_w + t * k + j);
-        if (r[j] < 0 || r[j] >= A) ok = false;
+        if (r[j] >= 0 && r[j] < A)
+          live |= 1u << j;
+        else if (!(allow_drop && r[j] == -1))
+          ok = false;
       }
     }
     if (!ok) {
@@ -96,7 +101,7 @@ __global__ void __launch_bounds__(kMoverThreads) combine_kernel(
       uint4 v[KMAX];
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
-        if (j < k) v[j] = moe::ld_stream_u4(yp + (int64_t)r[j] * H8 + c);
+        if ((live >> j) & 1u) v[j] = moe::ld_stream_u4(yp + (int64_t)r[j] * H8 + c);
       float acc[8];
       if (shared) {
         const uint4 s = moe::ld_stream_u4(shared + t * H8 + c);
@@ -112,7 +117,7 @@ __global__ void __launch_bounds__(kMoverThreads) combine_kernel(
       }
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
-        if (j < k) bf16x8_fma(v[j], w[j], acc);
+        if ((live >> j) & 1u) bf16x8_fma(v[j], w[j], acc);
       uint4 o;
       o.x = pack_bf16x2(acc[0], acc[1]);
       o.y = pack_bf16x2(acc[2], acc[3]);
@@ -271,30 +276,33 @@ unsigned mover_grid(int64_t T) {
 
 }  // namespace
 
-extern "C" moe_status moe_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
-                                  const int32_t *dest_row, uint16_t *x_perm, void *ws,
-                                  size_t ws_bytes, void *stream) {
-  if (T < 0 || H < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+namespace {
+
+// n_rows: rows of x_perm; allow_drop: dest_row -1 marks a dropped assignment.
+moe_status run_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                       const int32_t *dest_row, int64_t n_rows, uint16_t *x_perm, int allow_drop,
+                       void *ws, size_t ws_bytes, void *stream) {
+  if (T < 0 || H < 1 || k < 1 || n_rows < 0) return MOE_ERR_INVALID_ARG;
   if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  if (!x || !dest_row || !x_perm) return MOE_ERR_INVALID_ARG;
+  if (!x || !dest_row || (!x_perm && n_rows > 0)) return MOE_ERR_INVALID_ARG;
   if (!moe_host::aligned16(x) || !moe_host::aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
   if (moe_status s = moe_host::check_ws(ws, ws_bytes, moe::kStatusBytes)) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return moe_host::launch_pdl(permute_kernel, dim3(mover_grid(T)), dim3(kMoverThreads), 0, st,
+  return moe_host::launch_pdl(allow_drop ? permute_kernel<true> : permute_kernel<false>,
+                              dim3(mover_grid(T)), dim3(kMoverThreads), 0, st,
                               reinterpret_cast<const uint4 *>(x), T, H / 8, k, dest_row,
-                              reinterpret_cast<uint4 *>(x_perm), T * (int64_t)k,
-                              moe_host::status_ptr(ws));
+                              reinterpret_cast<uint4 *>(x_perm), n_rows, moe_host::status_ptr(ws));
 }
 
-extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *dest_row,
-                                  const float *topk_w, int64_t T, int32_t k, int32_t H,
-                                  const uint16_t *shared, uint16_t *y, void *ws, size_t ws_bytes,
-                                  void *stream) {
-  if (T < 0 || H < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+moe_status run_combine(const uint16_t *y_perm, int64_t n_rows, const int32_t *dest_row,
+                       const float *topk_w, int64_t T, int32_t k, int32_t H,
+                       const uint16_t *shared, uint16_t *y, int allow_drop, void *ws,
+                       size_t ws_bytes, void *stream) {
+  if (T < 0 || H < 1 || k < 1 || n_rows < 0) return MOE_ERR_INVALID_ARG;
   if (H % 8 != 0 || k > 16) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  if (!y_perm || !dest_row || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+  if ((!y_perm && n_rows > 0) || !dest_row || !topk_w || !y) return MOE_ERR_INVALID_ARG;
   if (!moe_host::aligned16(y_perm) || !moe_host::aligned16(y) ||
       (shared && !moe_host::aligned16(shared)))
     return MOE_ERR_INVALID_ARG;
@@ -303,17 +311,51 @@ extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *dest_ro
   const uint4 *yp = reinterpret_cast<const uint4 *>(y_perm);
   const uint4 *sh = reinterpret_cast<const uint4 *>(shared);
   uint4 *yo = reinterpret_cast<uint4 *>(y);
-  const int64_t A = T * (int64_t)k;
   int32_t *status = moe_host::status_ptr(ws);
   const dim3 g(mover_grid(T)), b(kMoverThreads);
   const int H8 = H / 8;
+  const int64_t A = n_rows;
+  const int d = allow_drop;
   if (k <= 2)
-    return moe_host::launch_pdl(combine_kernel<2>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, status);
+    return moe_host::launch_pdl(combine_kernel<2>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, d, status);
   if (k <= 4)
-    return moe_host::launch_pdl(combine_kernel<4>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, status);
+    return moe_host::launch_pdl(combine_kernel<4>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, d, status);
   if (k <= 8)
-    return moe_host::launch_pdl(combine_kernel<8>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, status);
-  return moe_host::launch_pdl(combine_kernel<16>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, status);
+    return moe_host::launch_pdl(combine_kernel<8>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, d, status);
+  return moe_host::launch_pdl(combine_kernel<16>, g, b, 0, st, yp, dest_row, topk_w, T, k, H8, sh, yo, A, d, status);
+}
+
+}  // namespace
+
+extern "C" moe_status moe_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                                  const int32_t *dest_row, uint16_t *x_perm, void *ws,
+                                  size_t ws_bytes, void *stream) {
+  if (T < 0 || k < 1) return MOE_ERR_INVALID_ARG;
+  return run_permute(x, T, H, k, dest_row, T * (int64_t)k, x_perm, 0, ws, ws_bytes, stream);
+}
+
+extern "C" moe_status moe_permute_masked(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                                         const int32_t *dest_row, int64_t n_rows,
+                                         uint16_t *x_perm, void *ws, size_t ws_bytes,
+                                         void *stream) {
+  return run_permute(x, T, H, k, dest_row, n_rows, x_perm, 1, ws, ws_bytes, stream);
+}
+
+extern "C" moe_status moe_combine(const uint16_t *y_perm, const int32_t *dest_row,
+                                  const float *topk_w, int64_t T, int32_t k, int32_t H,
+                                  const uint16_t *shared, uint16_t *y, void *ws, size_t ws_bytes,
+                                  void *stream) {
+  if (T < 0 || k < 1) return MOE_ERR_INVALID_ARG;
+  return run_combine(y_perm, T * (int64_t)k, dest_row, topk_w, T, k, H, shared, y, 0, ws,
+                     ws_bytes, stream);
+}
+
+extern "C" moe_status moe_combine_masked(const uint16_t *y_perm, int64_t n_rows,
+                                         const int32_t *dest_row, const float *topk_w, int64_t T,
+                                         int32_t k, int32_t H, const uint16_t *shared, uint16_t *y,
+                                         void *ws, size_t ws_bytes, void *stream) {
+  return run_combine(y_perm, n_rows, dest_row, topk_w, T, k, H, shared, y, 1, ws, ws_bytes,
+                     stream);
 }
 
 extern "C" moe_status moe_balance_stats(const int32_t *rank_counts, int32_t R, double *balancedness,

@@ -25,15 +25,27 @@ class MoELayer:
                  shared_w_gate_up: Optional[torch.Tensor] = None,
                  shared_w_down: Optional[torch.Tensor] = None, device="cuda",
                  packed: bool = True, replica_relax: Optional[tuple] = None,
-                 gather: bool = False):
+                 gather: bool = False, masked_cap: Optional[int] = None,
+                 fp8_dispatch: bool = False):
         """replica_relax=(c_num, c_den) chooses each assignment's replica by
         locality-preferred water-filling with load bounds C = c_num/c_den
         (moe_route_replicas); None keeps the fixed replica rule.
         gather=True reads the FFN's rows straight from x through the
-        inverse permutation (moe_grouped_ffn_gather): no permute step."""
-        if gather and not packed:
-            raise ValueError("gather mode streams packed weights")
+        inverse permutation (moe_grouped_ffn_gather): no permute step.
+        masked_cap=c uses the fixed-capacity layout (moe_dispatch_layout_masked):
+        every slot owns c rows, assignments beyond them are dropped.
+        fp8_dispatch=True moves E4M3 codes and block scales through the
+        dispatched buffer (moe_permute_fp8) and restores bf16 rows before
+        the FFN (moe_dequant_fp8)."""
+        if (gather or masked_cap is not None) and not packed:
+            raise ValueError("gather and fixed-capacity modes stream packed weights")
+        if gather and (masked_cap is not None or fp8_dispatch):
+            raise ValueError("gather mode reads x directly: no fixed capacity, no FP8 dispatch")
+        if masked_cap is not None and (replica_relax is not None or masked_cap < 1):
+            raise ValueError("fixed-capacity layout: cap >= 1, fixed replica rule")
         self.gather = gather
+        self.masked_cap = masked_cap
+        self.fp8_dispatch = fp8_dispatch
         self.H, self.I, self.E, self.k = H, I, E, k
         self.placement = placement
         self.packed = packed
@@ -54,15 +66,22 @@ class MoELayer:
         bf = dict(dtype=torch.bfloat16, device=dev)
         self.topk_ids = torch.empty(max_tokens, k, **i32)
         self.topk_w = torch.empty(max_tokens, k, dtype=torch.float32, device=dev)
+        # dispatched rows: T*k in the contiguous layout, S*cap in the fixed one
+        rows = A if masked_cap is None else S * masked_cap
         self.slot = torch.empty(A, **i32)
         self.seg_counts = torch.empty(S, **i32)
         self.seg_offsets = torch.empty(S + 1, **i32)
         self.dest_row = torch.empty(A, **i32)
-        self.src_assign = torch.empty(A, **i32)
+        self.src_assign = torch.empty(rows, **i32)
         self.rank_counts = torch.empty(R, **i32)
-        self.x_perm = torch.empty(0 if gather else A, H, **bf)
-        self.h = torch.empty(A, I, **bf)
-        self.y_perm = torch.empty(A, H, **bf)
+        self.masked_m = torch.zeros(S, **i32)
+        self.n_dropped = torch.zeros(1, **i32)
+        self.x_perm = torch.empty(0 if gather else rows, H, **bf)
+        if fp8_dispatch:
+            self.xq = torch.empty(rows, H, dtype=torch.uint8, device=dev)
+            self.x_scale = torch.empty(rows, H // 128, dtype=torch.float32, device=dev)
+        self.h = torch.empty(rows, I, **bf)
+        self.y_perm = torch.empty(rows, H, **bf)
         self.balancedness = torch.empty(1, dtype=torch.float64, device=dev)
         self.max_count = torch.empty(1, **i32)
         self.total = torch.empty(1, dtype=torch.int64, device=dev)
@@ -80,8 +99,10 @@ class MoELayer:
         # per step: route, layout scan + finalize, permute, FFN, combine,
         # balance (+1 shared FFN, +4 replica routing: prep, key scan,
         # water-fill, assign); packing happens once, here
+        # (+1 FP8 dequantization)
         self.launches_per_step = 7 + (1 if shared_w_gate_up is not None else 0) + \
-            (4 if replica_relax is not None else 0) - (1 if gather else 0)
+            (4 if replica_relax is not None else 0) - (1 if gather else 0) + \
+            (1 if fp8_dispatch else 0)
 
     @staticmethod
     def _pack(w_gate_up, w_down):
@@ -115,6 +136,8 @@ class MoELayer:
         ids, w = self.topk_ids[:T], self.topk_w[:T]
         moe.moe_route(logits, self.cfg, ids, w, self.ws, stream)
         mark("route")
+        if self.masked_cap is not None:
+            return self._forward_masked(x, y, ids, w, T, A, stream, mark)
         if self.replica_relax is None:
             moe.moe_dispatch_layout(ids, self.placement, self.slot[:A], self.seg_counts,
                                     self.seg_offsets, self.dest_row[:A], self.src_assign[:A],
@@ -132,22 +155,65 @@ class MoELayer:
                                        self.placement.slot_expert, self.w_gate_up, self.w_down,
                                        self.h[:A], self.y_perm[:A], self.ws, stream)
         else:
-            moe.moe_permute(x, self.k, self.dest_row[:A], self.x_perm[:A], self.ws, stream)
-            mark("permute")
+            self._dispatch(x, A, A, None, stream, mark)
             self._ffn(self.x_perm[:A], self.seg_offsets, self.placement.slot_expert,
                       self.w_gate_up, self.w_down, self.h[:A], self.y_perm[:A], self.ws, stream)
         mark("grouped_ffn")
-        shared = None
-        if self.shared_I:
-            self._ffn(x, self._shared_offs(T), self.shared_expert, self.shared_w_gate_up,
-                      self.shared_w_down, self.shared_h[:T], self.shared_y[:T], self.ws, stream)
-            shared = self.shared_y[:T]
-            mark("shared_ffn")
+        shared = self._shared(x, T, stream, mark)
         moe.moe_combine(self.y_perm[:A], self.dest_row[:A], w, y, self.ws, shared, stream)
         mark("combine")
+        self._balance(stream, mark)
+        return y
+
+    def _dispatch(self, x, A, rows, masked_m, stream, mark):
+        """Rows of x into the dispatched buffer: a bf16 copy, or E4M3 codes
+        plus block scales restored to bf16 by the receiving step."""
+        dr = self.dest_row[:A]
+        if self.fp8_dispatch:
+            moe.moe_permute_fp8(x, self.k, dr, self.xq[:rows], self.x_scale[:rows], self.ws, stream)
+            mark("permute")
+            moe.moe_dequant_fp8(self.xq[:rows], self.x_scale[:rows], self.x_perm[:rows], masked_m,
+                                self.masked_cap or 0, self.ws, stream)
+            mark("dequant")
+        elif masked_m is not None:
+            moe.moe_permute_masked(x, self.k, dr, self.x_perm[:rows], self.ws, stream)
+            mark("permute")
+        else:
+            moe.moe_permute(x, self.k, dr, self.x_perm[:A], self.ws, stream)
+            mark("permute")
+
+    def _shared(self, x, T, stream, mark):
+        if not self.shared_I:
+            return None
+        self._ffn(x, self._shared_offs(T), self.shared_expert, self.shared_w_gate_up,
+                  self.shared_w_down, self.shared_h[:T], self.shared_y[:T], self.ws, stream)
+        mark("shared_ffn")
+        return self.shared_y[:T]
+
+    def _balance(self, stream, mark):
         moe.moe_balance_stats(self.rank_counts, self.balancedness, self.max_count, self.total,
                               self.ws, stream)
         mark("balance")
+
+    def _forward_masked(self, x, y, ids, w, T, A, stream, mark):
+        """The step on the fixed-capacity layout: every buffer and launch has
+        the same shape whatever the routing; dropped assignments add
+        nothing to y."""
+        cap = self.masked_cap
+        rows = self.placement.n_slots * cap
+        moe.moe_dispatch_layout_masked(ids, self.placement, cap, self.slot[:A], self.seg_counts,
+                                       self.masked_m, self.dest_row[:A], self.src_assign,
+                                       self.rank_counts, self.n_dropped, self.ws, stream)
+        mark("layout")
+        self._dispatch(x, A, rows, self.masked_m, stream, mark)
+        moe.moe_grouped_ffn_masked(self.x_perm, cap, self.masked_m, self.placement.slot_expert,
+                                   self.w_gate_up, self.w_down, self.h, self.y_perm, self.ws,
+                                   stream)
+        mark("grouped_ffn")
+        shared = self._shared(x, T, stream, mark)
+        moe.moe_combine_masked(self.y_perm, self.dest_row[:A], w, y, self.ws, shared, stream)
+        mark("combine")
+        self._balance(stream, mark)
         return y
 
     def capture(self, logits: torch.Tensor, x: torch.Tensor, y: torch.Tensor):

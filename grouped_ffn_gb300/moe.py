@@ -82,6 +82,16 @@ _SIGNATURES = {
     "moe_combine_merged": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(PlacementC), _I64, _I32,
                                           _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_balance_stats": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_dispatch_layout_masked": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC),
+                                                  _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                                  _P]),
+    "moe_permute_masked": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _SZ, _P]),
+    "moe_grouped_ffn_masked": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _P, _P, _I32, _I32,
+                                              _P, _P, _P, _SZ, _P]),
+    "moe_combine_masked": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I32, _I32, _P, _P, _P, _SZ,
+                                          _P]),
+    "moe_permute_fp8": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _SZ, _P]),
+    "moe_dequant_fp8": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_version": (ctypes.c_char_p, []),
 }
@@ -391,6 +401,108 @@ def moe_balance_stats(rank_counts, balancedness, max_count, total, ws=None, stre
     _check("moe_balance_stats", lib().moe_balance_stats(
         _ptr(rank_counts), rank_counts.numel(), _ptr(balancedness), _ptr(max_count), _ptr(total),
         _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+# ------------------------------------------------------------------ fixed-capacity layout
+def moe_dispatch_layout_masked(topk_ids, placement: DevicePlacement, cap: int, slot, seg_counts,
+                               masked_m, dest_row, src_assign, rank_counts, n_dropped, ws,
+                               stream=None):
+    """Fixed-capacity layout: slot s owns rows [s*cap, (s+1)*cap); its
+    assignments past the first `cap` are dropped (dest_row -1).  src_assign
+    has S*cap entries; n_dropped is a device int32[1]."""
+    for n, t in (("topk_ids", topk_ids), ("slot", slot), ("seg_counts", seg_counts),
+                 ("masked_m", masked_m), ("dest_row", dest_row), ("src_assign", src_assign),
+                 ("rank_counts", rank_counts), ("n_dropped", n_dropped)):
+        _need(t, torch.int32, n)
+    T, k = topk_ids.shape
+    if src_assign.numel() < placement.c.n_slots * cap:
+        raise ValueError("moe_dispatch_layout_masked: src_assign needs S*cap entries")
+    _check("moe_dispatch_layout_masked", lib().moe_dispatch_layout_masked(
+        _ptr(topk_ids), T, k, ctypes.byref(placement.c), cap, _ptr(slot), _ptr(seg_counts),
+        _ptr(masked_m), _ptr(dest_row), _ptr(src_assign), _ptr(rank_counts), _ptr(n_dropped),
+        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_permute_masked(x, k: int, dest_row, x_perm, ws, stream=None):
+    """moe_permute into x_perm [n_rows, H] where dest_row -1 is a drop."""
+    _bf16(x, "x")
+    _bf16(x_perm, "x_perm")
+    _need(dest_row, torch.int32, "dest_row")
+    T, H = x.shape
+    _check("moe_permute_masked", lib().moe_permute_masked(
+        _ptr(x), T, H, k, _ptr(dest_row), x_perm.shape[0], _ptr(x_perm), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def moe_grouped_ffn_masked(x_perm, cap: int, masked_m, seg_expert, w_gate_up_packed,
+                           w_down_packed, h, y_perm, ws, stream=None):
+    """The grouped FFN on a fixed-capacity layout (packed weights): slot s
+    is rows [s*cap, s*cap + masked_m[s]) of x_perm [S*cap, H]."""
+    for n, t in (("x_perm", x_perm), ("w_gate_up_packed", w_gate_up_packed),
+                 ("w_down_packed", w_down_packed), ("h", h), ("y_perm", y_perm)):
+        _bf16(t, n)
+    _need(masked_m, torch.int32, "masked_m")
+    _need(seg_expert, torch.int32, "seg_expert")
+    S = seg_expert.numel()
+    n_rows, H = x_perm.shape
+    E, two_i, H2 = w_gate_up_packed.shape
+    I = two_i // 2
+    if n_rows != S * cap or masked_m.numel() != S or H2 != H or \
+            tuple(w_down_packed.shape) != (E, H, I) or tuple(h.shape) != (n_rows, I) or \
+            tuple(y_perm.shape) != (n_rows, H):
+        raise ValueError("moe_grouped_ffn_masked: inconsistent shapes")
+    _check("moe_grouped_ffn_masked", lib().moe_grouped_ffn_masked(
+        _ptr(x_perm), cap, _ptr(masked_m), _ptr(seg_expert), S, E, _ptr(w_gate_up_packed),
+        _ptr(w_down_packed), H, I, _ptr(h), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_combine_masked(y_perm, dest_row, topk_w, y, ws, shared=None, stream=None):
+    """moe_combine over y_perm [n_rows, H] where dest_row -1 (a dropped
+    assignment) adds nothing."""
+    _bf16(y_perm, "y_perm")
+    _bf16(y, "y")
+    if shared is not None:
+        _bf16(shared, "shared")
+    _need(dest_row, torch.int32, "dest_row")
+    _need(topk_w, torch.float32, "topk_w")
+    T, k = topk_w.shape
+    _check("moe_combine_masked", lib().moe_combine_masked(
+        _ptr(y_perm), y_perm.shape[0], _ptr(dest_row), _ptr(topk_w), T, k, y.shape[1],
+        _ptr(shared), _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+# ------------------------------------------------------------------ FP8 dispatch
+def moe_permute_fp8(x, k: int, dest_row, xq, x_scale, ws, stream=None):
+    """Quantize each token row to E4M3 (power-of-two scale per 128
+    channels) and write it to its k dispatched rows: xq uint8 [n_rows, H],
+    x_scale fp32 [n_rows, H/128]; dest_row -1 is a drop."""
+    _bf16(x, "x")
+    _need(dest_row, torch.int32, "dest_row")
+    _need(xq, torch.uint8, "xq")
+    _need(x_scale, torch.float32, "x_scale")
+    T, H = x.shape
+    n_rows = xq.shape[0]
+    if xq.shape[1] != H or tuple(x_scale.shape) != (n_rows, H // 128):
+        raise ValueError("moe_permute_fp8: inconsistent shapes")
+    _check("moe_permute_fp8", lib().moe_permute_fp8(
+        _ptr(x), T, H, k, _ptr(dest_row), n_rows, _ptr(xq), _ptr(x_scale), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def moe_dequant_fp8(xq, x_scale, x_perm, masked_m=None, cap: int = 0, ws=None, stream=None):
+    """x_perm = bf16(E4M3(xq) * x_scale); with masked_m only the used rows of
+    each fixed-capacity slot."""
+    _need(xq, torch.uint8, "xq")
+    _need(x_scale, torch.float32, "x_scale")
+    _bf16(x_perm, "x_perm")
+    if masked_m is not None:
+        _need(masked_m, torch.int32, "masked_m")
+    n_rows, H = xq.shape
+    if tuple(x_perm.shape) != (n_rows, H) or tuple(x_scale.shape) != (n_rows, H // 128):
+        raise ValueError("moe_dequant_fp8: inconsistent shapes")
+    _check("moe_dequant_fp8", lib().moe_dequant_fp8(
+        _ptr(xq), _ptr(x_scale), n_rows, H, cap, _ptr(masked_m), _ptr(x_perm), _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def moe_status_string(status: int) -> str:

@@ -237,6 +237,34 @@ moe_status moe_dispatch_layout_noalloc(const int32_t *topk_ids, int64_t T, int32
                                        int32_t *dest_row, int32_t *src_assign,
                                        int32_t *rank_counts, int32_t *status, void *stream);
 
+/* Fixed-capacity ("masked") dispatch layout: every slot owns `cap` rows of
+ * the dispatched buffer whatever its load, so buffer shapes, kernel grids
+ * and addresses are the same every step.  "Mixture-of-Experts Inference",
+ * "Communication pressure" (decode pads tokens into fixed-size masked
+ * layouts so that one captured CUDA graph can be replayed); "14. Serving
+ * Mixture-of-Experts Models", "Capacity, padding, and the drop decision"
+ * (a fixed per-expert capacity; assignments beyond it are dropped and
+ * their output for the layer is zero).
+ *  Slot choice as moe_dispatch_layout.  Slot s owns rows [s*cap, (s+1)*cap);
+ *  its assignments in ascending order a take rows s*cap, s*cap + 1, ...;
+ *  those after the first `cap` are dropped.
+ *  Outputs (device int32, caller-allocated):
+ *   slot[A]           slot of each assignment;
+ *   seg_counts[S]     assignments per slot (the demand, before dropping);
+ *   masked_m[S]       rows used in each slot: min(seg_counts[s], cap);
+ *   dest_row[A]       s*cap + rank within the slot, or -1 if dropped;
+ *   src_assign[S*cap] assignment held by each row, -1 on unused rows;
+ *   rank_counts[R]    rows each rank executes (sum of its slots' masked_m);
+ *   n_dropped[1]      assignments dropped.
+ *  Limits: those of moe_dispatch_layout, cap >= 1, S*cap < 2^31.
+ *  ws: moe_workspace_size(T, k, S), same zero-on-entry rule. */
+moe_status moe_dispatch_layout_masked(const int32_t *topk_ids, int64_t T, int32_t k,
+                                      const moe_placement *placement, int32_t cap,
+                                      int32_t *slot, int32_t *seg_counts, int32_t *masked_m,
+                                      int32_t *dest_row, int32_t *src_assign,
+                                      int32_t *rank_counts, int32_t *n_dropped, void *ws,
+                                      size_t ws_bytes, void *stream);
+
 /* Permute: x_perm[dest_row[t*k + j], :] = x[t, :] for every j (a byte
  * copy).  "14. Serving Mixture-of-Experts Models", "Price one dispatch"
  * (each assignment carries its token's hidden row: 2 * H bytes).
@@ -246,6 +274,40 @@ moe_status moe_dispatch_layout_noalloc(const int32_t *topk_ids, int64_t T, int32
 moe_status moe_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
                        const int32_t *dest_row, uint16_t *x_perm, void *ws,
                        size_t ws_bytes, void *stream);
+
+/* moe_permute into a buffer of n_rows rows (a fixed-capacity layout:
+ * n_rows = S*cap) where dest_row -1 marks a dropped assignment, which moves
+ * nothing.  Other out-of-range rows are skipped and reported as
+ * MOE_ERR_DEVICE_INDEX.  Rows no assignment lands on are left unwritten. */
+moe_status moe_permute_masked(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                              const int32_t *dest_row, int64_t n_rows, uint16_t *x_perm,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/* FP8 dispatch, sending side: quantize each token row once and write the
+ * codes to its k destination rows.  "Mixture-of-Experts Inference",
+ * "Communication pressure" (token activations can be quantized, for example
+ * to FP8, before dispatch, to cut the bytes the all-to-all moves).
+ *  Format (a reading; the pages name only "FP8"): OCP E4M3 codes; one fp32
+ *  scale 2^e per (token, 128 consecutive channels), e the smallest integer
+ *  with max|x| <= 448 * 2^e over the block, clamped to [-126, 127], e = 0
+ *  for an all-zero block; code = E4M3(x / 2^e), nearest, ties to even.
+ *  x        device bf16 [T, H];  dest_row device int32 [T*k] (-1: dropped);
+ *  xq       device uint8 [n_rows, H] (codes, row r = dispatched row r);
+ *  x_scale  device fp32 [n_rows, H/128].
+ *  Limits: H % 128 == 0; x and xq 16-byte aligned. */
+moe_status moe_permute_fp8(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                           const int32_t *dest_row, int64_t n_rows, uint8_t *xq, float *x_scale,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* FP8 dispatch, receiving side: x_perm[r, c] = bf16(E4M3 value of
+ * xq[r, c] * x_scale[r, c/128]) (the product is exact in fp32; one rounding
+ * to bf16, nearest even).  With masked_m (device int32 [n_rows / cap], a
+ * fixed-capacity layout) row r is restored only if r mod cap <
+ * masked_m[r / cap]; otherwise every row is.  ws may be NULL.
+ *  Limits: H % 128 == 0; xq and x_perm 16-byte aligned. */
+moe_status moe_dequant_fp8(const uint8_t *xq, const float *x_scale, int64_t n_rows, int32_t H,
+                           int32_t cap, const int32_t *masked_m, uint16_t *x_perm, void *ws,
+                           size_t ws_bytes, void *stream);
 
 /* Grouped SwiGLU expert FFN over contiguous segments.  "14. Serving
  * Mixture-of-Experts Models", "Follow one token", step 3 (a grouped matrix
@@ -276,6 +338,21 @@ moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t
                            const uint16_t *w_gate_up, const uint16_t *w_down, int32_t H,
                            int32_t I, uint16_t *h, uint16_t *y_perm, void *ws,
                            size_t ws_bytes, void *stream);
+
+/* moe_grouped_ffn_packed on a fixed-capacity layout: segment s is rows
+ * [s*cap, s*cap + masked_m[s]) of x_perm [S*cap, H], with expert
+ * seg_expert[s]; h is [S*cap, I] and y_perm [S*cap, H].  Only the rows in
+ * use are computed and stored, so padding costs memory but no tensor-core
+ * time.  The launch's shape depends on S and cap only, so it can be
+ * captured once in a CUDA graph and replayed for any routing.
+ *  masked_m device int32 [S] (moe_dispatch_layout_masked); a value outside
+ *  [0, cap] is clamped and reported as MOE_ERR_DEVICE_INDEX.
+ *  Limits as moe_grouped_ffn, and S*cap < 2^31. */
+moe_status moe_grouped_ffn_masked(const uint16_t *x_perm, int32_t cap, const int32_t *masked_m,
+                                  const int32_t *seg_expert, int32_t S, int32_t E,
+                                  const uint16_t *w_gate_up_packed, const uint16_t *w_down_packed,
+                                  int32_t H, int32_t I, uint16_t *h, uint16_t *y_perm, void *ws,
+                                  size_t ws_bytes, void *stream);
 
 /* Expert weights rearranged for streaming: each 128-row x 64-column block
  * that the grouped GEMM loads per pipeline stage becomes one contiguous
@@ -332,6 +409,15 @@ moe_status moe_grouped_ffn_gather(const uint16_t *x, int64_t T, int32_t k,
 moe_status moe_combine(const uint16_t *y_perm, const int32_t *dest_row, const float *topk_w,
                        int64_t T, int32_t k, int32_t H, const uint16_t *shared, uint16_t *y,
                        void *ws, size_t ws_bytes, void *stream);
+
+/* moe_combine on a buffer of n_rows rows (a fixed-capacity layout: n_rows =
+ * S*cap) where dest_row -1 marks a dropped assignment: its term is skipped,
+ * so it adds nothing ("14. Serving Mixture-of-Experts Models", "Capacity,
+ * padding, and the drop decision": a dropped token's output is zero). */
+moe_status moe_combine_masked(const uint16_t *y_perm, int64_t n_rows, const int32_t *dest_row,
+                              const float *topk_w, int64_t T, int32_t k, int32_t H,
+                              const uint16_t *shared, uint16_t *y, void *ws, size_t ws_bytes,
+                              void *stream);
 
 /* Combine with node-local pre-reduction, the combine side of "Zepp"'s
  * merge (Section 4.2, "Merge": the weighted expert outputs of one token on

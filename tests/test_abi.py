@@ -86,6 +86,28 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert lib.moe_dispatch_layout(FAKE, 8, 2, ctypes.byref(pl), FAKE, FAKE, FAKE, FAKE, FAKE,
                                    FAKE, FAKE, 256, None) == 6
     assert lib.moe_balance_stats(FAKE, 0, FAKE, FAKE, FAKE, None, 0, None) == 1
+    # fixed-capacity layout: cap >= 1, S*cap < 2^31, workspace
+    pl = moe.PlacementC(64, 64, 8, 8, FAKE.value, FAKE.value, FAKE.value, FAKE.value, None)
+    lay = lambda cap, wsb: lib.moe_dispatch_layout_masked(
+        FAKE, 8, 2, ctypes.byref(pl), cap, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, wsb, None)
+    assert lay(0, 1 << 20) == 1
+    assert lay(1 << 26, 1 << 20) == 2
+    assert lay(4, 256) == 6
+    # masked FFN: cap >= 1; masked permute / combine keep the plain checks
+    assert lib.moe_grouped_ffn_masked(FAKE, 0, FAKE, FAKE, 4, 8, FAKE, FAKE, 256, 128, FAKE, FAKE,
+                                      FAKE, 1 << 16, None) == 1
+    assert lib.moe_grouped_ffn_masked(FAKE, 8, FAKE, FAKE, 4, 8, FAKE, FAKE, 300, 128, FAKE, FAKE,
+                                      FAKE, 1 << 16, None) == 2
+    assert lib.moe_permute_masked(FAKE, 8, 12, 2, FAKE, 16, FAKE, FAKE, 256, None) == 2
+    assert lib.moe_permute_masked(FAKE, 8, 256, 2, FAKE, -1, FAKE, FAKE, 256, None) == 1
+    assert lib.moe_combine_masked(FAKE, 16, FAKE, FAKE, 8, 17, 256, None, FAKE, FAKE, 256, None) == 2
+    # FP8 dispatch: H % 128, alignment of the code buffer, masked geometry
+    assert lib.moe_permute_fp8(FAKE, 8, 192, 2, FAKE, 16, FAKE, FAKE, FAKE, 256, None) == 2
+    assert lib.moe_permute_fp8(FAKE, 8, 256, 2, FAKE, 16, ctypes.c_void_p(0x10004), FAKE, FAKE,
+                               256, None) == 1
+    assert lib.moe_permute_fp8(FAKE, 8, 256, 2, FAKE, 16, FAKE, FAKE, None, 0, None) == 6
+    assert lib.moe_dequant_fp8(FAKE, FAKE, 10, 256, 3, FAKE, FAKE, None, 0, None) == 1
+    assert lib.moe_dequant_fp8(FAKE, FAKE, 10, 200, 0, None, FAKE, None, 0, None) == 2
 
 
 def test_binding_refuses_cpu_tensors(lib):
