@@ -43,92 +43,145 @@ __device__ __forceinline__ float pow2f(int e) {  // e in [-126, 127]
 }
 
 // One CTA per token (grid-stride).  Half-warp h of the CTA quantizes blocks
-// h, h + 16, ...: each lane converts 8 channels (one 16-byte load) and the
-// half-warp reduces the block maximum with shuffles.  The codes of a block
-// are written to each of the token's k destination rows (8 bytes a lane).
+// h, h + 16, h + 32, ...: each lane converts 8 channels (one 16-byte load)
+// of a block and the half-warp reduces the block maximum with shuffles.  A
+// lane first loads its share of up to kPerLane blocks, so that many loads
+// are in flight, then quantizes them and writes the codes of each block to
+// the token's k destination rows (8 bytes a lane, 128 contiguous bytes a
+// half-warp).
+constexpr int kPerLane = 4;
+
+__device__ __forceinline__ uint2 quantize8(const uint4 &v, float inv) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t packed[2];
+#pragma unroll
+  for (int i = 0; i < 4; i += 2) {
+    const float2 lo = make_float2(__uint_as_float(w[i] << 16) * inv,
+                                  __uint_as_float(w[i] & 0xFFFF0000u) * inv);
+    const float2 hi = make_float2(__uint_as_float(w[i + 1] << 16) * inv,
+                                  __uint_as_float(w[i + 1] & 0xFFFF0000u) * inv);
+    const uint32_t c0 = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t c1 = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
+    packed[i / 2] = (c0 & 0xFFFFu) | (c1 << 16);
+  }
+  return make_uint2(packed[0], packed[1]);
+}
+
+__device__ __forceinline__ uint32_t abs_max_bits(const uint4 &v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+  return m;
+}
+
 __global__ void __launch_bounds__(kQuantThreads) permute_fp8_kernel(
     const uint4 *__restrict__ x, int64_t T, int H, int k, const int32_t *__restrict__ dest_row,
     int64_t n_rows, uint2 *__restrict__ xq, float *__restrict__ xs, int32_t *status) {
   moe::pdl_wait();
   moe::pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int sub = lane & 15;
+  constexpr int kHalfWarps = kQuantThreads / 16;
+  const int sub = threadIdx.x & 15;
   const int hw = threadIdx.x >> 4;
   const int nb = H / kBlock;
   const int H8 = H / 8;
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     const int32_t *dr = dest_row + t * k;
-    for (int b = hw; b < nb; b += kQuantThreads / 16) {
-      const uint4 v = moe::ld_stream_u4(x + t * H8 + b * 16 + sub);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t m = 0;
+    for (int b0 = hw; b0 < nb; b0 += kHalfWarps * kPerLane) {
+      uint4 v[kPerLane];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-      const int e = block_exponent(m);
-      const float inv = pow2f(-e);
-      uint32_t packed[2];
-#pragma unroll
-      for (int i = 0; i < 4; i += 2) {
-        const float2 lo = make_float2(__uint_as_float(w[i] << 16) * inv,
-                                      __uint_as_float(w[i] & 0xFFFF0000u) * inv);
-        const float2 hi = make_float2(__uint_as_float(w[i + 1] << 16) * inv,
-                                      __uint_as_float(w[i + 1] & 0xFFFF0000u) * inv);
-        const uint32_t c0 = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
-        const uint32_t c1 = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
-        packed[i / 2] = (c0 & 0xFFFFu) | (c1 << 16);
+      for (int u = 0; u < kPerLane; ++u) {
+        const int b = b0 + u * kHalfWarps;
+        v[u] = b < nb ? moe::ld_stream_u4(x + t * H8 + b * 16 + sub) : make_uint4(0, 0, 0, 0);
       }
-      const float scale = pow2f(e);
+      uint32_t m[kPerLane];
+#pragma unroll
+      for (int u = 0; u < kPerLane; ++u) m[u] = abs_max_bits(v[u]);
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < kPerLane; ++u) m[u] = max(m[u], __shfl_xor_sync(0xffffffffu, m[u], off));
+      uint2 q[kPerLane];
+      float scale[kPerLane];
+#pragma unroll
+      for (int u = 0; u < kPerLane; ++u) {
+        const int e = block_exponent(m[u]);
+        q[u] = quantize8(v[u], pow2f(-e));
+        scale[u] = pow2f(e);
+      }
       for (int j = 0; j < k; ++j) {
         const int32_t r = __ldg(dr + j);
         if (r < 0 || r >= n_rows) {  // -1: dropped by a fixed-capacity layout
-          if (r != -1 && sub == 0 && b == hw)
+          if (r != -1 && sub == 0 && b0 == hw)
             moe::report_error(status, MOE_ERR_DEVICE_INDEX, (int32_t)(t * k + j), moe::K_PERMUTE);
           continue;
         }
-        xq[((int64_t)r * H + b * kBlock) / 8 + sub] = make_uint2(packed[0], packed[1]);
-        if (sub == 0) xs[(int64_t)r * nb + b] = scale;
+        uint2 *dst = xq + (int64_t)r * (H / 8) + sub;
+#pragma unroll
+        for (int u = 0; u < kPerLane; ++u) {
+          const int b = b0 + u * kHalfWarps;
+          if (b < nb) {
+            dst[b * (kBlock / 8)] = q[u];
+            if (sub == 0) xs[(int64_t)r * nb + b] = scale[u];
+          }
+        }
       }
     }
   }
 }
 
-// Flat grid-stride over 16-channel chunks of the dispatched rows.  With a
-// fixed-capacity layout (masked_m != NULL) rows past a slot's used count
-// are padding and are skipped.
+// Grid-stride over 8-channel pieces of the dispatched rows: a lane loads 8
+// codes (8 bytes) and stores 8 bf16 values (one 16-byte store), so every
+// store instruction of a warp covers 512 contiguous bytes.  Each thread
+// issues kDeqPerLane loads before converting.  With a fixed-capacity layout
+// (masked_m != NULL) rows past a slot's used count are padding and skipped.
+constexpr int kDeqPerLane = 8;
+
 __global__ void __launch_bounds__(kDeqThreads) dequant_fp8_kernel(
-    const uint4 *__restrict__ xq, const float *__restrict__ xs, int64_t n_rows, int H, int cap,
+    const uint2 *__restrict__ xq, const float *__restrict__ xs, int64_t n_rows, int H, int cap,
     const int32_t *__restrict__ masked_m, uint4 *__restrict__ out) {
   moe::pdl_wait();
   moe::pdl_trigger();
-  const int per_row = H / 16;
+  const int per_row = H / 8;
   const int nb = H / kBlock;
   const int64_t total = n_rows * per_row;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int64_t row = i / per_row;
-    const int c = (int)(i - row * per_row);
-    if (masked_m != nullptr) {
-      const int64_t s = row / cap;
-      if ((int)(row - s * cap) >= __ldg(masked_m + s)) continue;
-    }
-    const uint4 q = moe::ld_stream_u4(xq + i);
-    const float scale = __ldg(xs + row * nb + c / 8);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-    uint32_t o[8];
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < total;
+       i0 += stride * kDeqPerLane) {
+    uint2 q[kDeqPerLane];
+    float scale[kDeqPerLane];
+    bool ok[kDeqPerLane];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[u] >> (16 * h)) & 0xFFFFu);
-        const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
-        __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-        o[2 * u + h] = *reinterpret_cast<uint32_t *>(&b);
+    for (int u = 0; u < kDeqPerLane; ++u) {
+      const int64_t i = i0 + u * stride;
+      const int64_t row = i / per_row;
+      ok[u] = i < total;
+      if (ok[u] && masked_m != nullptr) {
+        const int64_t s = row / cap;
+        ok[u] = (int)(row - s * cap) < __ldg(masked_m + s);
+      }
+      if (ok[u]) {
+        q[u] = __ldcs(xq + i);
+        scale[u] = __ldg(xs + row * nb + (int)(i - row * per_row) / (kBlock / 8));
       }
     }
-    out[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
-    out[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+    for (int u = 0; u < kDeqPerLane; ++u) {
+      if (!ok[u]) continue;
+      const uint32_t w[2] = {q[u].x, q[u].y};
+      uint32_t o[4];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[c] >> (16 * h)) & 0xFFFFu);
+          const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
+          __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale[u], f.y * scale[u]);
+          o[2 * c + h] = *reinterpret_cast<uint32_t *>(&b);
+        }
+      }
+      out[i0 + u * stride] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
@@ -166,12 +219,12 @@ extern "C" moe_status moe_dequant_fp8(const uint8_t *xq, const float *x_scale, i
   if (!moe_host::aligned16(xq) || !moe_host::aligned16(x_perm) ||
       (reinterpret_cast<uintptr_t>(x_scale) & 3u) != 0)
     return MOE_ERR_INVALID_ARG;
-  const int64_t chunks = n_rows * (H / 16);
-  int64_t blocks = (chunks + kDeqThreads - 1) / kDeqThreads;
+  const int64_t pieces = n_rows * (H / 8);
+  int64_t blocks = (pieces + kDeqThreads - 1) / kDeqThreads;
   const int64_t lim = (int64_t)moe_host::sm_count() * 8;
   if (blocks > lim) blocks = lim;
   return moe_host::launch_pdl(dequant_fp8_kernel, dim3((unsigned)blocks), dim3(kDeqThreads), 0,
                               static_cast<cudaStream_t>(stream),
-                              reinterpret_cast<const uint4 *>(xq), x_scale, n_rows, H,
+                              reinterpret_cast<const uint2 *>(xq), x_scale, n_rows, H,
                               masked_m ? cap : 1, masked_m, reinterpret_cast<uint4 *>(x_perm));
 }
