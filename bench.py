@@ -53,7 +53,7 @@ def load_peaks():
 # ------------------------------------------------------------------ ncu traffic
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "grouped_ffn_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "grouped_ffn_gb300", "csrc", f)
-                  for f in ("grouped_ffn.cu", "common.cuh")]
+                  for f in ("grouped_ffn.cu", "common.cuh", "tile_order.cuh")]
 
 
 def kernel_source_hash() -> str:

@@ -38,6 +38,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tile_order.cuh"
 
 namespace {
 
@@ -289,51 +290,24 @@ __device__ __forceinline__ float silu_mul(uint32_t g_bits, uint32_t u_bits) {
   return g / (1.0f + expf(-g)) * u;
 }
 
-// Tile t -> (segment, n-block, m-block).  tile_prefix[s] = m-tiles before
-// segment s; segment s owns tiles [tile_prefix[s]*NB, tile_prefix[s+1]*NB).
-__device__ __forceinline__ void decode_tile(int64_t t, const int32_t *tile_prefix, int S, int NB,
-                                            int &s, int &n_blk, int &m_blk) {
-  int lo = 0, hi = S - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((int64_t)tile_prefix[mid] * NB <= t)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  s = lo;
-  const int64_t local = t - (int64_t)tile_prefix[s] * NB;
-  const int mt = tile_prefix[s + 1] - tile_prefix[s];
-  n_blk = (int)(local / mt);
-  m_blk = (int)(local % mt);
-}
-
 // --------------------------------------------------------------- the kernel
 struct TileInfo {
   int ph, s, n_blk, m_blk;
 };
 
-// Tiles [0, T0) are phase 0, [T0, T0 + T1) phase 1.  Within a phase two
-// streams are merged in proportion to their lengths (u -> hot if
-// floor((u+1) Lh / L) > floor(u Lh / L)): the "hot" stream holds segments
-// with two or more 128-row tiles, whose weight tiles are re-read from L2 and
-// so lean on the tensor cores; the "cold" stream holds one-tile segments,
-// which stream fresh weights from HBM.  Each stream is ordered (segment,
-// n-block, m-block), so a segment's A rows and a weight tile's m-blocks stay
-// close in time, while every wave of CTAs mixes both kinds of work.
+// Tiles [0, T0) are phase 0, [T0, T0 + T1) phase 1.  Within a phase the
+// hot stream (segments with two or more m-blocks, whose weight tiles are
+// re-read from L2 and so lean on the tensor cores) and the cold stream
+// (one-block segments, which stream fresh weights from HBM) are merged in
+// proportion to their lengths, so that every wave of CTAs mixes both kinds
+// of work (tile_order.cuh).
 __device__ __forceinline__ TileInfo decode(int64_t t, int64_t T0, const int32_t *pre_h,
                                            const int32_t *pre_c, int S, int NB0, int NB1,
                                            int64_t Mh, int64_t Mc) {
   TileInfo ti;
   ti.ph = t < T0 ? 0 : 1;
   const int64_t u = ti.ph ? t - T0 : t;
-  const int NB = ti.ph ? NB1 : NB0;
-  const int64_t Lh = Mh * NB, L = (Mh + Mc) * NB;
-  const int64_t hb = u * Lh / L;
-  if ((u + 1) * Lh / L > hb)
-    decode_tile(hb, pre_h, S, NB, ti.s, ti.n_blk, ti.m_blk);
-  else
-    decode_tile(u - hb, pre_c, S, NB, ti.s, ti.n_blk, ti.m_blk);
+  tile_order::merged(u, pre_h, pre_c, S, ti.ph ? NB1 : NB0, Mh, Mc, ti.s, ti.n_blk, ti.m_blk);
   return ti;
 }
 
