@@ -123,7 +123,9 @@ def max_over_ranks(v: float, world: int) -> float:
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) during the timed region."""
+    """nvidia-smi samples every 20 ms, each stamped with the host clock when
+    read, so that the summary can keep only those taken while the GPU was
+    loaded (load() and the timed region)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -138,7 +140,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -148,7 +150,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -158,10 +160,14 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen in samples read in
+        [t0, t1] (host monotonic seconds; None = unbounded)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -283,13 +289,26 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        time.sleep(0.3)   # let the sampler start
+        time.sleep(0.2)   # let the sampler start
+        # keep the GPU loaded for at least 0.25 s right before the timed
+        # region, so that the clock samples describe a busy GPU even when
+        # the timed region itself is shorter than the sampling interval
+        t_load = time.monotonic()
+        with torch.cuda.stream(stream):
+            while time.monotonic() - t_load < 0.25:
+                for _ in range(max(1, W)):
+                    step()
+                stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
         start.record(stream)
         with torch.cuda.stream(stream):
             for i in range(K):
                 step(None if graph is not None else timed_marks(i))
         end.record(stream)
         stream.synchronize()
+        t_end = time.monotonic()
+        time.sleep(0.05)  # the last sample of the region reaches the reader
     torch.cuda.synchronize()
     barrier(world)
     ms_total = start.elapsed_time(end)
@@ -331,8 +350,10 @@ def run_ours(args, world, rank, local):
     dropped = int(layer.n_dropped.item()) if args.masked_cap else 0
     alg = algorithmic(w, seg_counts, pl.slot_expert, args.gather, kept=w.A - dropped,
                       fp8=args.fp8_dispatch)
+    clock_rec = clocks.summary(t_load, t_end + 0.03)
+    clock_rec["window_s"] = round(t_end - t_load, 3)   # loaded window the samples cover
     return finish(args, w, pl, layer, logits, x, wgu, wd, sgu, sd, names, stage_ms, ms_step,
-                  world, rank, K, W, alg, peaks, merge, e2e, dropped, clocks, dev)
+                  world, rank, K, W, alg, peaks, merge, e2e, dropped, clock_rec, dev)
 
 
 def run_merge(layer, w, y, stream, K):
@@ -428,7 +449,7 @@ def finish(args, w, pl, layer, logits, x, wgu, wd, sgu, sd, names, stage_ms, ms_
         "balancedness": float(layer.balancedness.item()),
         "dropped_assignments": dropped,
         "merge": merge,
-        "clocks": clocks.summary(),
+        "clocks": clocks,
     }
     if w.hot_experts > 0:
         out["replica_zipf_sweep"] = replica_sweep(w, dev, parse_relax(args.replica_relax) or (1, 10))
