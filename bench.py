@@ -123,9 +123,9 @@ def max_over_ranks(v: float, world: int) -> float:
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples every 20 ms, each stamped with the host clock when
-    read, so that the summary can keep only those taken while the GPU was
-    loaded (load() and the timed region)."""
+    """nvidia-smi samples every 10 ms, each stamped with the host clock when
+    read, so that the summary can keep only those taken during the timed
+    region."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -140,7 +140,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "20"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -160,14 +160,19 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self, t0=None, t1=None):
+    def summary(self, t0=None, t1=None, first=None):
         """Median SM clock and the throttle reasons seen in samples read in
-        [t0, t1] (host monotonic seconds; None = unbounded)."""
+        [t0, t1] (host monotonic seconds; None = unbounded), or in the first
+        `first` samples read after t0."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ts, ln in self.lines:
+        taken = 0
+        for ts, ln in list(self.lines):
             if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
                 continue
+            if first is not None and taken >= first:
+                break
+            taken += 1
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -290,17 +295,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         time.sleep(0.2)   # let the sampler start
-        # keep the GPU loaded for at least 0.25 s right before the timed
-        # region, so that the clock samples describe a busy GPU even when
-        # the timed region itself is shorter than the sampling interval
-        t_load = time.monotonic()
-        with torch.cuda.stream(stream):
-            while time.monotonic() - t_load < 0.25:
-                for _ in range(max(1, W)):
-                    step()
-                stream.synchronize()
         barrier(world)
         torch.cuda.synchronize()
+        t_start = time.monotonic()
         start.record(stream)
         with torch.cuda.stream(stream):
             for i in range(K):
@@ -332,6 +329,7 @@ def run_ours(args, world, rank, local):
     stage_ms = {n: float(np.mean([bd_ev[i][j].elapsed_time(bd_ev[i][j + 1]) for i in range(n_bd)]))
                 for j, n in enumerate(names)}
     stage_ms.update(ffn_ms)   # the FFN figures come from the timed region
+    iso_ms = isolated_movers(args, w, layer, x, y, stream, K)
 
     # Merge (simulated): inter-node dispatch messages before / after merge
     # and the pre-reducing combine timed like the plain one (not in the step;
@@ -350,10 +348,52 @@ def run_ours(args, world, rank, local):
     dropped = int(layer.n_dropped.item()) if args.masked_cap else 0
     alg = algorithmic(w, seg_counts, pl.slot_expert, args.gather, kept=w.A - dropped,
                       fp8=args.fp8_dispatch)
-    clock_rec = clocks.summary(t_load, t_end + 0.03)
-    clock_rec["window_s"] = round(t_end - t_load, 3)   # loaded window the samples cover
+    # samples read while the timed steps ran (one sampling interval of slack);
+    # a region shorter than the interval may hold none, then the first three
+    # read after it started stand in
+    clock_rec = clocks.summary(t_start, t_end + 0.01)
+    clock_rec["samples_in_region"] = clock_rec["samples"]
+    if clock_rec["samples"] == 0:
+        clock_rec = clocks.summary(t_start, None, first=3)
+        clock_rec["samples_in_region"] = 0
+    clock_rec["region_s"] = round(t_end - t_start, 4)
     return finish(args, w, pl, layer, logits, x, wgu, wd, sgu, sd, names, stage_ms, ms_step,
-                  world, rank, K, W, alg, peaks, merge, e2e, dropped, clock_rec, dev)
+                  world, rank, K, W, alg, peaks, merge, e2e, dropped, clock_rec, dev, iso_ms)
+
+
+def isolated_movers(args, w, layer, x, y, stream, K):
+    """Per-launch duration of the permute and combine kernels, each launch
+    timed alone between two events on its stream, with L2 flushed before
+    it by writing a buffer twice the L2 size (default step only).  The
+    in-step breakdown above also counts each kernel's launch and its wait
+    for the previous one."""
+    from grouped_ffn_gb300 import moe
+    if args.gather or args.masked_cap or args.fp8_dispatch:
+        return {}
+    A, T = w.A, w.T
+    shared = layer.shared_y[:T] if w.shared_I else None
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=y.device)
+    calls = {
+        "permute": lambda: moe.moe_permute(x, w.k, layer.dest_row[:A], layer.x_perm[:A],
+                                           layer.ws, stream),
+        "combine": lambda: moe.moe_combine(layer.y_perm[:A], layer.dest_row[:A],
+                                           layer.topk_w[:T], y, layer.ws, shared, stream),
+    }
+    out = {}
+    reps = max(3, min(K, 20))
+    for name, fn in calls.items():
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in ev:
+                flush.fill_(1)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        stream.synchronize()
+        out[name] = float(np.mean([e0.elapsed_time(e1) for e0, e1 in ev]))
+    layer.check(stream)
+    return out
 
 
 def run_merge(layer, w, y, stream, K):
@@ -381,7 +421,7 @@ def run_merge(layer, w, y, stream, K):
 
 
 def finish(args, w, pl, layer, logits, x, wgu, wd, sgu, sd, names, stage_ms, ms_step, world,
-           rank, K, W, alg, peaks, merge, e2e, dropped, clocks, dev):
+           rank, K, W, alg, peaks, merge, e2e, dropped, clocks, dev, iso_ms):
     """Stage table, roofline and the JSON record of our arm."""
     stages = {}
     for n in names:
@@ -401,6 +441,9 @@ def finish(args, w, pl, layer, logits, x, wgu, wd, sgu, sd, names, stage_ms, ms_
             bound_ms = max(a["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),
                            a["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
             s["roofline_frac"] = bound_ms / stage_ms[n]
+        if n in iso_ms:   # the kernel alone, cold L2 (see isolated_movers)
+            s["us_alone"] = iso_ms[n] * 1e3
+            s["hbm_frac_alone"] = a["bytes"] / (iso_ms[n] * 1e-3) / 1e9 / peaks["hbm_gbs"]
         stages[n] = s
     g = alg["grouped_ffn"]
     g_ms = stage_ms["grouped_ffn"]
@@ -444,8 +487,10 @@ def finish(args, w, pl, layer, logits, x, wgu, wd, sgu, sd, names, stage_ms, ms_
         "roofline": roof,
         "stages": stages,
         "gemm_pct_bf16_peak": 100.0 * stages["grouped_ffn"]["tflops"] / peaks["bf16_tflops"],
-        "permute_pct_hbm": None if args.gather else 100.0 * stages["permute"]["hbm_frac"],
-        "combine_pct_hbm": 100.0 * stages["combine"]["hbm_frac"],
+        "permute_pct_hbm": None if args.gather else 100.0 * stages["permute"].get(
+            "hbm_frac_alone", stages["permute"]["hbm_frac"]),
+        "combine_pct_hbm": 100.0 * stages["combine"].get("hbm_frac_alone",
+                                                         stages["combine"]["hbm_frac"]),
         "balancedness": float(layer.balancedness.item()),
         "dropped_assignments": dropped,
         "merge": merge,

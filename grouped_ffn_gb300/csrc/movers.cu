@@ -97,33 +97,48 @@ __global__ void __launch_bounds__(kMoverThreads) combine_kernel(
       if (threadIdx.x == 0) moe::report_error(status, MOE_ERR_DEVICE_INDEX, (int32_t)t, moe::K_COMBINE);
       continue;
     }
-    for (int c = threadIdx.x; c < H8; c += kMoverThreads) {
-      uint4 v[KMAX];
+    // U column chunks per thread and step, all their row loads issued
+    // before any arithmetic (more bytes in flight when k is small)
+    constexpr int U = KMAX <= 4 ? 4 : (KMAX <= 8 ? 2 : 1);
+    for (int c0 = threadIdx.x; c0 < H8; c0 += kMoverThreads * U) {
+      uint4 v[U][KMAX];
+      uint4 sv[U];
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if ((live >> j) & 1u) v[j] = moe::ld_stream_u4(yp + (int64_t)r[j] * H8 + c);
-      float acc[8];
-      if (shared) {
-        const uint4 s = moe::ld_stream_u4(shared + t * H8 + c);
-        const uint32_t u[4] = {s.x, s.y, s.z, s.w};
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * kMoverThreads;
+        if (c < H8) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[2 * i] = __uint_as_float(u[i] << 16);
-          acc[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+          for (int j = 0; j < KMAX; ++j)
+            if ((live >> j) & 1u) v[u][j] = moe::ld_stream_u4(yp + (int64_t)r[j] * H8 + c);
+          if (shared) sv[u] = moe::ld_stream_u4(shared + t * H8 + c);
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
       }
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if ((live >> j) & 1u) bf16x8_fma(v[j], w[j], acc);
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      y[t * H8 + c] = o;
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * kMoverThreads;
+        if (c >= H8) continue;
+        float acc[8];
+        if (shared) {
+          const uint32_t w4[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = __uint_as_float(w4[i] << 16);
+            acc[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if ((live >> j) & 1u) bf16x8_fma(v[u][j], w[j], acc);
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        y[t * H8 + c] = o;
+      }
     }
   }
 }
