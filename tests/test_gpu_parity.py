@@ -355,6 +355,80 @@ def test_grouped_ffn_small_full_compare(H, I, counts):
     assert torch.isnan(yp[A:].float()).all() and torch.isnan(h[A:].float()).all()
 
 
+def test_grouped_ffn_at_the_segment_limit():
+    """1024 segments (the limit), most empty or one row, a few long and
+    ragged, mapped onto 33 experts (segments may share an expert): the
+    device-side tile list over all of them, compared in full."""
+    m = moe()
+    S, E, H, I = 1024, 33, 256, 128
+    rng = np.random.default_rng(11)
+    counts = rng.choice([0, 0, 0, 1, 1, 2, 5], size=S)
+    counts[[3, 500, 1023]] = [300, 129, 257]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    seg_expert = ((np.arange(S) * 7) % E).astype(np.int32)
+    w = wl.Workload("segmax", 61, T=1, H=H, E=E, k=1, I=I, R=1, ranks_per_node=1)
+    A = int(offsets[-1])
+    g = torch.Generator(device="cuda").manual_seed(61)
+    xp = torch.randn(A, H, generator=g, device="cuda").to(torch.bfloat16)
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    pgu, pd = torch.empty_like(wgu), torch.empty_like(wd)
+    m.moe_pack_expert_weights(wgu, wd, pgu, pd)
+    h = torch.empty(A, I, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(A, H, dtype=torch.bfloat16, device="cuda")
+    ws = m.new_workspace(1, 1, S)
+    m.moe_grouped_ffn_packed(xp, torch.from_numpy(offsets).cuda(), torch.from_numpy(seg_expert).cuda(),
+                             pgu, pd, h, y, ws)
+    m.moe_check_device_status(ws)
+    rh, ry = oracle.grouped_ffn(f64(xp), offsets, seg_expert, oracle.bf16_bits_to_f64(bits(wgu)),
+                                oracle.bf16_bits_to_f64(bits(wd)), I)
+    assert_close(f64(h), rh, "h (1024 segments)")
+    assert_close(f64(y), ry, "y_perm (1024 segments)")
+
+
+def test_grouped_ffn_with_no_rows_launches_nothing():
+    m = moe()
+    w = wl.Workload("ffn0", 62, T=1, H=256, E=2, k=1, I=128, R=1, ranks_per_node=1)
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    h = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    xp = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    ws = m.new_workspace(1, 1, 2)
+    offs = torch.zeros(3, dtype=torch.int32, device="cuda")
+    m.moe_grouped_ffn(xp, offs, torch.zeros(2, dtype=torch.int32, device="cuda"), wgu, wd, h, y, ws)
+    m.moe_check_device_status(ws)
+
+
+def test_grouped_ffn_reports_a_bad_expert_and_computes_the_rest():
+    """A non-empty segment whose expert id is out of range is reported
+    (MOE_ERR_DEVICE_INDEX) and skipped, without a fault; the other segments'
+    rows are still right."""
+    m = moe()
+    H, I, E = 256, 128, 3
+    counts = [40, 25, 130]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    A = int(offsets[-1])
+    w = wl.Workload("ffnbad", 63, T=1, H=H, E=E, k=1, I=I, R=1, ranks_per_node=1)
+    g = torch.Generator(device="cuda").manual_seed(63)
+    xp = torch.randn(A, H, generator=g, device="cuda").to(torch.bfloat16)
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    h = torch.full((A, I), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y = torch.full((A, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    seg_expert = np.array([2, 7, 0], np.int32)          # segment 1 names expert 7 of 3
+    ws = m.new_workspace(1, 1, 3)
+    m.moe_grouped_ffn(xp, torch.from_numpy(offsets).cuda(), torch.from_numpy(seg_expert).cuda(),
+                      wgu, wd, h, y, ws)
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_check_device_status(ws)
+    assert ei.value.status == 4
+    good = np.r_[0:40, 65:195]
+    ok_exp = np.array([2, 0, 0], np.int32)             # any valid id for the skipped segment
+    rh, ry = oracle.grouped_ffn(f64(xp), offsets, ok_exp, oracle.bf16_bits_to_f64(bits(wgu)),
+                                oracle.bf16_bits_to_f64(bits(wd)), I)
+    gt = torch.from_numpy(good).cuda()
+    assert_close(f64(y[gt]), ry[good], "y_perm of the valid segments")
+    assert torch.isnan(y[40:65].float()).all()         # the bad segment is left unwritten
+
+
 @pytest.mark.parametrize("H,I,counts", [(256, 128, [3, 0, 5, 8]),
                                          (512, 384, [130, 1, 0, 257, 128, 75, 300, 12])])
 def test_packed_ffn_is_bit_identical_to_plain(H, I, counts):
