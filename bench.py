@@ -192,13 +192,16 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ algorithmic work
 def algorithmic(w: wl.Workload, seg_counts: np.ndarray, slot_expert: np.ndarray,
-                gather: bool = False, kept: int = None, fp8: bool = False):
+                gather: bool = False, kept: int = None, fp8: bool = False,
+                fused_shared: bool = False):
     """Bytes / flops per step by stage (the per-unit figures times the units).
     With the gather-fused FFN the rows come from x (2H bytes per token)
     instead of the permuted copy (2H per assignment).  kept: assignments
     that run (fewer than T*k when a fixed capacity drops some).  fp8: the
     dispatched rows carry H E4M3 bytes plus one fp32 scale per 128
-    channels, restored to bf16 by a separate pass."""
+    channels, restored to bf16 by a separate pass.  fused_shared: the shared
+    expert runs in the routed FFN's launch, so its work counts there, and
+    the permute writes its T extra rows."""
     A, T, H, I = w.A, w.T, w.H, w.I
     K = A if kept is None else kept
     active_slots = seg_counts > 0
@@ -218,8 +221,15 @@ def algorithmic(w: wl.Workload, seg_counts: np.ndarray, slot_expert: np.ndarray,
     if fp8:
         st["dequant"] = dict(bytes=K * wire + K * H * 2)
     if w.shared_I:
-        st["shared_ffn"] = dict(bytes=6 * H * w.shared_I + T * H * 2 * 2 + T * w.shared_I * 4,
-                                flops=6 * T * H * w.shared_I, weight_bytes=6 * H * w.shared_I)
+        sh = dict(bytes=6 * H * w.shared_I + T * H * 2 * 2 + T * w.shared_I * 4,
+                  flops=6 * T * H * w.shared_I, weight_bytes=6 * H * w.shared_I)
+        if fused_shared:
+            g = st["grouped_ffn"]
+            for key in ("bytes", "flops", "weight_bytes"):
+                g[key] += sh[key]
+            st["permute"]["bytes"] += T * H * 2
+        else:
+            st["shared_ffn"] = sh
     return st
 
 
@@ -241,14 +251,15 @@ def run_ours(args, world, rank, local):
                      shared_w_gate_up=sgu, shared_w_down=sd, device=dev,
                      packed=not args.unpacked, replica_relax=parse_relax(args.replica_relax),
                      gather=args.gather, masked_cap=args.masked_cap or None,
-                     fp8_dispatch=args.fp8_dispatch)
+                     fp8_dispatch=args.fp8_dispatch, fuse_shared=not args.no_fuse_shared)
     y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
+    shared_stage = bool(w.shared_I) and not layer.fuse_shared   # a launch of its own
     names = ["route", "layout", "permute"] + (["dequant"] if args.fp8_dispatch else []) + \
-        ["grouped_ffn"] + (["shared_ffn"] if w.shared_I else []) + ["combine", "balance"]
+        ["grouped_ffn"] + (["shared_ffn"] if shared_stage else []) + ["combine", "balance"]
     ffn_start = "dequant" if args.fp8_dispatch else "permute"
-    ffn_stages = ["grouped_ffn"] + (["shared_ffn"] if w.shared_I else [])
+    ffn_stages = ["grouped_ffn"] + (["shared_ffn"] if shared_stage else [])
     K, W = args.steps, args.warmup
     ET = lambda: torch.cuda.Event(enable_timing=True)
 
@@ -281,12 +292,12 @@ def run_ours(args, world, rank, local):
     def timed_marks(i):
         evs = ffn_ev[i]
         slot = {ffn_start: 0, "grouped_ffn": 1}
-        if w.shared_I:
+        if shared_stage:
             slot.update({"grouped_ffn": 1, "shared_ffn": 3})
         def mark(name):
             if name in slot:
                 evs[slot[name]].record(stream)
-                if name == "grouped_ffn" and w.shared_I:
+                if name == "grouped_ffn" and shared_stage:
                     evs[2].record(stream)
         return mark
 
@@ -347,7 +358,7 @@ def run_ours(args, world, rank, local):
     seg_counts = layer.seg_counts.cpu().numpy()
     dropped = int(layer.n_dropped.item()) if args.masked_cap else 0
     alg = algorithmic(w, seg_counts, pl.slot_expert, args.gather, kept=w.A - dropped,
-                      fp8=args.fp8_dispatch)
+                      fp8=args.fp8_dispatch, fused_shared=layer.fuse_shared)
     # samples read while the timed steps ran (one sampling interval of slack);
     # a region shorter than the interval may hold none, then the first three
     # read after it started stand in
@@ -371,11 +382,16 @@ def isolated_movers(args, w, layer, x, y, stream, K):
     if args.gather or args.masked_cap or args.fp8_dispatch:
         return {}
     A, T = w.A, w.T
-    shared = layer.shared_y[:T] if w.shared_I else None
+    shared = layer.shared_output(T)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=y.device)
+    if layer.fuse_shared:   # the step's permute also writes the shared expert's rows
+        perm = lambda: moe.moe_permute_shared(x, w.k, layer.dest_row[:A], layer.x_perm[:A + T],
+                                              layer.ws, stream)
+    else:
+        perm = lambda: moe.moe_permute(x, w.k, layer.dest_row[:A], layer.x_perm[:A],
+                                       layer.ws, stream)
     calls = {
-        "permute": lambda: moe.moe_permute(x, w.k, layer.dest_row[:A], layer.x_perm[:A],
-                                           layer.ws, stream),
+        "permute": perm,
         "combine": lambda: moe.moe_combine(layer.y_perm[:A], layer.dest_row[:A],
                                            layer.topk_w[:T], y, layer.ws, shared, stream),
     }
@@ -402,7 +418,7 @@ def run_merge(layer, w, y, stream, K):
     dev = y.device
     msgs = torch.zeros(2, dtype=torch.int32, device=dev)
     y_m = torch.empty_like(y)
-    shared_arg = layer.shared_y[:w.T] if w.shared_I else None
+    shared_arg = layer.shared_output(w.T)
     mev = [ET() for _ in range(2)]
     with torch.cuda.stream(stream):
         for i in range(3 + K):
@@ -479,6 +495,9 @@ def finish(args, w, pl, layer, logits, x, wgu, wd, sgu, sd, names, stage_ms, ms_
                                 if args.fp8_dispatch else "permute"),
                    "layout": ("fixed capacity %d rows per slot" % args.masked_cap)
                              if args.masked_cap else "contiguous",
+                   "shared_expert": None if not w.shared_I else
+                                    ("in the routed FFN launch" if layer.fuse_shared
+                                     else "second FFN launch"),
                    "launch": "cuda-graph replay" if args.graph else "stream (PDL)",
                    "l2": "inputs larger than L2: %.2f GB of expert weights stream per step"
                          % (g["weight_bytes"] / 1e9)},
@@ -750,6 +769,8 @@ def main():
                     help="fixed-capacity layout with this many rows per slot (0: contiguous)")
     ap.add_argument("--fp8-dispatch", action="store_true",
                     help="dispatch E4M3 codes + block scales, restore bf16 before the FFN")
+    ap.add_argument("--no-fuse-shared", action="store_true",
+                    help="run the shared expert as a second FFN launch")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count")
     args = ap.parse_args()

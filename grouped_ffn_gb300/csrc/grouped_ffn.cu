@@ -103,6 +103,11 @@ struct FfnParams {
   // (seg_offsets unused) when masked_m is set.
   const int32_t *masked_m;
   int32_t cap;
+  // Segments [0, n_listed) come from seg_offsets / masked_m; when S is one
+  // more, segment n_listed is rows [extra_lo, extra_hi) with expert
+  // extra_expert (a shared expert run in the same launch).
+  int32_t n_listed;
+  int32_t extra_lo, extra_hi, extra_expert;
   int32_t *status;
   Phase ph[2];
 };
@@ -373,8 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   for (int s = threadIdx.x; s < p.S; s += kThreads) {
-    int lo, hi;
-    if (p.masked_m != nullptr) {
+    int lo, hi, e;
+    if (s >= p.n_listed) {
+      lo = p.extra_lo;
+      hi = p.extra_hi;
+      e = p.extra_expert;
+    } else if (p.masked_m != nullptr) {
       int m = p.masked_m[s];
       if (m < 0 || m > p.cap) {
         moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, s, kid);
@@ -382,12 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       lo = s * p.cap;
       hi = lo + m;
+      e = p.seg_expert[s];
     } else {
       lo = p.seg_offsets[s];
       hi = p.seg_offsets[s + 1];
+      e = p.seg_expert[s];
     }
     hi = min(hi, p.n_rows);
-    const int e = p.seg_expert[s];
     seg_off[s] = lo;
     seg_end[s] = hi;
     seg_exp[s] = e;
@@ -756,7 +766,11 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
                    const uint16_t *w_down, int32_t H, int32_t I, uint16_t *h, uint16_t *y_perm,
                    void *ws, size_t ws_bytes, void *stream, bool packed,
                    const int32_t *gather_src = nullptr, int32_t gather_k = 1,
-                   int64_t gather_T = 0, const int32_t *masked_m = nullptr, int32_t cap = 0) {
+                   int64_t gather_T = 0, const int32_t *masked_m = nullptr, int32_t cap = 0,
+                   int64_t extra_lo = 0, int64_t extra_rows = 0, int32_t extra_expert = 0) {
+  // an extra segment (a shared expert) is appended after the S listed ones
+  const int32_t S_listed = S;
+  if (extra_rows > 0) S = S + 1;
   if (moe_status s = check_ffn_args(x_perm, n_rows, masked_m ? masked_m : seg_offsets, seg_expert,
                                     S, E, w_gate_up, w_down, H, I, h, y_perm, ws, ws_bytes))
     return s;
@@ -785,6 +799,10 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   p.seg_offsets = seg_offsets;
   p.seg_expert = seg_expert;
   p.S = S;
+  p.n_listed = S_listed;
+  p.extra_lo = (int32_t)extra_lo;
+  p.extra_hi = (int32_t)(extra_lo + extra_rows);
+  p.extra_expert = extra_expert;
   p.E = E;
   p.n_rows = (int32_t)n_rows;
   p.b_packed = packed ? 1 : 0;
@@ -839,6 +857,19 @@ extern "C" moe_status moe_grouped_ffn_packed(const uint16_t *x_perm, int64_t n_r
                                              size_t ws_bytes, void *stream) {
   return run_ffn(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up_packed, w_down_packed, H,
                  I, h, y_perm, ws, ws_bytes, stream, true);
+}
+
+extern "C" moe_status moe_grouped_ffn_packed_shared(
+    const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_offsets, const int32_t *seg_expert,
+    int32_t S, int32_t E, const uint16_t *w_gate_up_packed, const uint16_t *w_down_packed, int32_t H,
+    int32_t I, int64_t shared_row0, int64_t shared_rows, int32_t shared_expert, uint16_t *h,
+    uint16_t *y_perm, void *ws, size_t ws_bytes, void *stream) {
+  if (shared_row0 < 0 || shared_rows < 0 || shared_row0 + shared_rows > n_rows)
+    return MOE_ERR_INVALID_ARG;
+  if (shared_rows > 0 && (shared_expert < 0 || shared_expert >= E)) return MOE_ERR_INVALID_ARG;
+  return run_ffn(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up_packed, w_down_packed, H,
+                 I, h, y_perm, ws, ws_bytes, stream, true, nullptr, 1, 0, nullptr, 0, shared_row0,
+                 shared_rows, shared_expert);
 }
 
 extern "C" moe_status moe_grouped_ffn_gather(const uint16_t *x, int64_t T, int32_t k,

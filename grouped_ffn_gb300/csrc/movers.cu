@@ -20,10 +20,12 @@ namespace {
 constexpr int kMoverThreads = 128;
 constexpr int kUnroll = 4;
 
-template <bool DROP>
+// EXTRA: token t is also copied to row extra_row0 + t (the rows a shared
+// expert runs on inside the same grouped FFN launch).
+template <bool DROP, bool EXTRA>
 __global__ void __launch_bounds__(kMoverThreads) permute_kernel(
     const uint4 *__restrict__ x, int64_t T, int H8, int k, const int32_t *__restrict__ dest_row,
-    uint4 *__restrict__ xp, int64_t A, int32_t *status) {
+    uint4 *__restrict__ xp, int64_t A, int64_t extra_row0, int32_t *status) {
   moe::pdl_wait();
   moe::pdl_trigger();
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
@@ -44,6 +46,14 @@ __global__ void __launch_bounds__(kMoverThreads) permute_kernel(
           continue;
         }
         uint4 *dst = xp + (int64_t)r * H8;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int c = c0 + u * kMoverThreads;
+          if (c < H8) dst[c] = v[u];
+        }
+      }
+      if (EXTRA) {
+        uint4 *dst = xp + (extra_row0 + t) * H8;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int c = c0 + u * kMoverThreads;
@@ -293,10 +303,12 @@ unsigned mover_grid(int64_t T) {
 
 namespace {
 
-// n_rows: rows of x_perm; allow_drop: dest_row -1 marks a dropped assignment.
+// n_rows: rows of x_perm that assignments may land on; allow_drop: dest_row
+// -1 marks a dropped assignment; extra_row0 >= 0: also copy token t to row
+// extra_row0 + t.
 moe_status run_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
                        const int32_t *dest_row, int64_t n_rows, uint16_t *x_perm, int allow_drop,
-                       void *ws, size_t ws_bytes, void *stream) {
+                       void *ws, size_t ws_bytes, void *stream, int64_t extra_row0 = -1) {
   if (T < 0 || H < 1 || k < 1 || n_rows < 0) return MOE_ERR_INVALID_ARG;
   if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
@@ -304,10 +316,13 @@ moe_status run_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
   if (!moe_host::aligned16(x) || !moe_host::aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
   if (moe_status s = moe_host::check_ws(ws, ws_bytes, moe::kStatusBytes)) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return moe_host::launch_pdl(allow_drop ? permute_kernel<true> : permute_kernel<false>,
+  return moe_host::launch_pdl(extra_row0 >= 0 ? permute_kernel<false, true>
+                              : allow_drop   ? permute_kernel<true, false>
+                                             : permute_kernel<false, false>,
                               dim3(mover_grid(T)), dim3(kMoverThreads), 0, st,
                               reinterpret_cast<const uint4 *>(x), T, H / 8, k, dest_row,
-                              reinterpret_cast<uint4 *>(x_perm), n_rows, moe_host::status_ptr(ws));
+                              reinterpret_cast<uint4 *>(x_perm), n_rows, extra_row0,
+                              moe_host::status_ptr(ws));
 }
 
 moe_status run_combine(const uint16_t *y_perm, int64_t n_rows, const int32_t *dest_row,
@@ -347,6 +362,14 @@ extern "C" moe_status moe_permute(const uint16_t *x, int64_t T, int32_t H, int32
                                   size_t ws_bytes, void *stream) {
   if (T < 0 || k < 1) return MOE_ERR_INVALID_ARG;
   return run_permute(x, T, H, k, dest_row, T * (int64_t)k, x_perm, 0, ws, ws_bytes, stream);
+}
+
+extern "C" moe_status moe_permute_shared(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                                         const int32_t *dest_row, uint16_t *x_perm, void *ws,
+                                         size_t ws_bytes, void *stream) {
+  if (T < 0 || k < 1) return MOE_ERR_INVALID_ARG;
+  const int64_t A = T * (int64_t)k;
+  return run_permute(x, T, H, k, dest_row, A, x_perm, 0, ws, ws_bytes, stream, A);
 }
 
 extern "C" moe_status moe_permute_masked(const uint16_t *x, int64_t T, int32_t H, int32_t k,

@@ -26,7 +26,7 @@ class MoELayer:
                  shared_w_down: Optional[torch.Tensor] = None, device="cuda",
                  packed: bool = True, replica_relax: Optional[tuple] = None,
                  gather: bool = False, masked_cap: Optional[int] = None,
-                 fp8_dispatch: bool = False):
+                 fp8_dispatch: bool = False, fuse_shared: bool = True):
         """replica_relax=(c_num, c_den) chooses each assignment's replica by
         locality-preferred water-filling with load bounds C = c_num/c_den
         (moe_route_replicas); None keeps the fixed replica rule.
@@ -36,7 +36,11 @@ class MoELayer:
         every slot owns c rows, assignments beyond them are dropped.
         fp8_dispatch=True moves E4M3 codes and block scales through the
         dispatched buffer (moe_permute_fp8) and restores bf16 rows before
-        the FFN (moe_dequant_fp8)."""
+        the FFN (moe_dequant_fp8).
+        fuse_shared=True runs a shared expert of the routed experts' width
+        inside the routed experts' FFN launch (moe_permute_shared +
+        moe_grouped_ffn_packed_shared) in the plain contiguous bf16 step;
+        otherwise it is a second launch.  The results are the same bits."""
         if (gather or masked_cap is not None) and not packed:
             raise ValueError("gather and fixed-capacity modes stream packed weights")
         if gather and (masked_cap is not None or fp8_dispatch):
@@ -49,7 +53,21 @@ class MoELayer:
         self.H, self.I, self.E, self.k = H, I, E, k
         self.placement = placement
         self.packed = packed
-        if packed:
+        self.fuse_shared = bool(
+            fuse_shared and shared_w_gate_up is not None and packed and not gather
+            and masked_cap is None and not fp8_dispatch
+            and tuple(shared_w_gate_up.shape[1:]) == (2 * I, H))
+        if self.fuse_shared:
+            # one packed tensor holds the routed experts and, as expert E,
+            # the shared one, so that one launch serves both
+            gu = torch.empty((E + 1, 2 * I, H), dtype=w_gate_up.dtype, device=w_gate_up.device)
+            dn = torch.empty((E + 1, H, I), dtype=w_down.dtype, device=w_down.device)
+            moe.moe_pack_expert_weights(w_gate_up, w_down, gu[:E], dn[:E])
+            moe.moe_pack_expert_weights(shared_w_gate_up, shared_w_down, gu[E:], dn[E:])
+            w_gate_up, w_down = gu, dn
+            shared_w_gate_up = shared_w_down = None
+            self.shared_I = I
+        elif packed:
             # one-time rearrangement into the tile-contiguous layout the FFN
             # kernel streams best (each TMA box is one contiguous block)
             w_gate_up, w_down = self._pack(w_gate_up, w_down)
@@ -66,8 +84,11 @@ class MoELayer:
         bf = dict(dtype=torch.bfloat16, device=dev)
         self.topk_ids = torch.empty(max_tokens, k, **i32)
         self.topk_w = torch.empty(max_tokens, k, dtype=torch.float32, device=dev)
-        # dispatched rows: T*k in the contiguous layout, S*cap in the fixed one
+        # dispatched rows: T*k in the contiguous layout (+ T for a fused
+        # shared expert), S*cap in the fixed one
         rows = A if masked_cap is None else S * masked_cap
+        if self.fuse_shared:
+            rows = A + max_tokens
         self.slot = torch.empty(A, **i32)
         self.seg_counts = torch.empty(S, **i32)
         self.seg_offsets = torch.empty(S + 1, **i32)
@@ -88,7 +109,9 @@ class MoELayer:
         self.ws = moe.new_workspace(max_tokens, k, S, device=dev, n_experts=E, n_ranks=R)
         self.replica_relax = replica_relax
         self.inter_node = torch.zeros(1, **i32)
-        if shared_w_gate_up is not None:
+        if self.fuse_shared:
+            pass
+        elif shared_w_gate_up is not None:
             self.shared_I = shared_w_gate_up.shape[1] // 2
             self.shared_h = torch.empty(max_tokens, self.shared_I, **bf)
             self.shared_y = torch.empty(max_tokens, H, **bf)
@@ -154,12 +177,22 @@ class MoELayer:
             moe.moe_grouped_ffn_gather(x, self.k, self.src_assign[:A], self.seg_offsets,
                                        self.placement.slot_expert, self.w_gate_up, self.w_down,
                                        self.h[:A], self.y_perm[:A], self.ws, stream)
+        elif self.fuse_shared:
+            # rows [A, A + T) carry the tokens once more for the shared
+            # expert (expert E of the packed weights), in the same launch
+            moe.moe_permute_shared(x, self.k, self.dest_row[:A], self.x_perm[:A + T], self.ws,
+                                   stream)
+            mark("permute")
+            moe.moe_grouped_ffn_packed_shared(self.x_perm[:A + T], self.seg_offsets,
+                                              self.placement.slot_expert, self.w_gate_up,
+                                              self.w_down, A, T, self.E, self.h[:A + T],
+                                              self.y_perm[:A + T], self.ws, stream)
         else:
             self._dispatch(x, A, A, None, stream, mark)
             self._ffn(self.x_perm[:A], self.seg_offsets, self.placement.slot_expert,
                       self.w_gate_up, self.w_down, self.h[:A], self.y_perm[:A], self.ws, stream)
         mark("grouped_ffn")
-        shared = self._shared(x, T, stream, mark)
+        shared = self.shared_output(T) if self.fuse_shared else self._shared(x, T, stream, mark)
         moe.moe_combine(self.y_perm[:A], self.dest_row[:A], w, y, self.ws, shared, stream)
         mark("combine")
         self._balance(stream, mark)
@@ -189,6 +222,14 @@ class MoELayer:
                   self.shared_w_down, self.shared_h[:T], self.shared_y[:T], self.ws, stream)
         mark("shared_ffn")
         return self.shared_y[:T]
+
+    def shared_output(self, T: int):
+        """The shared expert's output rows [T, H] of the last step, or None
+        when the layer has no shared expert."""
+        if self.fuse_shared:
+            A = T * self.k
+            return self.y_perm[A:A + T]
+        return self.shared_y[:T] if self.shared_I else None
 
     def _balance(self, stream, mark):
         moe.moe_balance_stats(self.rank_counts, self.balancedness, self.max_count, self.total,

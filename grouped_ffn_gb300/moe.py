@@ -92,6 +92,10 @@ _SIGNATURES = {
                                           _P]),
     "moe_permute_fp8": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _SZ, _P]),
     "moe_dequant_fp8": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "moe_permute_shared": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_ffn_packed_shared": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _I32,
+                                                     _I32, _I64, _I64, _I32, _P, _P, _P, _SZ,
+                                                     _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_version": (ctypes.c_char_p, []),
 }
@@ -401,6 +405,42 @@ def moe_balance_stats(rank_counts, balancedness, max_count, total, ws=None, stre
     _check("moe_balance_stats", lib().moe_balance_stats(
         _ptr(rank_counts), rank_counts.numel(), _ptr(balancedness), _ptr(max_count), _ptr(total),
         _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+# ------------------------------------------------------------------ shared expert in the routed launch
+def moe_permute_shared(x, k: int, dest_row, x_perm, ws, stream=None):
+    """moe_permute plus a copy of every token row t at row T*k + t
+    (x_perm has T*k + T rows)."""
+    _bf16(x, "x")
+    _bf16(x_perm, "x_perm")
+    _need(dest_row, torch.int32, "dest_row")
+    T, H = x.shape
+    if x_perm.shape[0] < T * k + T:
+        raise ValueError("moe_permute_shared: x_perm needs T*k + T rows")
+    _check("moe_permute_shared", lib().moe_permute_shared(
+        _ptr(x), T, H, k, _ptr(dest_row), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_grouped_ffn_packed_shared(x_perm, seg_offsets, seg_expert, w_gate_up_packed,
+                                  w_down_packed, shared_row0: int, shared_rows: int,
+                                  shared_expert: int, h, y_perm, ws, stream=None):
+    """moe_grouped_ffn_packed plus one segment [shared_row0, shared_row0 +
+    shared_rows) run with expert shared_expert in the same launch."""
+    for n, t in (("x_perm", x_perm), ("w_gate_up_packed", w_gate_up_packed),
+                 ("w_down_packed", w_down_packed), ("h", h), ("y_perm", y_perm)):
+        _bf16(t, n)
+    _need(seg_offsets, torch.int32, "seg_offsets")
+    _need(seg_expert, torch.int32, "seg_expert")
+    n_rows, H = x_perm.shape
+    E, two_i, H2 = w_gate_up_packed.shape
+    I = two_i // 2
+    if H2 != H or tuple(w_down_packed.shape) != (E, H, I) or tuple(h.shape) != (n_rows, I) \
+            or tuple(y_perm.shape) != (n_rows, H):
+        raise ValueError("moe_grouped_ffn_packed_shared: inconsistent shapes")
+    _check("moe_grouped_ffn_packed_shared", lib().moe_grouped_ffn_packed_shared(
+        _ptr(x_perm), n_rows, _ptr(seg_offsets), _ptr(seg_expert), seg_expert.numel(), E,
+        _ptr(w_gate_up_packed), _ptr(w_down_packed), H, I, shared_row0, shared_rows,
+        shared_expert, _ptr(h), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 # ------------------------------------------------------------------ fixed-capacity layout

@@ -275,6 +275,17 @@ moe_status moe_permute(const uint16_t *x, int64_t T, int32_t H, int32_t k,
                        const int32_t *dest_row, uint16_t *x_perm, void *ws,
                        size_t ws_bytes, void *stream);
 
+/* moe_permute that also copies every token row t to row T*k + t, so that a
+ * shared expert can run on those T rows inside the same grouped FFN launch
+ * (moe_grouped_ffn_packed_shared).  "Mixture-of-Experts Inference", "MoE
+ * architecture recap" (the shared expert processes every token) and
+ * "Communication pressure" (shared-expert work is independent of the
+ * routed path until the outputs are merged, so it can overlap with it).
+ *  x_perm device bf16 [T*k + T, H].  Limits as moe_permute. */
+moe_status moe_permute_shared(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                              const int32_t *dest_row, uint16_t *x_perm, void *ws,
+                              size_t ws_bytes, void *stream);
+
 /* moe_permute into a buffer of n_rows rows (a fixed-capacity layout:
  * n_rows = S*cap) where dest_row -1 marks a dropped assignment, which moves
  * nothing.  Other out-of-range rows are skipped and reported as
@@ -378,6 +389,22 @@ moe_status moe_grouped_ffn_packed(const uint16_t *x_perm, int64_t n_rows,
                                   const uint16_t *w_down_packed, int32_t H, int32_t I,
                                   uint16_t *h, uint16_t *y_perm, void *ws, size_t ws_bytes,
                                   void *stream);
+
+/* moe_grouped_ffn_packed with one more segment after the S listed ones:
+ * rows [shared_row0, shared_row0 + shared_rows) of x_perm with expert
+ * shared_expert of the packed weights.  This runs a shared expert in the
+ * routed experts' launch, so that its tensor-bound tiles overlap the
+ * routed experts' weight streaming instead of following them.  Per row the
+ * arithmetic is that of a separate call: the results are bit-identical.
+ *  Requires 0 <= shared_row0, shared_row0 + shared_rows <= n_rows,
+ *  0 <= shared_expert < E, S + 1 <= 1024; ws: 256 + 4*(S+1) bytes. */
+moe_status moe_grouped_ffn_packed_shared(const uint16_t *x_perm, int64_t n_rows,
+                                         const int32_t *seg_offsets, const int32_t *seg_expert,
+                                         int32_t S, int32_t E, const uint16_t *w_gate_up_packed,
+                                         const uint16_t *w_down_packed, int32_t H, int32_t I,
+                                         int64_t shared_row0, int64_t shared_rows,
+                                         int32_t shared_expert, uint16_t *h, uint16_t *y_perm,
+                                         void *ws, size_t ws_bytes, void *stream);
 
 /* moe_grouped_ffn_packed without the permuted copy: dispatched row r of
  * the gate/up GEMM is read straight from token row src_assign[r] / k of x

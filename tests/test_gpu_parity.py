@@ -528,7 +528,8 @@ def test_full_layer_sampled(name):
     assert_close(f64(layer.h[torch.from_numpy(rows).cuda()]), rh, "h rows")
     assert_close(f64(layer.y_perm[torch.from_numpy(rows).cuda()]), ry, "y_perm rows")
     # combine bit-exact from the GPU's own expert outputs
-    shared_bits = bits(layer.shared_y[: w.T]) if w.shared_I else None
+    shared_out = layer.shared_output(w.T)
+    shared_bits = bits(shared_out) if shared_out is not None else None
     ref_y = oracle.combine_fma32(bits(layer.y_perm[:A]), lay["dest_row"],
                                  layer.topk_w[: w.T].cpu().numpy(), shared_bits)
     assert np.array_equal(bits(y), ref_y)
@@ -556,6 +557,69 @@ class _BitsExperts:
         if e not in self.cache:
             self.cache[e] = bits(self.t[e])
         return self.cache[e]
+
+
+def test_shared_expert_in_the_routed_launch():
+    """moe_permute_shared copies every token once more after the dispatched
+    rows, and moe_grouped_ffn_packed_shared runs the shared expert on those
+    rows in the routed experts' launch: the copied rows are bit-exact, the
+    shared rows match the dense definition, and the routed rows are the
+    bits of a launch without the extra segment."""
+    m = moe()
+    T, k, H, I, E = 300, 2, 512, 256, 5
+    w = wl.Workload("shfused", 64, T=T, H=H, E=E + 1, k=k, I=I, R=1, ranks_per_node=1)
+    A = T * k
+    g = torch.Generator(device="cuda").manual_seed(64)
+    x = torch.randn(T, H, generator=g, device="cuda").to(torch.bfloat16)
+    dest = torch.randperm(A, generator=g, device="cuda").to(torch.int32)
+    counts = [130, 0, 257, 1, 212]
+    offs = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32, device="cuda")
+    se = torch.tensor([4, 0, 2, 1, 3], dtype=torch.int32, device="cuda")
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")   # expert E is the shared one
+    pgu, pd = torch.empty_like(wgu), torch.empty_like(wd)
+    m.moe_pack_expert_weights(wgu, wd, pgu, pd)
+    ws = m.new_workspace(T, k, len(counts) + 1)
+    xp = torch.empty(A + T, H, dtype=torch.bfloat16, device="cuda")
+    m.moe_permute_shared(x, k, dest, xp, ws)
+    m.moe_check_device_status(ws)
+    xb = bits(x)
+    assert np.array_equal(bits(xp[:A]), oracle.permute(xb, dest.cpu().numpy(), k))
+    assert np.array_equal(bits(xp[A:]), xb)
+    h = torch.empty(A + T, I, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(A + T, H, dtype=torch.bfloat16, device="cuda")
+    m.moe_grouped_ffn_packed_shared(xp, offs, se, pgu, pd, A, T, E, h, y, ws)
+    m.moe_check_device_status(ws)
+    _, ry = oracle.swiglu_expert(f64(x), f64(wgu[E]), f64(wd[E]), I)
+    assert_close(f64(y[A:]), ry, "shared expert rows")
+    h2 = torch.empty(A, I, dtype=torch.bfloat16, device="cuda")
+    y2 = torch.empty(A, H, dtype=torch.bfloat16, device="cuda")
+    m.moe_grouped_ffn_packed(xp[:A].contiguous(), offs, se, pgu, pd, h2, y2, ws)
+    m.moe_check_device_status(ws)
+    assert torch.equal(h[:A], h2) and torch.equal(y[:A], y2)
+
+
+def test_fused_shared_layer_is_bit_identical_to_two_launches():
+    from grouped_ffn_gb300 import MoELayer
+    m = moe()
+    w = wl.WORKLOADS["group_limited"].scaled(T=512, E=64, R=16, H=1024, I=256, shared_I=256)
+    pl = wl.make_placement(w)
+    logits, x = wl.make_logits(w, "cuda"), wl.make_x(w, "cuda")
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    sgu, sd = wl.make_shared_weights(w, "cuda")
+    outs = []
+    for fuse in (True, False):
+        layer = MoELayer(H=w.H, I=w.I, E=w.E, k=w.k, placement=m.DevicePlacement.from_tables(pl),
+                         w_gate_up=wgu, w_down=wd, max_tokens=w.T, score_fn=w.score_fn,
+                         n_groups=w.n_groups, topk_groups=w.topk_groups, group_topn=w.group_topn,
+                         shared_w_gate_up=sgu, shared_w_down=sd, fuse_shared=fuse)
+        assert layer.fuse_shared == fuse
+        y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+        layer.forward(logits, x, y)
+        layer.check()
+        outs.append((y, layer.shared_output(w.T).clone(), layer.launches_per_step))
+        del layer
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert outs[0][2] == outs[1][2] - 1
 
 
 def test_shared_expert_alone_matches_dense_definition():
