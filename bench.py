@@ -621,6 +621,28 @@ def _bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model as /proc/cpuinfo names it (x86 'model name'; Arm
+    cores report implementer and part codes instead)."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key = key.strip()
+                if key in ("model name", "CPU implementer", "CPU part") and key not in fields:
+                    fields[key] = val.strip()
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return "%s, implementer %s part %s" % (platform.machine(), fields.get("CPU implementer", "?"),
+                                               fields["CPU part"])
+    return platform.machine()
+
+
 def oracle_sample_step(w, pl, logits_np, x_bits, experts_gu, experts_d, shared, tokens):
     """The oracle's stage-wise path on a sample of tokens: route, layout,
     permute, grouped FFN, combine, balancedness."""
@@ -687,6 +709,7 @@ def cpu_baseline(w, pl, logits, x, wgu, wd, sgu, sd, seconds):
         done_tokens += len(toks)
         n *= 2
     return {"value": done_tokens / t_used, "unit": "tokens/s", "cores": os.cpu_count(),
+            "cpu_model": host_cpu_model(),
             "kind": "oracle",
             "sample": f"{done_tokens} of {w.T} tokens of the {w.name} layer through the oracle's "
                       f"stage-wise path (route, layout, permute, grouped FFN, combine, balance) "
@@ -740,6 +763,7 @@ def run_reference(args, world, rank):
                        "top_k": w.k, "ffn_intermediate": w.I, "zipf_s": w.zipf_s,
                        "parallelism": "replicas1", "sampled_tokens_per_step": n_tok},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+                             "cpu_model": host_cpu_model(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
