@@ -377,6 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  // the next kernel on the stream (the combine) may start launching now; it
+  // waits (griddepcontrol.wait) until this grid has finished
+  moe::pdl_trigger();
   for (int s = threadIdx.x; s < p.S; s += kThreads) {
     int lo, hi, e;
     if (s >= p.n_listed) {
