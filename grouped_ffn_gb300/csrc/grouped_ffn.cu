@@ -177,6 +177,30 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// A tiled load with an L2 eviction-priority hint (a createpolicy value).
+__device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *m, int32_t x,
+                                                 int32_t y, uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policies for weight tiles: read by one m-block only -> evicted first;
+// read by several m-blocks of a segment -> kept last.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m, int32_t x,
                                             int32_t y, uint64_t *bar) {
   asm volatile(
@@ -489,6 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int e = seg_exp[ti.s];
         const int row_a = seg_off[ti.s] + ti.m_blk * kBM;
+        // a weight tile read by this m-block only need not stay in L2; one
+        // that the segment's other m-blocks read too should
+        const bool shared_w =
+            (pre_h[ti.s + 1] - pre_h[ti.s] + pre_c[ti.s + 1] - pre_c[ti.s]) >= 2;
+        const uint64_t wpol = shared_w ? policy_evict_last() : policy_evict_first();
         // B rows of k-block 0; packed: [e][n_blk][kb][half][128 rows][64 cols],
         // so one k-block of the tile is 32 contiguous KiB.
         const int64_t packed0 = (int64_t)(e * NB + ti.n_blk) * nk * 256;
@@ -512,9 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_2d(sa, ma, kb * kBK, row_a, &bars->full[stage]);
           }
-          tma_load_2d(sa + kABytes, mb, kb * b_x_step, row_b0 + kb * b_y_step, &bars->full[stage]);
-          tma_load_2d(sa + kABytes + kBHalfBytes, mb, kb * b_x_step, row_b1 + kb * b_y_step,
-                      &bars->full[stage]);
+          tma_load_2d_hint(sa + kABytes, mb, kb * b_x_step, row_b0 + kb * b_y_step,
+                           &bars->full[stage], wpol);
+          tma_load_2d_hint(sa + kABytes + kBHalfBytes, mb, kb * b_x_step, row_b1 + kb * b_y_step,
+                           &bars->full[stage], wpol);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
