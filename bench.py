@@ -57,11 +57,18 @@ KERNEL_SOURCES = [os.path.join(ROOT, "grouped_ffn_gb300", "csrc", f)
 
 
 def kernel_source_hash() -> str:
+    """sha256 of the kernel sources with comments and blank space removed, so
+    that an edit to comments alone keeps a capture valid.  (The sources hold
+    no comment markers inside string literals.)"""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("".join(text.split()).encode())
     return h.hexdigest()
 
 

@@ -27,7 +27,9 @@
 //              SwiGLU in fp32, bf16 stores masked to the segment.
 // Double-buffered accumulators overlap a tile's epilogue with the next
 // tile's main loop.  Tiles are ordered (segment, n-block, m-block) so that
-// CTAs running side by side share B tiles (weights) and A rows in L2.
+// CTAs running side by side share B tiles (weights) and A rows in L2; a
+// weight tile that only one m-block reads is loaded with an L2 evict_first
+// policy, one that several m-blocks read with evict_last.
 // All waits are bounded (%globaltimer); on expiry the CTA records
 // MOE_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, frees TMEM, exits.
 #include <cuda.h>
