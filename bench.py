@@ -650,24 +650,40 @@ def host_cpu_model() -> str:
     return platform.machine()
 
 
-def oracle_sample_step(w, pl, logits_np, x_bits, experts_gu, experts_d, shared, tokens):
+def oracle_sample_step(w, pl, logits_np, x_bits, experts_gu, experts_d, shared, tokens,
+                       stage_s=None):
     """The oracle's stage-wise path on a sample of tokens: route, layout,
-    permute, grouped FFN, combine, balancedness."""
+    permute, grouped FFN (+ shared expert), combine, balancedness.  If
+    stage_s (a dict) is given, each stage's seconds are added to it."""
     import oracle
+    clock = [time.perf_counter()]
+
+    def lap(name):
+        now = time.perf_counter()
+        if stage_s is not None:
+            stage_s[name] = stage_s.get(name, 0.0) + now - clock[0]
+        clock[0] = now
+
     lg = logits_np[tokens]
     if w.score_fn == wl.SCORE_SOFTMAX and w.n_groups == 1:
         ids, wts = oracle.route_softmax_topk(lg, w.k)
     else:
         ids, wts, _ = oracle.route_group_limited(lg, w.k, w.n_groups, w.topk_groups, w.group_topn)
+    lap("route")
     lay = oracle.dispatch_layout(ids, pl if pl.token_src_rank is None else pl)
+    lap("layout")
     xs = oracle.bf16_bits_to_f64(x_bits[tokens])
     xp = oracle.permute(xs, lay["dest_row"], w.k)
+    lap("permute")
     _, yp = oracle.grouped_ffn(xp, lay["seg_offsets"], pl.slot_expert, experts_gu, experts_d, w.I)
     sh = None
     if shared is not None:
         _, sh = oracle.swiglu_expert(xs, shared[0], shared[1], w.shared_I)
+    lap("grouped_ffn")
     y = oracle.combine_f64(yp, lay["dest_row"], wts.astype(np.float32).astype(np.float64), sh)
+    lap("combine")
     oracle.balance_stats(lay["rank_counts"])
+    lap("balance")
     return y
 
 
@@ -699,6 +715,7 @@ def cpu_baseline(w, pl, logits, x, wgu, wd, sgu, sd, seconds):
         __import__("oracle").bf16_bits_to_f64(_bits(sd[0])))
     n = 4
     done_tokens, t_used = 0, 0.0
+    stage_s = {}
     while t_used < seconds and done_tokens < w.T and n <= 256:
         toks = np.sort(rng.choice(w.T, size=min(n, w.T), replace=False))
         # host copies of the experts this sample needs are made outside the timer
@@ -711,7 +728,7 @@ def cpu_baseline(w, pl, logits, x, wgu, wd, sgu, sd, seconds):
             gu.fetch(int(e))
             d.fetch(int(e))
         t0 = time.perf_counter()
-        oracle_sample_step(w, pl, logits_np, x_bits, gu, d, shared, toks)
+        oracle_sample_step(w, pl, logits_np, x_bits, gu, d, shared, toks, stage_s)
         t_used += time.perf_counter() - t0
         done_tokens += len(toks)
         n *= 2
@@ -720,7 +737,10 @@ def cpu_baseline(w, pl, logits, x, wgu, wd, sgu, sd, seconds):
             "kind": "oracle",
             "sample": f"{done_tokens} of {w.T} tokens of the {w.name} layer through the oracle's "
                       f"stage-wise path (route, layout, permute, grouped FFN, combine, balance) "
-                      f"in {t_used:.1f} s; numpy fp64, BLAS threads = host cores"}
+                      f"in {t_used:.1f} s; numpy fp64, BLAS threads = host cores",
+            # route, layout and balance run single-threaded (plain Python /
+            # numpy loops); the FFN's matmuls use the BLAS threads
+            "stage_us_per_token": {k: v / done_tokens * 1e6 for k, v in stage_s.items()}}
 
 
 def run_reference(args, world, rank):
