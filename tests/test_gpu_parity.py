@@ -133,6 +133,21 @@ def test_route_group_limited_small_groups():
         np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
 
 
+@pytest.mark.parametrize("n_groups,topk_groups,topn,k", [(16, 4, 2, 8), (8, 2, 1, 6), (32, 8, 3, 16),
+                                                         (4, 4, 2, 8)])
+def test_route_group_limited_full_width_other_group_shapes(n_groups, topk_groups, topn, k):
+    """256 experts with other group shapes than the group-limited workload's
+    (8 groups, top 4, sum of top 2), Zipf-skewed logits; the last case keeps
+    every group, so it reduces to plain sigmoid top-k."""
+    w = wl.WORKLOADS["group_limited"].scaled(T=2000, k=k, n_groups=n_groups,
+                                             topk_groups=topk_groups, group_topn=topn)
+    logits = wl.make_logits(w, "cuda")
+    ids, wts = gpu_route(w, logits)
+    rid, rw, _ = oracle_route(w, logits.cpu().numpy())
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
+
+
 def test_route_group_limited_near_ties_decided_in_fp64():
     """Groups whose scores differ by less than fp32 can resolve: the kernel
     must fall back to the fp64 definition and agree with the oracle, and
@@ -192,6 +207,27 @@ def test_layout_many_tiles_many_slots_and_ragged_tail():
     ref = oracle.dispatch_layout(ids_np, pl)
     for key in ref:
         assert np.array_equal(got[key], ref[key]), key
+
+
+def test_layout_with_explicit_token_source_ranks():
+    """The fixed replica rule with each token's rank given by an array
+    instead of t mod R (tokens clustered on a few ranks, so that some nodes
+    hold no copy of a hot expert and the spread rule applies)."""
+    m = moe()
+    w = wl.WORKLOADS["replica"].scaled(T=6000)
+    base = wl.make_placement(w)
+    rng = np.random.default_rng(21)
+    src = rng.choice([0, 1, 5, 13], size=w.T).astype(np.int32)
+    pl = wl.Placement(base.n_experts, base.n_ranks, base.ranks_per_node, base.slot_expert,
+                      base.slot_rank, base.rep_offsets, base.rep_slots, src)
+    ids, _ = gpu_route(w, wl.make_logits(w, "cuda"))
+    got = gpu_layout(ids, m.DevicePlacement.from_tables(pl), w.T, w.k)
+    ref = oracle.dispatch_layout(ids.cpu().numpy(), pl)
+    for key in ("slot", "seg_counts", "seg_offsets", "dest_row", "src_assign", "rank_counts"):
+        assert np.array_equal(got[key], ref[key]), key
+    # the rule differs from t mod R here
+    default = oracle.dispatch_layout(ids.cpu().numpy(), base)
+    assert not np.array_equal(default["slot"], ref["slot"])
 
 
 def test_layout_empty_and_single_token():
@@ -273,7 +309,8 @@ def test_permute_bit_exact(name):
 
 
 @pytest.mark.parametrize("k,H,shared", [(2, 256, False), (4, 4096, False), (8, 7168, True),
-                                        (3, 136, True), (16, 64, False)])
+                                        (3, 136, True), (16, 64, False), (1, 520, True),
+                                        (1, 8192, False)])
 def test_combine_bit_exact(k, H, shared):
     m = moe()
     T = 333
@@ -289,6 +326,21 @@ def test_combine_bit_exact(k, H, shared):
     ref = oracle.combine_fma32(bits(yp), dr.cpu().numpy(), wts.cpu().numpy(),
                                None if sh is None else bits(sh))
     assert np.array_equal(bits(y), ref)
+
+
+@pytest.mark.parametrize("T,H,k", [(37, 136, 3), (5, 8, 1), (300, 4104, 2)])
+def test_permute_odd_widths_bit_exact(T, H, k):
+    """Row widths that are not a multiple of the copy loop's unroll (H/8 =
+    17, 1 and 513 chunks of 16 bytes)."""
+    m = moe()
+    g = torch.Generator(device="cuda").manual_seed(T + H)
+    x = torch.randn(T, H, generator=g, device="cuda").to(torch.bfloat16)
+    dr = torch.randperm(T * k, generator=g, device="cuda").to(torch.int32)
+    xp = torch.empty(T * k, H, dtype=torch.bfloat16, device="cuda")
+    ws = m.new_workspace(T, k, 1)
+    m.moe_permute(x, k, dr, xp, ws)
+    m.moe_check_device_status(ws)
+    assert np.array_equal(bits(xp), oracle.permute(bits(x), dr.cpu().numpy(), k))
 
 
 def test_permute_then_combine_one_hot_is_identity():
