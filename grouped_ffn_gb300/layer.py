@@ -107,6 +107,12 @@ class MoELayer:
         self.max_count = torch.empty(1, **i32)
         self.total = torch.empty(1, dtype=torch.int64, device=dev)
         self.ws = moe.new_workspace(max_tokens, k, S, device=dev, n_experts=E, n_ranks=R)
+        # the balancedness statistic needs only the layout's per-rank counts:
+        # it runs on a side stream forked after the layout and joined at the
+        # end of the step, off the permute -> FFN -> combine path
+        self._side = torch.cuda.Stream(device=dev)
+        self._ev_layout = torch.cuda.Event()
+        self._ev_stats = torch.cuda.Event()
         self.replica_relax = replica_relax
         self.inter_node = torch.zeros(1, **i32)
         if self.fuse_shared:
@@ -172,6 +178,7 @@ class MoELayer:
                                            self.seg_offsets, self.dest_row[:A],
                                            self.src_assign[:A], self.rank_counts, self.ws, stream)
         mark("layout")
+        self._fork_balance(stream)
         if self.gather:
             mark("permute")
             moe.moe_grouped_ffn_gather(x, self.k, self.src_assign[:A], self.seg_offsets,
@@ -195,7 +202,7 @@ class MoELayer:
         shared = self.shared_output(T) if self.fuse_shared else self._shared(x, T, stream, mark)
         moe.moe_combine(self.y_perm[:A], self.dest_row[:A], w, y, self.ws, shared, stream)
         mark("combine")
-        self._balance(stream, mark)
+        self._join_balance(stream, mark)
         return y
 
     def _dispatch(self, x, A, rows, masked_m, stream, mark):
@@ -231,9 +238,16 @@ class MoELayer:
             return self.y_perm[A:A + T]
         return self.shared_y[:T] if self.shared_I else None
 
-    def _balance(self, stream, mark):
+    def _fork_balance(self, stream):
+        s = stream or torch.cuda.current_stream()
+        self._ev_layout.record(s)
+        self._side.wait_event(self._ev_layout)
         moe.moe_balance_stats(self.rank_counts, self.balancedness, self.max_count, self.total,
-                              self.ws, stream)
+                              None, self._side)
+        self._ev_stats.record(self._side)
+
+    def _join_balance(self, stream, mark):
+        (stream or torch.cuda.current_stream()).wait_event(self._ev_stats)
         mark("balance")
 
     def _forward_masked(self, x, y, ids, w, T, A, stream, mark):
@@ -246,6 +260,7 @@ class MoELayer:
                                        self.masked_m, self.dest_row[:A], self.src_assign,
                                        self.rank_counts, self.n_dropped, self.ws, stream)
         mark("layout")
+        self._fork_balance(stream)
         self._dispatch(x, A, rows, self.masked_m, stream, mark)
         moe.moe_grouped_ffn_masked(self.x_perm, cap, self.masked_m, self.placement.slot_expert,
                                    self.w_gate_up, self.w_down, self.h, self.y_perm, self.ws,
@@ -254,7 +269,7 @@ class MoELayer:
         shared = self._shared(x, T, stream, mark)
         moe.moe_combine_masked(self.y_perm, self.dest_row[:A], w, y, self.ws, shared, stream)
         mark("combine")
-        self._balance(stream, mark)
+        self._join_balance(stream, mark)
         return y
 
     def capture(self, logits: torch.Tensor, x: torch.Tensor, y: torch.Tensor):
