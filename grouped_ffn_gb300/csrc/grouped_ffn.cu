@@ -315,10 +315,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&p);
 }
 
+// silu(g) * u = g / (1 + e^-g) * u in fp32, with CUDA's fast exponential and
+// division intrinsics: their few-ulp error is far below the bf16 rounding of
+// h, and the gate/up epilogue (128 of these per thread and tile) shares its
+// SM sub-partitions with the TMA and MMA issuing warps.  For g below about
+// -88, e^-g overflows and the result is 0 (the exact value is below 1e-36).
 __device__ __forceinline__ float silu_mul(uint32_t g_bits, uint32_t u_bits) {
   const float g = __uint_as_float(g_bits);
   const float u = __uint_as_float(u_bits);
-  return g / (1.0f + expf(-g)) * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // --------------------------------------------------------------- the kernel
@@ -331,16 +336,44 @@ struct TileInfo {
 // re-read from L2 and so lean on the tensor cores) and the cold stream
 // (one-block segments, which stream fresh weights from HBM) are merged in
 // proportion to their lengths, so that every wave of CTAs mixes both kinds
-// of work (tile_order.cuh).
-__device__ __forceinline__ TileInfo decode(int64_t t, int64_t T0, const int32_t *pre_h,
-                                           const int32_t *pre_c, int S, int NB0, int NB1,
-                                           int64_t Mh, int64_t Mc) {
-  TileInfo ti;
-  ti.ph = t < T0 ? 0 : 1;
-  const int64_t u = ti.ph ? t - T0 : t;
-  tile_order::merged(u, pre_h, pre_c, S, ti.ph ? NB1 : NB0, Mh, Mc, ti.s, ti.n_blk, ti.m_blk);
-  return ti;
-}
+// of work (tile_order.cuh).  A CTA takes tiles blockIdx.x, + gridDim.x, ...;
+// each role walks that sequence with additions only, since a division per
+// tile on the producer's single thread stalled the k-block pipeline at
+// every tile boundary.
+struct TileWalk {
+  tile_order::MergedWalk w;
+  int64_t t, T0, Mh, Mc;
+  int NB0, NB1;
+
+  __device__ __forceinline__ void start(int64_t t_first, int64_t T0_, int64_t Mh_, int64_t Mc_,
+                                        int NB0_, int NB1_) {
+    t = t_first;
+    T0 = T0_;
+    Mh = Mh_;
+    Mc = Mc_;
+    NB0 = NB0_;
+    NB1 = NB1_;
+    if (t < T0)
+      w.start(t, gridDim.x, Mh, Mc, NB0);
+    else
+      w.start(t - T0, gridDim.x, Mh, Mc, NB1);
+  }
+  __device__ __forceinline__ void next() {
+    const bool was0 = t < T0;
+    t += gridDim.x;
+    if (was0 && t >= T0)
+      w.start(t - T0, gridDim.x, Mh, Mc, NB1);  // first tile of phase 1
+    else
+      w.advance();
+  }
+  __device__ __forceinline__ TileInfo info(const int32_t *pre_h, const int32_t *pre_c,
+                                           int S) const {
+    TileInfo ti;
+    ti.ph = t < T0 ? 0 : 1;
+    w.tile(pre_h, pre_c, S, ti.ph ? NB1 : NB0, ti.s, ti.n_blk, ti.m_blk);
+    return ti;
+  }
+};
 
 // In-place exclusive scan of a[0..n) by one warp (lane L owns a chunk);
 // a[n] receives the total.
@@ -468,95 +501,138 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_par = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode(t, T0, pre_h, pre_c, p.S, NB0, NB1, Mh, Mc);
-      const bool gather = p.gather_src != nullptr && ti.ph == 0;
-      if (gather) {  // token row of each of the tile's 128 rows (row 0 past the end)
-        const int row0 = seg_off[ti.s] + ti.m_blk * kBM;
-        const int row_end = seg_end[ti.s];
-        for (int j = lane; j < kBM; j += 32) {
-          int tok = 0;
-          if (row0 + j < row_end) {
-            tok = __ldg(p.gather_src + row0 + j) / p.gather_k;
-            if (tok < 0 || tok >= p.gather_T) tok = 0;
+    // Everything one tile's loads need, prepared by lane 0 from its TileInfo.
+    struct Loads {
+      int ph, s, nk, need, row_a, row_b0, row_b1, b_x_step, b_y_step;
+      uint64_t wpol;
+    };
+    auto prepare = [&](const TileInfo &ti) {
+      Loads L;
+      const Phase &P = p.ph[ti.ph];
+      const int NB = ti.ph ? NB1 : NB0;
+      const int mt = pre_h[ti.s + 1] - pre_h[ti.s] + pre_c[ti.s + 1] - pre_c[ti.s];
+      L.ph = ti.ph;
+      L.s = ti.s;
+      L.nk = P.K / kBK;
+      L.need = mt * NB0;  // phase-0 tiles of the segment, all of which store h
+      const int e = seg_exp[ti.s];
+      L.row_a = seg_off[ti.s] + ti.m_blk * kBM;
+      // a weight tile read by this m-block only need not stay in L2; one
+      // that the segment's other m-blocks read too should
+      L.wpol = mt >= 2 ? policy_evict_last() : policy_evict_first();
+      // B rows of k-block 0; packed: [e][n_blk][kb][half][128 rows][64 cols],
+      // so one k-block of the tile is 32 contiguous KiB.
+      const int64_t packed0 = (int64_t)(e * NB + ti.n_blk) * L.nk * 256;
+      L.row_b0 = p.b_packed ? (int)packed0 : e * P.b_rows_per_expert + ti.n_blk * P.b_nblk_stride;
+      L.row_b1 = p.b_packed ? L.row_b0 + 128 : L.row_b0 + P.b_second_off;
+      L.b_x_step = p.b_packed ? 0 : kBK;
+      L.b_y_step = p.b_packed ? 256 : 0;
+      return L;
+    };
+    // A phase-1 tile reads h rows: every phase-0 tile of its segment must
+    // have stored them (bounded wait on the segment's counter).
+    auto wait_h = [&](const Loads &L) {
+      if (ld_acquire_s32(p.ready + L.s) < L.need) {
+        const uint64_t t0 = moe::global_timer_ns();
+        while (ld_acquire_s32(p.ready + L.s) < L.need) {
+          if (*abort_flag) return false;
+          const uint64_t dt = moe::global_timer_ns() - t0;
+          if (dt > moe::kWaitLimitNs) {
+            *abort_flag = 1;
+            moe::report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, (int32_t)(dt / 1000), kid);
+            return false;
           }
-          gidx[j] = tok;
+          __nanosleep(64);
         }
-        __syncwarp();
       }
-      if (lane == 0) {
-        const Phase &P = p.ph[ti.ph];
-        const CUtensorMap *ma = ti.ph ? &tmap_a1 : &tmap_a0;
-        const CUtensorMap *mb = ti.ph ? &tmap_b1 : &tmap_b0;
-        const int NB = ti.ph ? NB1 : NB0;
-        const int nk = P.K / kBK;
-        if (ti.ph == 1) {
-          // every phase-0 tile of this segment must have stored its h rows
-          const int need =
-              (pre_h[ti.s + 1] - pre_h[ti.s] + pre_c[ti.s + 1] - pre_c[ti.s]) * NB0;
-          if (ld_acquire_s32(p.ready + ti.s) < need) {
-            const uint64_t t0 = moe::global_timer_ns();
-            while (ld_acquire_s32(p.ready + ti.s) < need) {
-              if (*abort_flag) {
-                ok = false;
-                break;
-              }
-              const uint64_t dt = moe::global_timer_ns() - t0;
-              if (dt > moe::kWaitLimitNs) {
-                *abort_flag = 1;
-                moe::report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, (int32_t)(dt / 1000), kid);
-                ok = false;
-                break;
-              }
-              __nanosleep(64);
-            }
-          }
-          if (ok) fence_proxy_async_global();
-        }
-        const int e = seg_exp[ti.s];
-        const int row_a = seg_off[ti.s] + ti.m_blk * kBM;
-        // a weight tile read by this m-block only need not stay in L2; one
-        // that the segment's other m-blocks read too should
-        const bool shared_w =
-            (pre_h[ti.s + 1] - pre_h[ti.s] + pre_c[ti.s + 1] - pre_c[ti.s]) >= 2;
-        const uint64_t wpol = shared_w ? policy_evict_last() : policy_evict_first();
-        // B rows of k-block 0; packed: [e][n_blk][kb][half][128 rows][64 cols],
-        // so one k-block of the tile is 32 contiguous KiB.
-        const int64_t packed0 = (int64_t)(e * NB + ti.n_blk) * nk * 256;
-        const int row_b0 = p.b_packed ? (int)packed0
-                                      : e * P.b_rows_per_expert + ti.n_blk * P.b_nblk_stride;
-        const int row_b1 = p.b_packed ? row_b0 + 128 : row_b0 + P.b_second_off;
-        const int b_x_step = p.b_packed ? 0 : kBK;
-        const int b_y_step = p.b_packed ? 256 : 0;
-        for (int kb = 0; kb < nk && ok; ++kb) {
-          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.status, kid)) {
+      fence_proxy_async_global();
+      return true;
+    };
+    // k-block kb of a tile into the next ring stage.
+    auto load_stage = [&](const Loads &L, int kb, bool gather) {
+      if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.status, kid)) return false;
+      const CUtensorMap *ma = L.ph ? &tmap_a1 : &tmap_a0;
+      const CUtensorMap *mb = L.ph ? &tmap_b1 : &tmap_b0;
+      uint8_t *sa = smem + (size_t)stage * kStageBytes;
+      mbar_arrive_expect_tx(&bars->full[stage], kStageBytes);
+      if (gather) {
+#pragma unroll 4
+        for (int g = 0; g < kBM / 4; ++g)
+          tma_gather4(sa + g * 512, ma, kb * kBK, gidx[4 * g], gidx[4 * g + 1], gidx[4 * g + 2],
+                      gidx[4 * g + 3], &bars->full[stage]);
+      } else {
+        tma_load_2d(sa, ma, kb * kBK, L.row_a, &bars->full[stage]);
+      }
+      tma_load_2d_hint(sa + kABytes, mb, kb * L.b_x_step, L.row_b0 + kb * L.b_y_step,
+                       &bars->full[stage], L.wpol);
+      tma_load_2d_hint(sa + kABytes + kBHalfBytes, mb, kb * L.b_x_step,
+                       L.row_b1 + kb * L.b_y_step, &bars->full[stage], L.wpol);
+      armed |= 1u << stage;
+      armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      return true;
+    };
+    TileWalk walk;
+    walk.start(blockIdx.x, T0, Mh, Mc, NB0, NB1);
+    if (p.gather_src == nullptr) {
+      // Lane 0 alone.  The next tile's loads are prepared right after the
+      // current tile's first stage is issued, while the ring is full, so
+      // that its first stage goes out as soon as a slot frees.
+      if (lane == 0 && walk.t < total) {
+        Loads cur = prepare(walk.info(pre_h, pre_c, p.S));
+        for (;;) {
+          if (cur.ph == 1 && !wait_h(cur)) {
             ok = false;
             break;
           }
-          uint8_t *sa = smem + (size_t)stage * kStageBytes;
-          mbar_arrive_expect_tx(&bars->full[stage], kStageBytes);
-          if (gather) {
-#pragma unroll 4
-            for (int g = 0; g < kBM / 4; ++g)
-              tma_gather4(sa + g * 512, ma, kb * kBK, gidx[4 * g], gidx[4 * g + 1],
-                          gidx[4 * g + 2], gidx[4 * g + 3], &bars->full[stage]);
-          } else {
-            tma_load_2d(sa, ma, kb * kBK, row_a, &bars->full[stage]);
+          Loads nxt = cur;
+          bool more = false;
+          for (int kb = 0; kb < cur.nk; ++kb) {
+            if (!load_stage(cur, kb, false)) {
+              ok = false;
+              break;
+            }
+            if (kb == 0) {
+              walk.next();
+              more = walk.t < total;
+              if (more) nxt = prepare(walk.info(pre_h, pre_c, p.S));
+            }
           }
-          tma_load_2d_hint(sa + kABytes, mb, kb * b_x_step, row_b0 + kb * b_y_step,
-                           &bars->full[stage], wpol);
-          tma_load_2d_hint(sa + kABytes + kBHalfBytes, mb, kb * b_x_step, row_b1 + kb * b_y_step,
-                           &bars->full[stage], wpol);
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (!ok || !more) break;
+          cur = nxt;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // lane 0 is done with gidx too
-      if (!ok) break;
+    } else {
+      // Gathered A rows: the whole warp stages each phase-0 tile's 128
+      // token indices, then lane 0 issues its loads.
+      for (; walk.t < total; walk.next()) {
+        const TileInfo ti = walk.info(pre_h, pre_c, p.S);
+        const bool gather = ti.ph == 0;
+        if (gather) {  // token row of each of the tile's 128 rows (row 0 past the end)
+          const int row0 = seg_off[ti.s] + ti.m_blk * kBM;
+          const int row_end = seg_end[ti.s];
+          for (int j = lane; j < kBM; j += 32) {
+            int tok = 0;
+            if (row0 + j < row_end) {
+              tok = __ldg(p.gather_src + row0 + j) / p.gather_k;
+              if (tok < 0 || tok >= p.gather_T) tok = 0;
+            }
+            gidx[j] = tok;
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          const Loads L = prepare(ti);
+          if (L.ph == 1 && !wait_h(L)) ok = false;
+          for (int kb = 0; kb < L.nk && ok; ++kb)
+            if (!load_stage(L, kb, gather)) ok = false;
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // lane 0 is done with gidx too
+        if (!ok) break;
+      }
     }
     if (lane == 0)
       for (int i = 0; i < kStages; ++i)  // own copies land before the CTA exits
@@ -604,8 +680,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_in = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode(t, T0, pre_h, pre_c, p.S, NB0, NB1, Mh, Mc);
+    TileWalk walk;
+    walk.start(blockIdx.x, T0, Mh, Mc, NB0, NB1);
+    for (; walk.t < total; walk.next()) {
+      const TileInfo ti = walk.info(pre_h, pre_c, p.S);
       const Phase &P = p.ph[ti.ph];
       const int row = seg_off[ti.s] + ti.m_blk * kBM + r_in;
       const bool valid = row < seg_end[ti.s];
@@ -782,6 +860,9 @@ moe_status check_ffn_args(const uint16_t *x_perm, int64_t n_rows, const int32_t 
   if (S > kMaxSegs || H % 256 != 0 || I % 128 != 0 || n_rows >= ((int64_t)1 << 31))
     return MOE_ERR_UNSUPPORTED;
   if ((int64_t)E * 2 * I * (int64_t)H / 64 >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  // tile indices, and a segment's tiles, are split in 32-bit arithmetic
+  if (((n_rows + kBM - 1) / kBM + S) * (int64_t)(I / 128 + H / 256) >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED;
   if (!seg_offsets || !seg_expert || !w_gate_up || !w_down) return MOE_ERR_INVALID_ARG;
   if (moe_status s = moe_host::check_ws(ws, ws_bytes, kReadyOff + (size_t)S * sizeof(int32_t)))
     return s;

@@ -342,7 +342,8 @@ moe_status moe_dequant_fp8(const uint8_t *xq, const float *x_scale, int64_t n_ro
  *  as soon as all its gate/up tiles have stored h.
  *  ws: at least 256 + 4*S bytes (moe_workspace_size(T, k, S) is enough).
  *  Limits: H % 256 == 0, I % 128 == 0, S <= 1024, n_rows < 2^31,
- *  E*2I*H/64 < 2^31.
+ *  E*2I*H/64 < 2^31, and a tile list of (ceil(n_rows/128) + S) *
+ *  (I/128 + H/256) < 2^31 tiles.
  *  Device errors: MOE_ERR_DEVICE_INDEX (expert id), MOE_ERR_DEVICE_TIMEOUT. */
 moe_status moe_grouped_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_offsets,
                            const int32_t *seg_expert, int32_t S, int32_t E,

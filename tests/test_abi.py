@@ -78,6 +78,9 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert lib.moe_grouped_ffn(*args(256, 96, 64)) == 2
     assert lib.moe_grouped_ffn(*args(256, 128, 2000)) == 2
     assert lib.moe_grouped_ffn(*args(256, 128, 0)) == 1
+    # a tile list of 2^31 tiles or more: 2^24 m-blocks times (1024/128 + 30720/256) n-blocks
+    assert lib.moe_grouped_ffn(FAKE, (1 << 31) - 1, FAKE, FAKE, 1, 1, FAKE, FAKE, 30720, 1024,
+                               FAKE, FAKE, FAKE, 256, None) == 2
     # layout: slot limit, workspace size
     pl = moe.PlacementC(64, 2000, 8, 8, FAKE.value, FAKE.value, FAKE.value, FAKE.value, None)
     assert lib.moe_dispatch_layout(FAKE, 8, 2, ctypes.byref(pl), FAKE, FAKE, FAKE, FAKE, FAKE,

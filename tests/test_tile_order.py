@@ -1,7 +1,8 @@
-"""The grouped FFN's tile order (grouped_ffn_gb300/csrc/tile_order.cuh) is a
-bijection that keeps each hot (segment, n-block) group contiguous: checked
-by a host program built with nvcc from the same header the kernel uses.
-CPU only."""
+"""The grouped FFN's tile order (grouped_ffn_gb300/csrc/tile_order.cuh): the
+proportional hot/cold merge is a bijection that keeps each stream's order
+and the hot:cold mix at every position, and the incremental walk each CTA
+uses visits the same tiles.  Checked by a host program built with nvcc from
+the same header the kernel uses.  CPU only."""
 
 import os
 import shutil
@@ -12,7 +13,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_tile_order_is_a_bijection_with_contiguous_groups(tmp_path):
+def test_tile_order_is_a_bijection_and_the_walk_matches(tmp_path):
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     if not os.path.exists(nvcc):
         pytest.skip("nvcc not available")

@@ -2,8 +2,10 @@
 // random segment layouts, every (segment, n-block, m-block) tile appears at
 // exactly one merged position, each stream keeps its own (segment, n-block,
 // m-block) order, and after u positions exactly floor(u * Lh / L) hot tiles
-// have been placed.  Built with nvcc as a host program; needs no GPU.  Exit
-// code 0 = all cases pass.
+// have been placed.  The incremental MergedWalk, started at every CTA index
+// below the grid size G, visits the same tiles as merged() at u0, u0 + G, ...
+// Built with nvcc as a host program; needs no GPU.  Exit code 0 = all cases
+// pass.
 #include <cstdio>
 #include <cstdlib>
 #include <vector>
@@ -59,6 +61,23 @@ static int check(const std::vector<int> &mt, int NB, bool interleave) {
     if (total > 0 && hot_seen != (u + 1) * Lh / total) {
       std::printf("mix broken at u=%lld: %lld hot placed\n", (long long)u, (long long)hot_seen);
       return 1;
+    }
+  }
+  // the walk of each CTA u0 < G matches merged() position by position
+  for (int64_t G : {(int64_t)1, (int64_t)3, (int64_t)152, (int64_t)1000}) {
+    for (int64_t u0 = 0; u0 < G && u0 < total; ++u0) {
+      tile_order::MergedWalk w;
+      w.start(u0, G, Mh, Mc, NB);
+      for (int64_t u = u0; u < total; u += G, w.advance()) {
+        int s0, n0, m0, s1, n1, m1;
+        tile_order::merged(u, pre_h.data(), pre_c.data(), S, NB, Mh, Mc, s0, n0, m0);
+        w.tile(pre_h.data(), pre_c.data(), S, NB, s1, n1, m1);
+        if (w.u != u || s0 != s1 || n0 != n1 || m0 != m1) {
+          std::printf("walk G=%lld u0=%lld differs at u=%lld: (%d,%d,%d) vs (%d,%d,%d)\n",
+                      (long long)G, (long long)u0, (long long)u, s1, n1, m1, s0, n0, m0);
+          return 1;
+        }
+      }
     }
   }
   for (int s = 0; s < S; ++s)
