@@ -548,21 +548,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_global();
       return true;
     };
-    // k-block kb of a tile into the next ring stage.
-    auto load_stage = [&](const Loads &L, int kb, bool gather) {
+    // k-block kb of a tile into the next ring stage (lane 0; tiled A rows).
+    auto load_stage = [&](const Loads &L, int kb) {
       if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.status, kid)) return false;
       const CUtensorMap *ma = L.ph ? &tmap_a1 : &tmap_a0;
       const CUtensorMap *mb = L.ph ? &tmap_b1 : &tmap_b0;
       uint8_t *sa = smem + (size_t)stage * kStageBytes;
       mbar_arrive_expect_tx(&bars->full[stage], kStageBytes);
-      if (gather) {
-#pragma unroll 4
-        for (int g = 0; g < kBM / 4; ++g)
-          tma_gather4(sa + g * 512, ma, kb * kBK, gidx[4 * g], gidx[4 * g + 1], gidx[4 * g + 2],
-                      gidx[4 * g + 3], &bars->full[stage]);
-      } else {
-        tma_load_2d(sa, ma, kb * kBK, L.row_a, &bars->full[stage]);
-      }
+      tma_load_2d(sa, ma, kb * kBK, L.row_a, &bars->full[stage]);
       tma_load_2d_hint(sa + kABytes, mb, kb * L.b_x_step, L.row_b0 + kb * L.b_y_step,
                        &bars->full[stage], L.wpol);
       tma_load_2d_hint(sa + kABytes + kBHalfBytes, mb, kb * L.b_x_step,
@@ -591,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           Loads nxt = cur;
           bool more = false;
           for (int kb = 0; kb < cur.nk; ++kb) {
-            if (!load_stage(cur, kb, false)) {
+            if (!load_stage(cur, kb)) {
               ok = false;
               break;
             }
@@ -607,31 +600,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // Gathered A rows: the whole warp stages each phase-0 tile's 128
-      // token indices, then lane 0 issues its loads.
+      // token indices; in every stage of such a tile each lane issues one
+      // four-row gather (the TMA requests go out in parallel, not from one
+      // thread in turn), lane 0 the two weight loads.  Phase-1 tiles load as
+      // above, from lane 0.
       for (; walk.t < total; walk.next()) {
         const TileInfo ti = walk.info(pre_h, pre_c, p.S);
-        const bool gather = ti.ph == 0;
-        if (gather) {  // token row of each of the tile's 128 rows (row 0 past the end)
-          const int row0 = seg_off[ti.s] + ti.m_blk * kBM;
-          const int row_end = seg_end[ti.s];
-          for (int j = lane; j < kBM; j += 32) {
-            int tok = 0;
-            if (row0 + j < row_end) {
-              tok = __ldg(p.gather_src + row0 + j) / p.gather_k;
-              if (tok < 0 || tok >= p.gather_T) tok = 0;
-            }
-            gidx[j] = tok;
+        const Loads L = prepare(ti);
+        if (ti.ph == 1) {
+          if (lane == 0) {
+            if (!wait_h(L)) ok = false;
+            for (int kb = 0; kb < L.nk && ok; ++kb)
+              if (!load_stage(L, kb)) ok = false;
           }
-          __syncwarp();
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          // the other lanes follow lane 0's ring position
+          stage = __shfl_sync(0xffffffffu, stage, 0);
+          phase = __shfl_sync(0xffffffffu, phase, 0);
+          if (!ok) break;
+          continue;
         }
-        if (lane == 0) {
-          const Loads L = prepare(ti);
-          if (L.ph == 1 && !wait_h(L)) ok = false;
-          for (int kb = 0; kb < L.nk && ok; ++kb)
-            if (!load_stage(L, kb, gather)) ok = false;
+        // token row of each of the tile's 128 rows (token 0 past the end)
+        const int row0 = seg_off[ti.s] + ti.m_blk * kBM;
+        const int row_end = seg_end[ti.s];
+        for (int j = lane; j < kBM; j += 32) {
+          int tok = 0;
+          if (row0 + j < row_end) {
+            tok = __ldg(p.gather_src + row0 + j) / p.gather_k;
+            if (tok < 0 || tok >= p.gather_T) tok = 0;
+          }
+          gidx[j] = tok;
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // lane 0 is done with gidx too
+        __syncwarp();
+        for (int kb = 0; kb < L.nk; ++kb) {
+          int got = 0;
+          if (lane == 0)
+            got = mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.status, kid) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, got, 0)) {
+            ok = false;
+            break;
+          }
+          uint8_t *sa = smem + (size_t)stage * kStageBytes;
+          if (lane == 0) mbar_arrive_expect_tx(&bars->full[stage], kStageBytes);
+          __syncwarp();  // the transaction count is armed before any copy lands
+          tma_gather4(sa + lane * 512, &tmap_a0, kb * kBK, gidx[4 * lane], gidx[4 * lane + 1],
+                      gidx[4 * lane + 2], gidx[4 * lane + 3], &bars->full[stage]);
+          if (lane == 0) {
+            tma_load_2d_hint(sa + kABytes, &tmap_b0, kb * L.b_x_step, L.row_b0 + kb * L.b_y_step,
+                             &bars->full[stage], L.wpol);
+            tma_load_2d_hint(sa + kABytes + kBHalfBytes, &tmap_b0, kb * L.b_x_step,
+                             L.row_b1 + kb * L.b_y_step, &bars->full[stage], L.wpol);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
         if (!ok) break;
+        __syncwarp();  // gidx is rewritten for the next tile only after every lane issued
       }
     }
     if (lane == 0)
