@@ -19,6 +19,7 @@ enum KernelId : int32_t {
   K_FFN_DOWN = 6,
   K_COMBINE = 7,
   K_BALANCE = 8,
+  K_SELFTEST = 9,
 };
 
 // Status block at the start of every workspace (int32 words):

@@ -145,17 +145,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait; gives up when another role aborted or the deadline passed.
+// Bounded wait; gives up when another role aborted or the deadline passed
+// (then it raises the abort flag and records MOE_ERR_DEVICE_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           volatile int32_t *abort_flag, int32_t *status,
-                                          int32_t kid) {
+                                          int32_t kid, uint64_t limit_ns = moe::kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = moe::global_timer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     const uint64_t dt = moe::global_timer_ns() - t0;
-    if (dt > moe::kWaitLimitNs) {
+    if (dt > limit_ns) {
       *abort_flag = 1;
       moe::report_error(status, MOE_ERR_DEVICE_TIMEOUT, (int32_t)(dt / 1000), kid);
       return false;
@@ -234,6 +235,27 @@ __device__ __forceinline__ int32_t ld_acquire_s32(const int32_t *p) {
   int32_t v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// Bounded wait until a global counter written by other CTAs reaches `need`
+// (acquire loads).  Gives up like mbar_wait: on another role's abort, or at
+// the deadline, raising the abort flag and recording the timeout.
+__device__ __forceinline__ bool wait_counter(const int32_t *counter, int32_t need,
+                                             volatile int32_t *abort_flag, int32_t *status,
+                                             int32_t kid, uint64_t limit_ns = moe::kWaitLimitNs) {
+  if (ld_acquire_s32(counter) >= need) return true;
+  const uint64_t t0 = moe::global_timer_ns();
+  for (;;) {
+    if (ld_acquire_s32(counter) >= need) return true;
+    if (*abort_flag) return false;
+    const uint64_t dt = moe::global_timer_ns() - t0;
+    if (dt > limit_ns) {
+      *abort_flag = 1;
+      moe::report_error(status, MOE_ERR_DEVICE_TIMEOUT, (int32_t)(dt / 1000), kid);
+      return false;
+    }
+    __nanosleep(64);
+  }
 }
 
 __device__ __forceinline__ void epilogue_bar() {  // the 128 epilogue threads only
@@ -532,19 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A phase-1 tile reads h rows: every phase-0 tile of its segment must
     // have stored them (bounded wait on the segment's counter).
     auto wait_h = [&](const Loads &L) {
-      if (ld_acquire_s32(p.ready + L.s) < L.need) {
-        const uint64_t t0 = moe::global_timer_ns();
-        while (ld_acquire_s32(p.ready + L.s) < L.need) {
-          if (*abort_flag) return false;
-          const uint64_t dt = moe::global_timer_ns() - t0;
-          if (dt > moe::kWaitLimitNs) {
-            *abort_flag = 1;
-            moe::report_error(p.status, MOE_ERR_DEVICE_TIMEOUT, (int32_t)(dt / 1000), kid);
-            return false;
-          }
-          __nanosleep(64);
-        }
-      }
+      if (!wait_counter(p.ready + L.s, L.need, abort_flag, p.status, kid)) return false;
       fence_proxy_async_global();
       return true;
     };
@@ -1064,4 +1074,44 @@ extern "C" moe_status moe_pack_expert_weights(const uint16_t *w_gate_up, const u
                                                reinterpret_cast<uint4 *>(w_down_packed), d16,
                                                H / 256, I / kBK, H, I / 8, 1, I);
   return moe_host::launch_status();
+}
+
+// ------------------------------------------------------------ watchdog self-test
+namespace {
+
+__device__ int32_t g_never_set = 0;  // no code writes this word
+
+// One thread runs the two kinds of wait the grouped FFN uses, on conditions
+// nothing will ever satisfy: an mbarrier phase that expects an arrival
+// nobody makes, and a global counter nobody increments.  Each gives up at
+// its deadline and records MOE_ERR_DEVICE_TIMEOUT; the kernel then returns.
+__global__ void wait_selftest_kernel(int32_t *status, uint64_t limit_ns, int32_t *waited_us) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int32_t abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_barrier_init();
+  const uint64_t t0 = moe::global_timer_ns();
+  const bool a = mbar_wait(&bar, 0, &abort_flag, status, moe::K_SELFTEST, limit_ns);
+  const uint64_t t1 = moe::global_timer_ns();
+  abort_flag = 0;  // the second wait must run to its own deadline
+  const bool b = wait_counter(&g_never_set, 1, &abort_flag, status, moe::K_SELFTEST, limit_ns);
+  const uint64_t t2 = moe::global_timer_ns();
+  if (waited_us != nullptr) {
+    waited_us[0] = a ? -1 : (int32_t)((t1 - t0) / 1000);
+    waited_us[1] = b ? -1 : (int32_t)((t2 - t1) / 1000);
+  }
+}
+
+}  // namespace
+
+extern "C" moe_status moe_selftest_wait_timeout(void *ws, size_t ws_bytes, int32_t limit_us,
+                                                int32_t *waited_us, void *stream) {
+  if (limit_us < 1 || (int64_t)limit_us * 1000 > (int64_t)moe::kWaitLimitNs)
+    return MOE_ERR_INVALID_ARG;
+  if (moe_status s = moe_host::check_ws(ws, ws_bytes, moe::kStatusBytes)) return s;
+  wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      moe_host::status_ptr(ws), (uint64_t)limit_us * 1000, waited_us);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -60,6 +60,7 @@ _SIGNATURES = {
     "moe_workspace_size": (_SZ, [_I64, _I32, _I32]),
     "moe_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
     "moe_check_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(_I32)]),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [_P, _SZ, _I32, _P, _P]),
     "moe_route": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(RouteCfg), _P, _P, _P, _SZ, _P]),
     "moe_dispatch_layout": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC),
                                            _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -171,6 +172,16 @@ def moe_check_device_status(ws: torch.Tensor, stream=None):
     st = lib().moe_check_device_status(_ptr(ws), _stream(stream), ctypes.byref(info))
     if st != MOE_OK:
         raise MoeError("device", st, info.value)
+
+
+def moe_selftest_wait_timeout(ws: torch.Tensor, limit_us: int, waited_us=None, stream=None):
+    """Run the device wait watchdog self-test (moe.h); the timeout it records
+    is read with moe_check_device_status."""
+    if waited_us is not None:
+        _need(waited_us, torch.int32, "waited_us")
+    _check("moe_selftest_wait_timeout",
+           lib().moe_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), int(limit_us),
+                                           _ptr(waited_us), _stream(stream)))
 
 
 # ------------------------------------------------------------------ placement

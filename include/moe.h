@@ -108,8 +108,23 @@ moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 /* Synchronise `stream`, read the status word of `ws`, clear it, and return
  * the first device-side error recorded since the last check (MOE_OK if
  * none).  *info_host (may be NULL) receives a code-specific detail (the
- * offending index, or the kernel id of an expired wait). */
+ * offending index, or for MOE_ERR_DEVICE_TIMEOUT the microseconds the
+ * expired wait lasted). */
 moe_status moe_check_device_status(void *ws, void *stream, int32_t *info_host);
+
+/* Watchdog self-test of the device-side waits.  Launches one thread that
+ * runs the grouped FFN's two kinds of bounded wait on conditions nothing
+ * will satisfy: an mbarrier phase that expects an arrival nobody makes,
+ * and a global counter nobody increments.  Each gives up after limit_us
+ * microseconds of %globaltimer and records MOE_ERR_DEVICE_TIMEOUT in the
+ * status word of `ws` (the first one is kept; read it with
+ * moe_check_device_status).  The kernel then returns normally, so the
+ * context stays usable.  waited_us (device, 2 int32, may be NULL) receives
+ * how long each wait lasted (-1 if it completed).  Nothing faults, traps
+ * or hangs: the production kernels use the same waits with a 2 s limit.
+ * 1 <= limit_us <= 2,000,000; ws: at least MOE_WS_STATUS_BYTES. */
+moe_status moe_selftest_wait_timeout(void *ws, size_t ws_bytes, int32_t limit_us,
+                                     int32_t *waited_us, void *stream);
 
 /* Router: per token, the k experts with the largest scores and their
  * weights.  "14. Serving Mixture-of-Experts Models", "Follow one token

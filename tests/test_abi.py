@@ -78,6 +78,11 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert lib.moe_grouped_ffn(*args(256, 96, 64)) == 2
     assert lib.moe_grouped_ffn(*args(256, 128, 2000)) == 2
     assert lib.moe_grouped_ffn(*args(256, 128, 0)) == 1
+    # watchdog self-test: 1 us <= limit <= 2 s, a workspace with its status block
+    assert lib.moe_selftest_wait_timeout(FAKE, 256, 0, None, None) == 1
+    assert lib.moe_selftest_wait_timeout(FAKE, 256, 2_000_001, None, None) == 1
+    assert lib.moe_selftest_wait_timeout(None, 0, 1000, None, None) == 6
+    assert lib.moe_selftest_wait_timeout(FAKE, 16, 1000, None, None) == 6
     # a tile list of 2^31 tiles or more: 2^24 m-blocks times (1024/128 + 30720/256) n-blocks
     assert lib.moe_grouped_ffn(FAKE, (1 << 31) - 1, FAKE, FAKE, 1, 1, FAKE, FAKE, 30720, 1024,
                                FAKE, FAKE, FAKE, 256, None) == 2

@@ -8,6 +8,8 @@ Frobenius error <= 1e-2 and, after normalising each row by its largest
 of fp64.
 """
 
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -290,6 +292,31 @@ def test_layout_reports_bad_expert_id_without_faulting():
         m.moe_check_device_status(ws)
     assert ei.value.status == 4
     m.moe_check_device_status(ws)   # cleared after reading
+
+
+def test_bounded_waits_expire_report_and_leave_the_context_usable():
+    """Failure detection without a fault: the grouped FFN's two kinds of
+    bounded wait (an mbarrier phase, a global counter), run on conditions
+    nothing satisfies, give up at their deadline, record
+    MOE_ERR_DEVICE_TIMEOUT for the host, and leave the context usable."""
+    m = moe()
+    ws = m.new_workspace(8, 2, 64)
+    waited = torch.full((2,), -7, dtype=torch.int32, device="cuda")
+    limit_us = 50_000
+    t0 = time.perf_counter()
+    m.moe_selftest_wait_timeout(ws, limit_us, waited)
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_check_device_status(ws)
+    wall = time.perf_counter() - t0
+    assert ei.value.status == 5                          # MOE_ERR_DEVICE_TIMEOUT
+    assert limit_us <= ei.value.info < limit_us + 500_000
+    w = waited.cpu().tolist()
+    assert all(limit_us <= x < limit_us + 500_000 for x in w), w
+    assert wall < 10.0
+    m.moe_check_device_status(ws)                        # reported once, then cleared
+    # the same context still computes: permute then combine with one-hot
+    # weights gives back the input bit for bit
+    test_permute_then_combine_one_hot_is_identity()
 
 
 # ------------------------------------------------------------------ permute / combine
