@@ -89,3 +89,16 @@ def test_parse_relax(bench):
     assert bench.parse_relax("") is None
     assert bench.parse_relax("1/10") == (1, 10)
     assert bench.parse_relax("2") == (2, 1)
+
+
+def test_tensor_peak_follows_the_timed_region_clocks(bench):
+    peaks = {"bf16_tflops": 1951.4, "bf16_tflops_sustained": 1707.8}
+    at_max = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert bench.tensor_peak(peaks, at_max)[0] == 1951.4
+    assert bench.tensor_peak(peaks, {})[0] == 1951.4               # no samples: the larger one
+    capped = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    assert bench.tensor_peak(peaks, capped)[0] == 1707.8
+    slow = {"sm_mhz": 1600.0, "sm_max_mhz": 2070.0, "reasons": []}
+    p, label = bench.tensor_peak(peaks, slow)
+    assert p == 1707.8 and label.startswith("sustained")
+
