@@ -7,13 +7,16 @@
 // (gate, up, activation, down) is SwiGLU: h = silu(x Wg^T) * (x Wu^T),
 // y = h Wd^T.
 //
-// Two launches of one persistent, warp-specialised kernel:
-//   mode 0 (gate/up):  acc[128 x 256] = X[128 x H] * [Wg; Wu]^T tile,
+// One persistent, warp-specialised kernel runs both GEMMs in a single
+// cooperative launch, over one tile list:
+//   phase 0 (gate/up): acc[128 x 256] = X[128 x H] * [Wg; Wu]^T tile,
 //                      epilogue h = bf16(silu(acc[:, :128]) * acc[:, 128:])
-//   mode 1 (down):     acc[128 x 256] = h[128 x I] * Wd^T tile, epilogue bf16.
-// A 128-row tile always starts at a segment's first row plus a multiple of
-// 128 and uses that segment's expert; rows past the segment's end are
-// computed from whatever follows (or TMA zero fill) and are never stored.
+//   phase 1 (down):    acc[128 x 256] = h[128 x I] * Wd^T tile, epilogue bf16.
+// A segment's phase-1 tiles start once all its phase-0 tiles have stored
+// their h rows (a per-segment counter; bounded wait).  A 128-row tile
+// always starts at a segment's first row plus a multiple of 128 and uses
+// that segment's expert; rows past the segment's end are computed from
+// whatever follows (or TMA zero fill) and are never stored.
 //
 // Per CTA (one per SM, 192 threads):
 //   warp 0     TMA producer: A tile 128x64 and two B halves 128x64 per
@@ -96,7 +99,7 @@ struct FfnParams {
   int32_t b_packed;   // B in the tile-contiguous layout (see moe_pack_expert_weights)
   int32_t n_phases;   // 2: phase 1 reads what phase 0 writes, in the same launch
   int32_t *ready;     // [S] finished phase-0 tiles per segment (zeroed by the host)
-  int32_t interleave; // merge multi-tile and one-tile segments' tiles (see decode)
+  int32_t interleave; // merge multi-tile and one-tile segments' tiles (tile_order.cuh)
   // Gather mode: phase 0 reads row r of a segment from x[gather_src[r] / gather_k]
   // (token rows, gather_T of them) instead of a permuted copy.
   const int32_t *gather_src;
@@ -822,8 +825,9 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tile order: 1 (default) merges multi-tile and one-tile segments (see
-// decode); MOE_FFN_INTERLEAVE=0 keeps plain segment order, for comparison.
+// Tile order: 1 (default) merges multi-tile and one-tile segments
+// (tile_order.cuh); MOE_FFN_INTERLEAVE=0 keeps plain segment order, for
+// comparison.
 int interleave_tiles() {
   static int v = [] {
     const char *e = getenv("MOE_FFN_INTERLEAVE");
