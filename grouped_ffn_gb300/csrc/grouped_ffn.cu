@@ -1080,6 +1080,124 @@ extern "C" moe_status moe_pack_expert_weights(const uint16_t *w_gate_up, const u
   return moe_host::launch_status();
 }
 
+// ------------------------------------------------------ L2 prefetch of weights
+namespace {
+
+// "Mixture-of-Experts Inference", "Memory pressure" (EP size in prefill and
+// decode): in a decode step the expert work is dominated by loading the
+// expert weights.  Once routing is known, so are the weight tiles the
+// grouped FFN's first wave of CTAs streams first.  One warp per first-wave
+// tile derives the FFN's segments and tile order from the routed ids (an
+// expert's rows land in its first slot, exact for placements without
+// replicas) and asks L2 for the first k-blocks of its tile's gate/up
+// weights.  The fetches run beside the layout and the permute, while HBM is
+// otherwise idle.  They are spread over every SM's TMA unit, and each CTA
+// holds a few KiB of shared memory and exits within microseconds, so it
+// never keeps the cooperative FFN launch from finding room on an SM.
+// Prefetches are hints: no result depends on them.
+constexpr int kPrefetchMaxSegs = 256;
+
+struct PrefetchArgs {
+  const int32_t *topk_ids;
+  int64_t A;
+  const int32_t *rep_offsets, *rep_slots, *slot_expert;
+  int32_t E, S;
+  const uint16_t *w_gu;  // packed [e][n_blk][kb][half][128][64]
+  int32_t NB, nk;        // gate/up n-blocks (I/128) and k-blocks (H/64)
+  int32_t kblocks;       // k-blocks fetched per first-wave tile (<= 32)
+  int32_t interleave;
+};
+
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// grid = the FFN's persistent grid (its first-wave tiles), one warp each;
+// dynamic shared memory: 3 * (S + 1) int32.
+__global__ void __launch_bounds__(32) prefetch_ffn_weights_kernel(PrefetchArgs a) {
+  extern __shared__ int32_t pf_smem[];
+  int32_t *cnt = pf_smem;               // [S]
+  int32_t *pre_h = cnt + (a.S + 1);     // [S+1]
+  int32_t *pre_c = pre_h + (a.S + 1);   // [S+1]
+  const int lane = threadIdx.x;
+  for (int i = lane; i < a.S; i += 32) cnt[i] = 0;
+  __syncwarp();
+  for (int64_t i = lane; i < a.A; i += 32) {
+    const int e = __ldg(a.topk_ids + i);
+    if (e < 0 || e >= a.E) continue;
+    const int r0 = __ldg(a.rep_offsets + e);
+    if (r0 < 0 || r0 >= a.S || r0 >= __ldg(a.rep_offsets + e + 1)) continue;
+    const int s = __ldg(a.rep_slots + r0);
+    if (s >= 0 && s < a.S) atomicAdd(&cnt[s], 1);
+  }
+  __syncwarp();
+  for (int s = lane; s < a.S; s += 32) {  // as the FFN's prologue
+    const int mt = (cnt[s] + kBM - 1) / kBM;
+    const bool hot = a.interleave && mt >= 2;
+    pre_h[s] = hot ? mt : 0;
+    pre_c[s] = hot ? 0 : mt;
+  }
+  __syncwarp();
+  warp_exclusive_scan(pre_h, a.S, lane);
+  __syncwarp();
+  warp_exclusive_scan(pre_c, a.S, lane);
+  __syncwarp();
+  const int64_t Mh = pre_h[a.S], Mc = pre_c[a.S];
+  const int64_t t = blockIdx.x;  // the FFN's CTA blockIdx.x takes this tile first
+  if (t >= (Mh + Mc) * a.NB || lane >= a.kblocks) return;
+  int s, nb, mb;
+  tile_order::merged(t, pre_h, pre_c, a.S, a.NB, Mh, Mc, s, nb, mb);
+  // m-blocks of one (segment, n-block) share their weight tile, and the
+  // earlier ones sit earlier in the wave: fetch it once, for m-block 0
+  const int e = __ldg(a.slot_expert + s);
+  if (mb != 0 || e < 0 || e >= a.E) return;
+  prefetch_l2(a.w_gu + (((int64_t)e * a.NB + nb) * a.nk + lane) * 256 * kBK, 256 * kBK * 2);
+}
+
+}  // namespace
+
+extern "C" moe_status moe_prefetch_ffn_weights(const int32_t *topk_ids, int64_t T, int32_t k,
+                                               const moe_placement *pl,
+                                               const uint16_t *w_gate_up_packed, int32_t H,
+                                               int32_t I, int64_t max_bytes, void *stream) {
+  if (T < 0 || k < 1 || pl == nullptr || H < 1 || I < 1 || max_bytes < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 128 != 0 || pl->n_slots < 1 || pl->n_slots > kMaxSegs ||
+      pl->n_experts < 1)
+    return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)pl->n_experts * 2 * I * (int64_t)H / 64 >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (!topk_ids || !w_gate_up_packed || !pl->slot_expert || !pl->rep_offsets || !pl->rep_slots)
+    return MOE_ERR_INVALID_ARG;
+  if (!moe_host::aligned16(w_gate_up_packed)) return MOE_ERR_INVALID_ARG;
+  const int64_t tile_bytes = 256 * kBK * 2;  // one k-block of a gate/up weight tile
+  // nothing to do: no rows, a budget below one k-block, or more segments
+  // than the few KiB of shared memory a prefetching CTA may hold
+  if (T == 0 || max_bytes < tile_bytes || pl->n_slots > kPrefetchMaxSegs) return MOE_OK;
+  const int wave = moe_host::sm_count();
+  if (wave < 1) return MOE_ERR_CUDA;
+  PrefetchArgs a{};
+  a.topk_ids = topk_ids;
+  a.A = T * (int64_t)k;
+  a.rep_offsets = pl->rep_offsets;
+  a.rep_slots = pl->rep_slots;
+  a.slot_expert = pl->slot_expert;
+  a.E = pl->n_experts;
+  a.S = pl->n_slots;
+  a.w_gu = w_gate_up_packed;
+  a.NB = I / 128;
+  a.nk = H / kBK;
+  a.interleave = interleave_tiles();
+  int64_t kb = max_bytes / ((int64_t)wave * tile_bytes);
+  if (kb > a.nk) kb = a.nk;
+  if (kb > 32) kb = 32;  // one k-block per lane
+  a.kblocks = (int32_t)kb;
+  if (a.kblocks < 1) return MOE_OK;
+  const size_t smem = (size_t)3 * (a.S + 1) * sizeof(int32_t);
+  prefetch_ffn_weights_kernel<<<wave, 32, smem, static_cast<cudaStream_t>(stream)>>>(a);
+  return moe_host::launch_status();
+}
+
 // ------------------------------------------------------------ watchdog self-test
 namespace {
 

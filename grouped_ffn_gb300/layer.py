@@ -18,6 +18,9 @@ from . import moe
 
 
 class MoELayer:
+    PREFETCH_BYTES = 96 << 20          # three quarters of L2
+    PREFETCH_MAX_DISPATCH = 32 << 20   # dispatched bf16 bytes up to which it applies
+
     def __init__(self, *, H: int, I: int, E: int, k: int, placement: moe.DevicePlacement,
                  w_gate_up: torch.Tensor, w_down: torch.Tensor, max_tokens: int,
                  score_fn: int = moe.MOE_SCORE_SOFTMAX, n_groups: int = 1,
@@ -127,11 +130,21 @@ class MoELayer:
             self.shared_I = 0
         # per step: route, layout scan + finalize, permute, FFN, combine,
         # balance (+1 shared FFN, +4 replica routing: prep, key scan,
-        # water-fill, assign); packing happens once, here
-        # (+1 FP8 dequantization)
+        # water-fill, assign, +1 FP8 dequantization, +1 weight prefetch);
+        # packing happens once, here
+        # L2 prefetch of the FFN's first weight tiles, on the side stream
+        # right after routing: worth it when the step is weight-bound and its
+        # dispatch is small (decode), so that the fetched tiles are neither
+        # competing with nor evicted by a large permute; exact placement
+        # without replicas, packed weights, the contiguous layout
+        small = max_tokens * k * H * 2 <= self.PREFETCH_MAX_DISPATCH
+        self.prefetch_bytes = self.PREFETCH_BYTES if (
+            small and packed and not gather and masked_cap is None and replica_relax is None
+            and placement.n_slots == placement.n_experts) else 0
+        self._ev_route = torch.cuda.Event()
         self.launches_per_step = 7 + (1 if shared_w_gate_up is not None else 0) + \
             (4 if replica_relax is not None else 0) - (1 if gather else 0) + \
-            (1 if fp8_dispatch else 0)
+            (1 if fp8_dispatch else 0) + (1 if self.prefetch_bytes else 0)
 
     @staticmethod
     def _pack(w_gate_up, w_down):
@@ -164,6 +177,7 @@ class MoELayer:
         A = T * self.k
         ids, w = self.topk_ids[:T], self.topk_w[:T]
         moe.moe_route(logits, self.cfg, ids, w, self.ws, stream)
+        self._fork_prefetch(ids, stream)
         mark("route")
         if self.masked_cap is not None:
             return self._forward_masked(x, y, ids, w, T, A, stream, mark)
@@ -237,6 +251,17 @@ class MoELayer:
             A = T * self.k
             return self.y_perm[A:A + T]
         return self.shared_y[:T] if self.shared_I else None
+
+    def _fork_prefetch(self, ids, stream):
+        """The routed ids fix which weight tiles the FFN streams first: ask
+        L2 for them on the side stream while the layout and the permute run."""
+        if not self.prefetch_bytes:
+            return
+        s = stream or torch.cuda.current_stream()
+        self._ev_route.record(s)
+        self._side.wait_event(self._ev_route)
+        moe.moe_prefetch_ffn_weights(ids, self.placement, self.w_gate_up, self.H, self.I,
+                                     self.prefetch_bytes, self._side)
 
     def _fork_balance(self, stream):
         s = stream or torch.cuda.current_stream()

@@ -61,6 +61,8 @@ _SIGNATURES = {
     "moe_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
     "moe_check_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(_I32)]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [_P, _SZ, _I32, _P, _P]),
+    "moe_prefetch_ffn_weights": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC), _P,
+                                                _I32, _I32, _I64, _P]),
     "moe_route": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(RouteCfg), _P, _P, _P, _SZ, _P]),
     "moe_dispatch_layout": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC),
                                            _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -237,6 +239,18 @@ def moe_dispatch_layout(topk_ids, placement: DevicePlacement, slot, seg_counts, 
         _ptr(topk_ids), T, k, ctypes.byref(placement.c), _ptr(slot), _ptr(seg_counts),
         _ptr(seg_offsets), _ptr(dest_row), _ptr(src_assign), _ptr(rank_counts), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def moe_prefetch_ffn_weights(topk_ids, placement: DevicePlacement, w_gate_up_packed, H: int,
+                             I: int, max_bytes: int, stream=None):
+    """Ask L2 for the weight tiles the grouped FFN's first wave streams first
+    (moe.h); a hint that writes nothing."""
+    _need(topk_ids, torch.int32, "topk_ids")
+    _bf16(w_gate_up_packed, "w_gate_up_packed")
+    T, k = topk_ids.shape
+    _check("moe_prefetch_ffn_weights", lib().moe_prefetch_ffn_weights(
+        _ptr(topk_ids), T, k, ctypes.byref(placement.c), _ptr(w_gate_up_packed), int(H), int(I),
+        int(max_bytes), _stream(stream)))
 
 
 def moe_dispatch_layout_noalloc(topk_ids, placement: DevicePlacement, slot, seg_counts,

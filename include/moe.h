@@ -112,6 +112,26 @@ moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  * expired wait lasted). */
 moe_status moe_check_device_status(void *ws, void *stream, int32_t *info_host);
 
+/* L2 prefetch of the grouped FFN's first weight tiles.  "Mixture-of-Experts
+ * Inference", "Memory pressure" (EP size in prefill and decode): a decode
+ * step's expert work is dominated by loading the expert weights.  One warp
+ * per CTA of the FFN's first wave derives, from the routed ids (device
+ * int32 [T,k]) and the placement, the segments and tile order of
+ * moe_grouped_ffn_packed (an expert's rows land in its first slot, exact
+ * without replicas) and asks L2 for the first k-blocks of the gate/up
+ * weight tile that CTA takes first: at most max_bytes in all, at most 32
+ * k-blocks a tile.  Issued on a second stream right after moe_route, the
+ * fetches run while the layout and the permute leave HBM idle; each CTA
+ * holds 12*(n_slots+1) bytes of shared memory and exits at once, so the
+ * cooperative FFN launch still finds room on every SM.  The fetches are
+ * hints: no output depends on them and the call writes nothing.
+ * w_gate_up_packed: the packed gate/up weights (moe_pack_expert_weights),
+ * 16-byte aligned.  Limits as moe_grouped_ffn_packed; T == 0, a budget
+ * below one 32 KiB k-block, or n_slots > 256 launches nothing. */
+moe_status moe_prefetch_ffn_weights(const int32_t *topk_ids, int64_t T, int32_t k,
+                                    const moe_placement *pl, const uint16_t *w_gate_up_packed,
+                                    int32_t H, int32_t I, int64_t max_bytes, void *stream);
+
 /* Watchdog self-test of the device-side waits.  Launches one thread that
  * runs the grouped FFN's two kinds of bounded wait on conditions nothing
  * will satisfy: an mbarrier phase that expects an arrival nobody makes,

@@ -78,6 +78,16 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert lib.moe_grouped_ffn(*args(256, 96, 64)) == 2
     assert lib.moe_grouped_ffn(*args(256, 128, 2000)) == 2
     assert lib.moe_grouped_ffn(*args(256, 128, 0)) == 1
+    # L2 weight prefetch: sizes and pointers first; T = 0 or a budget below one
+    # 32 KiB k-block launches nothing
+    pl = moe.PlacementC(64, 64, 8, 8, FAKE.value, FAKE.value, FAKE.value, FAKE.value, None)
+    pf = lambda ids, T, H, nbytes: lib.moe_prefetch_ffn_weights(ids, T, 2, ctypes.byref(pl), FAKE,
+                                                                 H, 128, nbytes, None)
+    assert pf(FAKE, -1, 256, 1 << 20) == 1
+    assert pf(FAKE, 8, 300, 1 << 20) == 2
+    assert pf(None, 8, 256, 1 << 20) == 1
+    assert pf(FAKE, 8, 256, 1000) == 0
+    assert pf(FAKE, 0, 256, 1 << 20) == 0
     # watchdog self-test: 1 us <= limit <= 2 s, a workspace with its status block
     assert lib.moe_selftest_wait_timeout(FAKE, 256, 0, None, None) == 1
     assert lib.moe_selftest_wait_timeout(FAKE, 256, 2_000_001, None, None) == 1

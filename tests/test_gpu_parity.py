@@ -903,6 +903,47 @@ def test_combine_merged_figure4_counts():
 
 
 # ------------------------------------------------------------------ whole step as a CUDA graph
+@pytest.mark.parametrize("name", ALL)
+def test_weight_prefetch_is_only_a_hint(name):
+    """moe_prefetch_ffn_weights derives the grouped FFN's first-wave tiles
+    from the routed ids and asks L2 for their weights: it runs cleanly on
+    every workload's routing and placement (full-size packed weights, so
+    every fetched address is in bounds), and where the layer uses it (small
+    dispatches: tiny, decode) the output bits are those of a step without it."""
+    from grouped_ffn_gb300 import MoELayer
+    m = moe()
+    w = wl.WORKLOADS[name]
+    pl = wl.make_placement(w)
+    dp = m.DevicePlacement.from_tables(pl)
+    logits = wl.make_logits(w, "cuda")
+    ids = torch.empty(w.T, w.k, dtype=torch.int32, device="cuda")
+    tw = torch.empty(w.T, w.k, dtype=torch.float32, device="cuda")
+    ws = m.new_workspace(w.T, w.k, dp.n_slots)
+    m.moe_route(logits, route_cfg(w), ids, tw, ws)
+    wgu = torch.empty(w.E, 2 * w.I, w.H, dtype=torch.bfloat16, device="cuda")
+    m.moe_prefetch_ffn_weights(ids, dp, wgu, w.H, w.I, 64 << 20)
+    torch.cuda.synchronize()
+    m.moe_check_device_status(ws)
+    del wgu
+    if w.T * w.k * w.H * 2 > MoELayer.PREFETCH_MAX_DISPATCH:
+        return
+    x = wl.make_x(w, "cuda")
+    layer = MoELayer(H=w.H, I=w.I, E=w.E, k=w.k, placement=dp,
+                     w_gate_up=wl.make_w_gate_up(w, "cuda"), w_down=wl.make_w_down(w, "cuda"),
+                     max_tokens=w.T, score_fn=w.score_fn, n_groups=w.n_groups,
+                     topk_groups=w.topk_groups, group_topn=w.group_topn)
+    assert layer.prefetch_bytes > 0
+    y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    layer.forward(logits, x, y)
+    with_prefetch = y.clone()
+    layer.prefetch_bytes = 0
+    y.zero_()
+    layer.forward(logits, x, y)
+    torch.cuda.synchronize()
+    layer.check()
+    assert torch.equal(y, with_prefetch)
+
+
 @pytest.mark.parametrize("name", ["decode", "group_limited", "replica"])
 def test_graph_replay_matches_eager(name):
     """The step records into one CUDA graph (cooperative FFN, programmatic
