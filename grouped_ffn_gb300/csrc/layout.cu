@@ -54,6 +54,9 @@ struct LayoutArgs {
   const int32_t *slot_in;   // kModeSlots: the chosen slot of each assignment
   const int32_t *rkey;      // kModeKeys: [E] replicated-expert index or -1
   int32_t *key_totals;      // kModeKeys: [K] assignments per key
+  // One tile only (and a contiguous layout): the scan CTA also does the
+  // finalize's work, with no look-back flags written and no second launch.
+  int32_t fused_finalize;
 };
 
 // What the scan counts and ranks: the slot given by the fixed replica rule,
@@ -207,7 +210,9 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
     uint32_t *my_flag = p.tile_flags + (size_t)tile * K + s;
     int prefix = 0;
     bool ok = true;
-    if (tile == 0) {
+    if (p.fused_finalize) {
+      // the only tile: no other CTA reads a flag
+    } else if (tile == 0) {
       moe::st_relaxed_u32(my_flag, kFlagInc | (uint32_t)run);
     } else {
       moe::st_relaxed_u32(my_flag, kFlagAgg | (uint32_t)run);
@@ -237,15 +242,45 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
     tile_prefix[s] = prefix;
   }
   __syncthreads();
+  if (MODE != kModeKeys && p.fused_finalize && warp == 0) {
+    // the only tile's per-slot totals are final: their exclusive scan is
+    // the segment offsets, which take the place of the (zero) tile prefix
+    const int per = (K + 31) / 32;
+    const int lo = lane * per, hi = min(K, lo + per);
+    int sum = 0;
+    for (int s = lo; s < hi; ++s) sum += tile_agg[s];
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int run = incl - sum;
+    for (int s = lo; s < hi; ++s) {
+      tile_prefix[s] = run;
+      run += tile_agg[s];
+    }
+  }
+  __syncthreads();
 
-  // ---- partial ranks (slot modes: seg_offsets added by the finalize kernel)
+  // ---- ranks: partial (seg_offsets added by the finalize kernel), or final
+  // with the inverse permutation when this CTA finalizes too
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
     const int64_t a = base + r * 32 + lane;
     if (a < p.A) {
       const int s = my_slot[r];
       if (MODE == kModeRule) p.slot[a] = s;
-      p.dest_row[a] = (s >= 0) ? tile_prefix[s] + whist[warp * K + s] + my_rank[r] : -1;
+      int d = (s >= 0) ? tile_prefix[s] + whist[warp * K + s] + my_rank[r] : -1;
+      if (MODE != kModeKeys && p.fused_finalize && d >= 0) {
+        if (d >= p.A) {
+          moe::report_error(p.status, MOE_ERR_DEVICE_INDEX, (int32_t)a, moe::K_LAYOUT_SCAN);
+          d = -1;
+        } else {
+          p.src_assign[d] = (int32_t)a;
+        }
+      }
+      p.dest_row[a] = d;
     }
   }
 
@@ -258,7 +293,7 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
   int32_t *tot = whist;  // reuse: [S] totals
   __syncthreads();
   for (int s = tid; s < p.S; s += kThreads) {
-    tot[s] = tile_prefix[s] + tile_agg[s];
+    tot[s] = p.fused_finalize ? tile_agg[s] : tile_prefix[s] + tile_agg[s];
     p.seg_counts[s] = tot[s];
   }
   for (int r = tid; r < p.R; r += kThreads) rload[r] = 0;
@@ -297,6 +332,8 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(LayoutArgs p) {
   }
   __syncthreads();
   for (int r = tid; r < p.R; r += kThreads) p.rank_counts[r] = rload[r];
+  // the finalize kernel would clear the ticket for the next call
+  if (p.fused_finalize && tid == 0) *p.ticket = 0;
 }
 
 // Adds seg_offsets to the partial ranks and writes the inverse permutation;
@@ -601,7 +638,8 @@ extern "C" moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, in
   const int64_t n_tiles = std::max<int64_t>(n_tiles_for(A), 1);
   char *wsb = static_cast<char *>(ws);
   // The ticket and flags are zero on entry: moe_workspace_init clears them
-  // once and every call's finalize kernel clears them again after use.
+  // once, and every call leaves them clear (the finalize kernel, or with a
+  // single tile the scan CTA itself, which writes no flag).
 
   LayoutArgs p{};
   p.topk_ids = topk_ids;
@@ -634,9 +672,11 @@ extern "C" moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, in
                              (int)smem) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
+  p.fused_finalize = n_tiles == 1 ? 1 : 0;
   if (moe_status s = moe_host::launch_pdl(layout_scan_kernel<kModeRule>, dim3((unsigned)n_tiles),
                                           dim3(kThreads), smem, st, p))
     return s;
+  if (p.fused_finalize) return MOE_OK;
   int64_t blocks = (std::max<int64_t>(A, n_tiles * p.K) + 255) / 256;
   const int64_t cap = (int64_t)moe_host::sm_count() * 8;
   if (blocks > cap) blocks = cap;
@@ -809,9 +849,12 @@ extern "C" moe_status moe_dispatch_layout_noalloc(const int32_t *topk_ids, int64
                              (int)smem) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
+  // one tile (this includes A == 0): the scan CTA finalizes and leaves the
+  // ticket and flags clear itself
+  p.fused_finalize = n_tiles == 1 ? 1 : 0;
   layout_scan_kernel<kModeRule><<<(unsigned)n_tiles, kThreads, smem, st>>>(p);
   if (moe_status s = moe_host::launch_status()) return s;
-  if (A > 0) {
+  if (!p.fused_finalize) {
     int64_t blocks = (A + 255) / 256;
     const int64_t cap = (int64_t)moe_host::sm_count() * 8;
     if (blocks > cap) blocks = cap;
@@ -976,9 +1019,11 @@ extern "C" moe_status moe_dispatch_layout_routed(const int32_t *topk_ids, const 
       cudaFuncSetAttribute(layout_scan_kernel<kModeSlots>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MOE_ERR_CUDA;
+  p.fused_finalize = p.n_tiles == 1 ? 1 : 0;
   if (moe_status s = moe_host::launch_pdl(layout_scan_kernel<kModeSlots>, dim3((unsigned)p.n_tiles),
                                           dim3(kThreads), smem, st, p))
     return s;
+  if (p.fused_finalize) return MOE_OK;
   int64_t blocks = (std::max<int64_t>(A, (int64_t)p.n_tiles * p.K) + 255) / 256;
   const int64_t cap = (int64_t)moe_host::sm_count() * 8;
   if (blocks > cap) blocks = cap;

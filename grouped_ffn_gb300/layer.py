@@ -142,9 +142,12 @@ class MoELayer:
             small and packed and not gather and masked_cap is None and replica_relax is None
             and placement.n_slots == placement.n_experts) else 0
         self._ev_route = torch.cuda.Event()
+        # the layout scan takes up to 4096 assignments in one CTA, which then
+        # also finalizes (no second launch) on the contiguous layout
+        one_tile = max_tokens * k <= 4096 and masked_cap is None
         self.launches_per_step = 7 + (1 if shared_w_gate_up is not None else 0) + \
             (4 if replica_relax is not None else 0) - (1 if gather else 0) + \
-            (1 if fp8_dispatch else 0) + (1 if self.prefetch_bytes else 0)
+            (1 if fp8_dispatch else 0) + (1 if self.prefetch_bytes else 0) - (1 if one_tile else 0)
 
     @staticmethod
     def _pack(w_gate_up, w_down):

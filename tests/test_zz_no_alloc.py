@@ -56,6 +56,37 @@ def test_noalloc_layout_matches_workspace_layout_on_consecutive_calls(first, sec
             assert torch.equal(r, g), name
 
 
+@pytest.mark.parametrize("name", ["prefill", "replica"])
+def test_layout_after_an_empty_call_on_the_same_scratch(name):
+    """A call with no assignments leaves the ticket and the look-back flags
+    clear (its single scan CTA finalizes and writes no flag), so a following
+    multi-tile call on the same scratch -- the library's fixed array, or a
+    workspace -- still gives the workspace layout of a fresh workspace."""
+    from grouped_ffn_gb300 import moe
+    w, ids = _ids(name, 7)
+    pl_dev = moe.DevicePlacement.from_tables(wl.make_placement(w))
+    fresh = moe.new_workspace(w.T, w.k, pl_dev.n_slots)
+    ref = _outputs(w.T, w.k, pl_dev)
+    moe.moe_dispatch_layout(ids, pl_dev, *ref, fresh)
+    # the library's scratch
+    moe.moe_dispatch_layout_noalloc(ids[:0], pl_dev, *_outputs(0, w.k, pl_dev))
+    got = _outputs(w.T, w.k, pl_dev)
+    status = torch.zeros(3, dtype=torch.int32, device="cuda")
+    moe.moe_dispatch_layout_noalloc(ids, pl_dev, *got, status=status)
+    torch.cuda.synchronize()
+    assert status.tolist() == [0, 0, 0]
+    for r, g in zip(ref, got):
+        assert torch.equal(r, g), name
+    # a workspace
+    ws = moe.new_workspace(w.T, w.k, pl_dev.n_slots)
+    moe.moe_dispatch_layout(ids[:0], pl_dev, *_outputs(0, w.k, pl_dev), ws)
+    got = _outputs(w.T, w.k, pl_dev)
+    moe.moe_dispatch_layout(ids, pl_dev, *got, ws)
+    moe.moe_check_device_status(ws)
+    for r, g in zip(ref, got):
+        assert torch.equal(r, g), name
+
+
 def test_noalloc_layout_rejects_requests_beyond_its_scratch():
     from grouped_ffn_gb300 import moe
     # 1024 slots x 256 tiles of 4096 assignments needs more than 262144 flag words
