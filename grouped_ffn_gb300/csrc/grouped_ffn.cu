@@ -100,6 +100,7 @@ struct FfnParams {
   int32_t n_phases;   // 2: phase 1 reads what phase 0 writes, in the same launch
   int32_t *ready;     // [S] finished phase-0 tiles per segment (zeroed by the host)
   int32_t interleave; // merge multi-tile and one-tile segments' tiles (tile_order.cuh)
+  int32_t ph1_shift;  // phase-1 positions that go first to the CTAs with one gate/up tile fewer
   // Gather mode: phase 0 reads row r of a segment from x[gather_src[r] / gather_k]
   // (token rows, gather_T of them) instead of a permuted copy.
   const int32_t *gather_src;
@@ -356,46 +357,31 @@ struct TileInfo {
   int ph, s, n_blk, m_blk;
 };
 
-// Tiles [0, T0) are phase 0, [T0, T0 + T1) phase 1.  Within a phase the
-// hot stream (segments with two or more m-blocks, whose weight tiles are
+// Phase 0 (gate/up) and phase 1 (down) each order their tiles by merging
+// the hot stream (segments with two or more m-blocks, whose weight tiles are
 // re-read from L2 and so lean on the tensor cores) and the cold stream
-// (one-block segments, which stream fresh weights from HBM) are merged in
-// proportion to their lengths, so that every wave of CTAs mixes both kinds
-// of work (tile_order.cuh).  A CTA takes tiles blockIdx.x, + gridDim.x, ...;
-// each role walks that sequence with additions only, since a division per
-// tile on the producer's single thread stalled the k-block pipeline at
-// every tile boundary.
+// (one-block segments, which stream fresh weights from HBM) in proportion
+// to their lengths, so that every wave of CTAs mixes both kinds of work.
+// A CTA takes phase-0 positions blockIdx.x, + gridDim.x, ..., then its
+// phase-1 positions, shifted so that CTAs which took one more gate/up tile
+// take about as many fewer down tiles (tile_order.cuh, Ph1Plan).  Each role
+// walks that sequence with additions only: a division per tile on the
+// producer's single thread stalled the k-block pipeline at every tile
+// boundary.
 struct TileWalk {
-  tile_order::MergedWalk w;
-  int64_t t, T0, Mh, Mc;
-  int NB0, NB1;
+  tile_order::CtaWalk w;
 
-  __device__ __forceinline__ void start(int64_t t_first, int64_t T0_, int64_t Mh_, int64_t Mc_,
-                                        int NB0_, int NB1_) {
-    t = t_first;
-    T0 = T0_;
-    Mh = Mh_;
-    Mc = Mc_;
-    NB0 = NB0_;
-    NB1 = NB1_;
-    if (t < T0)
-      w.start(t, gridDim.x, Mh, Mc, NB0);
-    else
-      w.start(t - T0, gridDim.x, Mh, Mc, NB1);
+  __device__ __forceinline__ void start(int64_t Mh, int64_t Mc, int NB0, int NB1, int shift) {
+    w.start(blockIdx.x, gridDim.x, Mh, Mc, NB0, NB1, shift);
   }
-  __device__ __forceinline__ void next() {
-    const bool was0 = t < T0;
-    t += gridDim.x;
-    if (was0 && t >= T0)
-      w.start(t - T0, gridDim.x, Mh, Mc, NB1);  // first tile of phase 1
-    else
-      w.advance();
-  }
+  __device__ __forceinline__ bool valid() const { return w.valid(); }
+  __device__ __forceinline__ void next() { w.next(); }
+  __device__ __forceinline__ int phase() const { return w.ph; }
   __device__ __forceinline__ TileInfo info(const int32_t *pre_h, const int32_t *pre_c,
                                            int S) const {
     TileInfo ti;
-    ti.ph = t < T0 ? 0 : 1;
-    w.tile(pre_h, pre_c, S, ti.ph ? NB1 : NB0, ti.s, ti.n_blk, ti.m_blk);
+    ti.ph = w.ph;
+    w.tile(pre_h, pre_c, S, ti.s, ti.n_blk, ti.m_blk);
     return ti;
   }
 };
@@ -507,9 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int NB0 = p.ph[0].n_blocks;
   const int NB1 = p.n_phases > 1 ? p.ph[1].n_blocks : 0;
   const int64_t Mh = pre_h[p.S], Mc = pre_c[p.S];
-  const int64_t mtot = Mh + Mc;
-  const int64_t T0 = mtot * NB0;
-  const int64_t total = T0 + mtot * NB1;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (lane 0;
@@ -582,12 +565,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     TileWalk walk;
-    walk.start(blockIdx.x, T0, Mh, Mc, NB0, NB1);
+    walk.start(Mh, Mc, NB0, NB1, p.ph1_shift);
     if (p.gather_src == nullptr) {
       // Lane 0 alone.  The next tile's loads are prepared right after the
       // current tile's first stage is issued, while the ring is full, so
       // that its first stage goes out as soon as a slot frees.
-      if (lane == 0 && walk.t < total) {
+      if (lane == 0 && walk.valid()) {
         Loads cur = prepare(walk.info(pre_h, pre_c, p.S));
         for (;;) {
           if (cur.ph == 1 && !wait_h(cur)) {
@@ -603,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (kb == 0) {
               walk.next();
-              more = walk.t < total;
+              more = walk.valid();
               if (more) nxt = prepare(walk.info(pre_h, pre_c, p.S));
             }
           }
@@ -617,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // four-row gather (the TMA requests go out in parallel, not from one
       // thread in turn), lane 0 the two weight loads.  Phase-1 tiles load as
       // above, from lane 0.
-      for (; walk.t < total; walk.next()) {
+      for (; walk.valid(); walk.next()) {
         const TileInfo ti = walk.info(pre_h, pre_c, p.S);
         const Loads L = prepare(ti);
         if (ti.ph == 1) {
@@ -684,8 +667,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const int nk = p.ph[t < T0 ? 0 : 1].K / kBK;
+      TileWalk walk;
+      walk.start(Mh, Mc, NB0, NB1, p.ph1_shift);
+      for (; walk.valid() && ok; walk.next()) {
+        const int nk = p.ph[walk.phase()].K / kBK;
         if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, p.status, kid)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
@@ -722,8 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     TileWalk walk;
-    walk.start(blockIdx.x, T0, Mh, Mc, NB0, NB1);
-    for (; walk.t < total; walk.next()) {
+    walk.start(Mh, Mc, NB0, NB1, p.ph1_shift);
+    for (; walk.valid(); walk.next()) {
       const TileInfo ti = walk.info(pre_h, pre_c, p.S);
       const Phase &P = p.ph[ti.ph];
       const int row = seg_off[ti.s] + ti.m_blk * kBM + r_in;
@@ -823,6 +808,16 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Phase-1 shift (Ph1Plan's delta): the given default, or MOE_FFN_PH1_SHIFT
+// for comparison runs.
+int ph1_shift(int dflt) {
+  static int v = [] {
+    const char *e = getenv("MOE_FFN_PH1_SHIFT");
+    return e ? atoi(e) : -1;
+  }();
+  return v >= 0 ? v : dflt;
 }
 
 // Tile order: 1 (default) merges multi-tile and one-tile segments
@@ -968,6 +963,8 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   p.ready = ready;
   p.status = moe_host::status_ptr(ws);
   p.interleave = interleave_tiles();
+  // a gate/up tile (depth H) takes about H/I down tiles' time (depth I)
+  p.ph1_shift = ph1_shift((H + I / 2) / I);
   p.gather_src = gather_src;
   p.gather_k = gather_k;
   p.gather_T = (int32_t)gather_T;

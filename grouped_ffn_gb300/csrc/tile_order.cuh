@@ -108,4 +108,116 @@ struct MergedWalk {
   }
 };
 
+// Which merged positions of the down-projection phase (phase 1) CTA c of G
+// takes.  Phase 0 hands position u to CTA u mod G, so with T0 = q*G + r0
+// tiles the first r0 CTAs take one tile more (about K0/K1 phase-1 tiles'
+// worth of work, K the GEMMs' depths) and reach phase 1 late.  The first
+// PA = min(delta * (G - r0), T1) phase-1 positions therefore go round-robin
+// to the G - r0 CTAs that arrive early (delta each), and the rest to all G
+// CTAs in turn:
+//   v <  PA:  CTA r0 + (v mod (G - r0))
+//   v >= PA:  CTA (v - PA) mod G
+// With r0 = 0 or delta = 0 this is plain round-robin.  A CTA's positions
+// rise, and every position has exactly one CTA.
+struct Ph1Plan {
+  int64_t T1, PA;
+  int G, r0;
+
+  TILE_ORDER_HD void init(int64_t T0, int64_t T1_, int G_, int delta) {
+    T1 = T1_;
+    G = G_;
+    r0 = (int)(T0 % G_);
+    const int64_t pa = (r0 > 0 && delta > 0) ? (int64_t)delta * (G_ - r0) : 0;
+    PA = pa < T1_ ? pa : T1_;
+  }
+  // First position of CTA c and its step (first leg: v < PA).
+  TILE_ORDER_HD bool first_leg(int c, int64_t &v0, int64_t &step) const {
+    if (c < r0 || PA == 0 || c - r0 >= PA) return false;
+    v0 = c - r0;
+    step = G - r0;
+    return true;
+  }
+  TILE_ORDER_HD void second_leg(int c, int64_t &v0, int64_t &step) const {
+    v0 = PA + c;
+    step = G;
+  }
+};
+
+// The tiles of CTA c of G over both phases, in its order: phase-0
+// positions c, c + G, ... below T0 = (Mh + Mc) * NB0, then its phase-1
+// positions by Ph1Plan (T1 = (Mh + Mc) * NB1).  Additions per step; a
+// division when a leg starts.
+struct CtaWalk {
+  MergedWalk w;
+  Ph1Plan plan;
+  int64_t T0, Mh, Mc, step, leg_end;
+  int NB0, NB1, c, G, ph, leg;
+  bool done;
+
+  TILE_ORDER_HD void start(int c_, int G_, int64_t Mh_, int64_t Mc_, int NB0_, int NB1_,
+                           int delta) {
+    c = c_;
+    G = G_;
+    Mh = Mh_;
+    Mc = Mc_;
+    NB0 = NB0_;
+    NB1 = NB1_;
+    T0 = (Mh + Mc) * NB0;
+    plan.init(T0, (Mh + Mc) * NB1, G, delta);
+    done = false;
+    if (c < T0) {
+      ph = 0;
+      step = G;
+      leg_end = T0;
+      w.start(c, G, Mh, Mc, NB0);
+    } else {
+      enter_ph1();
+    }
+  }
+  TILE_ORDER_HD void enter_ph1() {
+    ph = 1;
+    int64_t v0;
+    if (plan.first_leg(c, v0, step)) {
+      leg = 0;
+      leg_end = plan.PA;
+    } else {
+      leg = 1;
+      plan.second_leg(c, v0, step);
+      leg_end = plan.T1;
+    }
+    if (v0 >= leg_end) {
+      done = true;
+      return;
+    }
+    w.start(v0, step, Mh, Mc, NB1);
+  }
+  TILE_ORDER_HD void next() {
+    if (w.u + step < leg_end) {
+      w.advance();
+      return;
+    }
+    if (ph == 0) {
+      enter_ph1();
+    } else if (leg == 0) {
+      leg = 1;
+      int64_t v0;
+      plan.second_leg(c, v0, step);
+      leg_end = plan.T1;
+      if (v0 >= leg_end)
+        done = true;
+      else
+        w.start(v0, step, Mh, Mc, NB1);
+    } else {
+      done = true;
+    }
+  }
+  TILE_ORDER_HD bool valid() const { return !done; }
+  // Position within the current phase.
+  TILE_ORDER_HD int64_t pos() const { return w.u; }
+  TILE_ORDER_HD void tile(const int32_t *pre_h, const int32_t *pre_c, int S, int &s, int &n_blk,
+                          int &m_blk) const {
+    w.tile(pre_h, pre_c, S, ph ? NB1 : NB0, s, n_blk, m_blk);
+  }
+};
+
 }  // namespace tile_order

@@ -96,6 +96,98 @@ static int check(const std::vector<int> &mt, int NB, bool interleave) {
   return 0;
 }
 
+// Every CTA's two-phase walk (CtaWalk): each phase-0 position once, by CTA
+// u mod G; each phase-1 position once, by the CTA Ph1Plan names; a CTA's
+// phase-0 tiles before its phase-1 tiles, positions rising within a phase;
+// the tile at each position is merged()'s; and with the first leg not cut
+// short, CTAs that reach phase 1 early take delta more phase-1 tiles (+-1).
+static int check_walks(const std::vector<int> &mt, int NB0, int NB1, int G, int delta) {
+  const int S = (int)mt.size();
+  std::vector<int32_t> pre_h(S + 1, 0), pre_c(S + 1, 0);
+  for (int s = 0; s < S; ++s) {
+    const bool hot = mt[s] >= 2;
+    pre_h[s + 1] = pre_h[s] + (hot ? mt[s] : 0);
+    pre_c[s + 1] = pre_c[s] + (hot ? 0 : mt[s]);
+  }
+  const int64_t Mh = pre_h[S], Mc = pre_c[S];
+  const int64_t T0 = (Mh + Mc) * NB0, T1 = (Mh + Mc) * NB1;
+  std::vector<int> seen0(T0, -1), seen1(T1, -1);
+  std::vector<int64_t> n1(G, 0);
+  tile_order::Ph1Plan plan;
+  plan.init(T0, T1, G, delta);
+  for (int c = 0; c < G; ++c) {
+    tile_order::CtaWalk w;
+    w.start(c, G, Mh, Mc, NB0, NB1, delta);
+    int last_ph = 0;
+    int64_t last = -1;
+    for (int guard = 0; w.valid(); w.next()) {
+      if (++guard > T0 + T1 + 2) {
+        std::printf("walk of CTA %d does not end\n", c);
+        return 1;
+      }
+      const int64_t u = w.pos();
+      if (w.ph < last_ph || (w.ph == last_ph && u <= last)) {
+        std::printf("CTA %d: order broken at phase %d position %lld\n", c, w.ph, (long long)u);
+        return 1;
+      }
+      if (w.ph != last_ph) last = -1;
+      last_ph = w.ph;
+      last = u;
+      const int NB = w.ph ? NB1 : NB0;
+      int s0, n0, m0, s1, nn1, m1;
+      tile_order::merged(u, pre_h.data(), pre_c.data(), S, NB, Mh, Mc, s0, n0, m0);
+      w.tile(pre_h.data(), pre_c.data(), S, s1, nn1, m1);
+      if (s0 != s1 || n0 != nn1 || m0 != m1) {
+        std::printf("CTA %d phase %d position %lld: tile differs from merged()\n", c, w.ph,
+                    (long long)u);
+        return 1;
+      }
+      if (w.ph == 0) {
+        if (u < 0 || u >= T0 || seen0[u] >= 0 || u % G != c) {
+          std::printf("phase-0 position %lld: bad owner %d\n", (long long)u, c);
+          return 1;
+        }
+        seen0[u] = c;
+      } else {
+        const int owner = u < plan.PA ? plan.r0 + (int)(u % (G - plan.r0))
+                                      : (int)((u - plan.PA) % G);
+        if (u < 0 || u >= T1 || seen1[u] >= 0 || owner != c) {
+          std::printf("phase-1 position %lld: bad owner %d (plan says %d)\n", (long long)u, c,
+                      owner);
+          return 1;
+        }
+        seen1[u] = c;
+        ++n1[c];
+      }
+    }
+  }
+  for (int64_t u = 0; u < T0; ++u)
+    if (seen0[u] < 0) {
+      std::printf("phase-0 position %lld never taken\n", (long long)u);
+      return 1;
+    }
+  for (int64_t u = 0; u < T1; ++u)
+    if (seen1[u] < 0) {
+      std::printf("phase-1 position %lld never taken\n", (long long)u);
+      return 1;
+    }
+  if (plan.r0 > 0 && plan.PA == (int64_t)delta * (G - plan.r0) && T1 >= plan.PA + G) {
+    int64_t lo_late = 1 << 30, hi_late = -1, lo_early = 1 << 30, hi_early = -1;
+    for (int c = 0; c < G; ++c) {
+      int64_t &lo = c < plan.r0 ? lo_late : lo_early, &hi = c < plan.r0 ? hi_late : hi_early;
+      if (n1[c] < lo) lo = n1[c];
+      if (n1[c] > hi) hi = n1[c];
+    }
+    if (lo_early - hi_late < delta - 1 || hi_early - lo_late > delta + 1) {
+      std::printf("phase-1 shares: late CTAs %lld..%lld, early %lld..%lld, delta %d\n",
+                  (long long)lo_late, (long long)hi_late, (long long)lo_early,
+                  (long long)hi_early, delta);
+      return 1;
+    }
+  }
+  return 0;
+}
+
 int main() {
   int cases = 0;
   // hand-made layouts: no hot segment, only hot segments, empty segments, one segment
@@ -119,6 +211,30 @@ int main() {
     ++cases;
     if (check(mt, NB, (it & 3) != 0)) return 1;
   }
+  // the two-phase walks of every CTA, over grids and shifts
+  for (int it = 0; it < 1500; ++it) {
+    const int S = 1 + (int)(next_u32() % 200);
+    std::vector<int> mt(S);
+    for (int s = 0; s < S; ++s) {
+      const uint32_t r = next_u32() % 100;
+      mt[s] = r < 10 ? 0 : (r < 70 ? 1 : 2 + (int)(next_u32() % (r < 95 ? 4 : 20)));
+    }
+    const int NB0 = 1 + (int)(next_u32() % 32), NB1 = 1 + (int)(next_u32() % 64);
+    const int grids[] = {1, 2, 7, 152, 160};
+    const int G = grids[next_u32() % 5];
+    const int delta = (int)(next_u32() % 6);
+    ++cases;
+    if (check_walks(mt, NB0, NB1, G, delta)) {
+      std::printf("  (S=%d NB0=%d NB1=%d G=%d delta=%d)\n", S, NB0, NB1, G, delta);
+      return 1;
+    }
+  }
+  for (const auto &mt : fixed)
+    for (int G : {1, 3, 152})
+      for (int delta : {0, 4}) {
+        ++cases;
+        if (check_walks(mt, 16, 32, G, delta)) return 1;
+      }
   std::printf("tile order ok: %d cases\n", cases);
   return 0;
 }
