@@ -626,6 +626,63 @@ def test_full_layer_sampled(name):
     assert layer.total.item() == tot == A
 
 
+def _random_workload(seed: int) -> wl.Workload:
+    """A seeded random small layer: hidden, intermediate, expert count, top-k,
+    tokens, ranks and skew vary; every third is group-limited (sigmoid), and
+    every fourth has a shared expert of the routed width (run in the routed
+    launch)."""
+    rng = np.random.default_rng(1000 + seed)
+    H = int(rng.choice([256, 512, 768, 1024]))
+    I = int(rng.choice([128, 256, 384, 512]))
+    if seed % 3 == 2:
+        n_groups = int(rng.choice([2, 4, 8]))
+        per = int(rng.choice([4, 8, 16]))
+        E = n_groups * per
+        topk_groups = int(rng.integers(1, n_groups + 1))
+        group_topn = int(rng.integers(1, min(3, per) + 1))
+        k = int(rng.integers(1, min(8, topk_groups * per) + 1))
+        score = wl.SCORE_SIGMOID
+    else:
+        E = int(rng.integers(1, 81))
+        k = int(rng.integers(1, min(8, E) + 1))
+        n_groups = topk_groups = group_topn = 1
+        score = wl.SCORE_SOFTMAX
+    R = int(rng.choice([1, 2, 4, 8]))
+    return wl.Workload(f"random{seed}", 100 + seed, T=int(rng.integers(1, 301)), H=H, E=E, k=k, I=I,
+                       R=R, ranks_per_node=R, score_fn=score, n_groups=n_groups,
+                       topk_groups=topk_groups, group_topn=group_topn,
+                       shared_I=I if seed % 4 == 1 else 0,
+                       zipf_s=float(rng.choice([0.0, 0.5, 1.0, 1.5])))
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_random_small_layers_against_the_oracle(seed):
+    """Seeded random small layers: every integer output bit-exact and every
+    token's output within tolerance of the oracle's token-by-token
+    definition.  Such layers have fewer FFN tiles than CTAs or a ragged last
+    wave, one-tile layouts, k = 1, single experts and empty experts."""
+    w = _random_workload(seed)
+    pl, logits, x, wgu, wd, sgu, sd, layer, y = _full_layer(w)
+    A = w.A
+    ids_ref, _, _ = oracle_route(w, logits.cpu().numpy())
+    assert np.array_equal(layer.topk_ids[: w.T].cpu().numpy(), ids_ref), w
+    lay = oracle.dispatch_layout(ids_ref, pl)
+    for key in ("seg_counts", "seg_offsets", "rank_counts"):
+        assert np.array_equal(getattr(layer, key).cpu().numpy(), lay[key]), (key, w)
+    assert np.array_equal(layer.dest_row[:A].cpu().numpy(), lay["dest_row"])
+    assert np.array_equal(layer.src_assign[:A].cpu().numpy(), lay["src_assign"])
+    cfg = dict(score_fn=w.score_fn, k=w.k, n_groups=w.n_groups, topk_groups=w.topk_groups,
+               group_topn=w.group_topn)
+    shared = None if sgu is None else (bits(sgu[0]), bits(sd[0]))
+    ref = oracle.moe_layer_tokens(np.arange(w.T), logits.cpu().numpy(), bits(x), _BitsExperts(wgu),
+                                  _BitsExperts(wd), pl, cfg, shared_w=shared, I=w.I,
+                                  shared_I=w.shared_I)
+    assert_close(f64(y), ref, f"layer output of {w}")
+    bal, mx, tot = oracle.balance_stats(lay["rank_counts"])
+    assert layer.balancedness.item() == bal and layer.max_count.item() == mx
+    assert layer.total.item() == tot == A
+
+
 class _BitsExperts:
     """Copies one expert's bf16 bits to the host on first use."""
 
