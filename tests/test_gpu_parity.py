@@ -683,6 +683,47 @@ def test_random_small_layers_against_the_oracle(seed):
     assert layer.total.item() == tot == A
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_random_small_layers_variants_are_bit_identical(seed):
+    """On the same random layers, every variant path gives the plain step's
+    output bits: rows gathered straight from x (no permute), the
+    fixed-capacity layout with a capacity no slot exceeds (no drops), plain
+    (unpacked) weights, the shared expert as a second launch, and the step
+    replayed as one CUDA graph."""
+    from grouped_ffn_gb300 import MoELayer
+    m = moe()
+    w = _random_workload(seed)
+    pl = wl.make_placement(w)
+    dp = m.DevicePlacement.from_tables(pl)
+    logits, x = wl.make_logits(w, "cuda"), wl.make_x(w, "cuda")
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    sgu, sd = wl.make_shared_weights(w, "cuda")
+
+    def run(**kw):
+        layer = MoELayer(H=w.H, I=w.I, E=w.E, k=w.k, placement=dp, w_gate_up=wgu, w_down=wd,
+                         max_tokens=w.T, score_fn=w.score_fn, n_groups=w.n_groups,
+                         topk_groups=w.topk_groups, group_topn=w.group_topn,
+                         shared_w_gate_up=sgu, shared_w_down=sd, **kw)
+        y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+        layer.forward(logits, x, y)
+        layer.check()
+        return layer, y
+
+    base_layer, base = run()
+    cap = max(1, int(base_layer.seg_counts.max().item()))
+    variants = {"unpacked": dict(packed=False), "two launches": dict(fuse_shared=False),
+                "gather": dict(gather=True), "fixed capacity %d" % cap: dict(masked_cap=cap)}
+    for name, kw in variants.items():
+        _, y = run(**kw)
+        assert torch.equal(y, base), (name, w)
+    graph = base_layer.capture(logits, x, base)
+    out = base.clone()
+    base.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(base, out), ("graph replay", w)
+
+
 class _BitsExperts:
     """Copies one expert's bf16 bits to the host on first use."""
 
