@@ -28,6 +28,9 @@
 //              hand a finished accumulator to the epilogue.
 //   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
 //              SwiGLU in fp32, bf16 stores masked to the segment.
+// A segment of at most 64 rows (not gathered) runs M = 64 tiles instead:
+// 64 A rows a stage and M = 64 MMAs, so a stage moves 40 KiB through shared
+// memory, and the epilogue takes rows from lanes 0..15 of each quadrant.
 // Double-buffered accumulators overlap a tile's epilogue with the next
 // tile's main loop.  Tiles are ordered (segment, n-block, m-block) so that
 // CTAs running side by side share B tiles (weights) and A rows in L2; a
@@ -65,6 +68,12 @@ constexpr size_t kReadyOff = moe::kFfnReadyOff;
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+// Segments of at most kBMSmall rows run M = 64 tiles: half the A tile is
+// loaded and read, so a stage moves 40 KiB through shared memory instead of
+// 48.  Their accumulator row r sits in TMEM lane 32 (r / 16) + r % 16
+// (16 rows in each warp's lane quadrant), column n in column n.
+constexpr int kBMSmall = 64;
+constexpr uint32_t kIdescSmall = (kIdesc & ~(0x1Fu << 24)) | ((uint32_t)(kBMSmall >> 4) << 24);
 
 struct __align__(8) Bars {
   uint64_t full[kStages];
@@ -76,7 +85,7 @@ struct __align__(8) Bars {
 
 constexpr size_t kBarsOff = (size_t)kStages * kStageBytes;
 constexpr size_t kMiscOff = kBarsOff + sizeof(Bars);
-constexpr size_t kSegOff = kMiscOff + 16;
+constexpr size_t kSegOff = kMiscOff + 32;
 constexpr size_t kGidxOff = kSegOff + (size_t)(5 * kMaxSegs + 3) * 4;  // [kBM] gathered token rows
 constexpr size_t kSmemBytes = kGidxOff + kBM * 4 + 1024;
 
@@ -101,6 +110,7 @@ struct FfnParams {
   int32_t *ready;     // [S] finished phase-0 tiles per segment (zeroed by the host)
   int32_t interleave; // merge multi-tile and one-tile segments' tiles (tile_order.cuh)
   int32_t ph1_shift;  // phase-1 positions that go first to the CTAs with one gate/up tile fewer
+  int32_t small_rows; // segments with at most this many rows run M = 64 tiles (0: none)
   // Gather mode: phase 0 reads row r of a segment from x[gather_src[r] / gather_k]
   // (token rows, gather_T of them) instead of a permuted copy.
   const int32_t *gather_src;
@@ -408,11 +418,47 @@ __device__ __forceinline__ void warp_exclusive_scan(int32_t *a, int n, int lane)
   if (lane == 31) a[n] = incl;
 }
 
+// Whether segment s runs M = 64 tiles (never with gathered rows).
+__device__ __forceinline__ bool small_segment(const FfnParams &p, const int32_t *seg_off,
+                                              const int32_t *seg_end, int s) {
+  return p.gather_src == nullptr && seg_end[s] - seg_off[s] <= p.small_rows;
+}
+
+// The k-block loop of one tile, with its instruction descriptor fixed at
+// compile time (one instantiation for M = 128 tiles, one for M = 64).
+// WAIT_FIRST false: the caller has waited for the first stage's full barrier.
+template <uint32_t IDESC, bool WAIT_FIRST>
+__device__ __forceinline__ bool mma_tile(int nk, uint32_t d_tmem, uint8_t *smem, Bars *bars,
+                                         int &stage, uint32_t &phase,
+                                         volatile int32_t *abort_flag, int32_t *status,
+                                         int32_t kid) {
+  for (int kb = 0; kb < nk; ++kb) {
+    if ((WAIT_FIRST || kb > 0) && !mbar_wait(&bars->full[stage], phase, abort_flag, status, kid))
+      return false;
+    tc_fence_after();
+    const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes);
+    const uint32_t sb = sa + kABytes;
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      umma_bf16(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), IDESC,
+                (kb | kk) != 0 ? 1u : 0u);
+    umma_commit(&bars->empty[stage]);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  return true;
+}
+
+// tmap_a0s / tmap_a1s: the A maps with 64-row boxes, for M = 64 tiles.
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmap_a0,
                        const __grid_constant__ CUtensorMap tmap_b0,
                        const __grid_constant__ CUtensorMap tmap_a1,
-                       const __grid_constant__ CUtensorMap tmap_b1, const FfnParams p) {
+                       const __grid_constant__ CUtensorMap tmap_b1,
+                       const __grid_constant__ CUtensorMap tmap_a0s,
+                       const __grid_constant__ CUtensorMap tmap_a1s, const FfnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -421,6 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + kMiscOff + 4);
   // the epilogue's shared go/stop decision, one per accumulator buffer
   volatile int32_t *epi_ok = reinterpret_cast<int32_t *>(smem + kMiscOff + 8);
+  // Per tile, in walk order mod 8 (only when the launch has M = 64 tiles,
+  // which gathered rows never do): 1 for an M = 64 tile.  The producer writes
+  // it before arming the tile's first stage and the MMA reads it after that
+  // stage's full barrier, which orders the two.  The producer runs at most
+  // kStages stages, so at most kStages tiles, ahead of the MMA: 8 entries
+  // are never overwritten before they are read.
+  uint8_t *tile_small = smem + kMiscOff + 16;
   int32_t *seg_off = reinterpret_cast<int32_t *>(smem + kSegOff);  // [S] first row of s
   int32_t *pre_h = seg_off + (kMaxSegs + 1);  // [S+1] m-tiles before s, multi-tile segments
   int32_t *pre_c = pre_h + (kMaxSegs + 1);    // [S+1] m-tiles before s, one-tile segments
@@ -450,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the next kernel on the stream (the combine) may start launching now; it
   // waits (griddepcontrol.wait) until this grid has finished
   moe::pdl_trigger();
+  int has_small = 0;
   for (int s = threadIdx.x; s < p.S; s += kThreads) {
     int lo, hi, e;
     if (s >= p.n_listed) {
@@ -482,8 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool hot = p.interleave && mt >= 2;
     pre_h[s] = hot ? mt : 0;
     pre_c[s] = hot ? 0 : mt;
+    if (mt > 0 && small_segment(p, seg_off, seg_end, s)) has_small = 1;
   }
-  __syncthreads();
+  // any M = 64 tile in this launch?  If not, every role runs the plain path.
+  const bool any_small = __syncthreads_or(has_small) != 0;
   if (warp == 0) warp_exclusive_scan(pre_h, p.S, lane);
   if (warp == 2) warp_exclusive_scan(pre_c, p.S, lane);
   tc_fence_before();
@@ -501,17 +557,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tmap_a0);
       prefetch_tmap(&tmap_b0);
+      if (p.small_rows > 0) prefetch_tmap(&tmap_a0s);
       if (p.n_phases > 1) {
         prefetch_tmap(&tmap_a1);
         prefetch_tmap(&tmap_b1);
+        if (p.small_rows > 0) prefetch_tmap(&tmap_a1s);
       }
     }
     int stage = 0;
-    uint32_t phase = 0, armed = 0, armed_par = 0;
+    uint32_t phase = 0, armed = 0, armed_par = 0, tile_seq = 0;
     bool ok = true;
     // Everything one tile's loads need, prepared by lane 0 from its TileInfo.
     struct Loads {
       int ph, s, nk, need, row_a, row_b0, row_b1, b_x_step, b_y_step;
+      bool small;  // an M = 64 tile: 64 A rows a stage
       uint64_t wpol;
     };
     auto prepare = [&](const TileInfo &ti) {
@@ -525,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       L.need = mt * NB0;  // phase-0 tiles of the segment, all of which store h
       const int e = seg_exp[ti.s];
       L.row_a = seg_off[ti.s] + ti.m_blk * kBM;
+      L.small = any_small && small_segment(p, seg_off, seg_end, ti.s);
       // a weight tile read by this m-block only need not stay in L2; one
       // that the segment's other m-blocks read too should
       L.wpol = mt >= 2 ? policy_evict_last() : policy_evict_first();
@@ -547,10 +607,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // k-block kb of a tile into the next ring stage (lane 0; tiled A rows).
     auto load_stage = [&](const Loads &L, int kb) {
       if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, p.status, kid)) return false;
-      const CUtensorMap *ma = L.ph ? &tmap_a1 : &tmap_a0;
+      const CUtensorMap *ma =
+          L.ph ? (L.small ? &tmap_a1s : &tmap_a1) : (L.small ? &tmap_a0s : &tmap_a0);
       const CUtensorMap *mb = L.ph ? &tmap_b1 : &tmap_b0;
       uint8_t *sa = smem + (size_t)stage * kStageBytes;
-      mbar_arrive_expect_tx(&bars->full[stage], kStageBytes);
+      if (any_small && kb == 0) tile_small[tile_seq++ & 7u] = L.small ? 1 : 0;
+      mbar_arrive_expect_tx(&bars->full[stage],
+                            L.small ? kStageBytes - kABytes / 2 : kStageBytes);
       tma_load_2d(sa, ma, kb * kBK, L.row_a, &bars->full[stage]);
       tma_load_2d_hint(sa + kABytes, mb, kb * L.b_x_step, L.row_b0 + kb * L.b_y_step,
                        &bars->full[stage], L.wpol);
@@ -667,6 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
+      uint32_t tile_seq = 0;
       TileWalk walk;
       walk.start(Mh, Mc, NB0, NB1, p.ph1_shift);
       for (; walk.valid() && ok; walk.next()) {
@@ -674,23 +738,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, p.status, kid)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&bars->full[stage], phase, abort_flag, p.status, kid)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes);
-          const uint32_t sb = sa + kABytes;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16(d_tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc,
-                      (kb | kk) != 0 ? 1u : 0u);
-          umma_commit(&bars->empty[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        if (!any_small) {
+          ok = mma_tile<kIdesc, true>(nk, d_tmem, smem, bars, stage, phase, abort_flag, p.status,
+                                      kid);
+        } else {
+          // the first stage has landed, so the producer's flag for this tile is visible
+          if (!mbar_wait(&bars->full[stage], phase, abort_flag, p.status, kid)) break;
+          ok = tile_small[tile_seq++ & 7u]
+                   ? mma_tile<kIdescSmall, false>(nk, d_tmem, smem, bars, stage, phase,
+                                                  abort_flag, p.status, kid)
+                   : mma_tile<kIdesc, false>(nk, d_tmem, smem, bars, stage, phase, abort_flag,
+                                             p.status, kid);
         }
         if (!ok) break;
         umma_commit(&bars->tfull[acc]);
@@ -703,7 +761,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------- epilogue warps 2..5
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int r_in = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     TileWalk walk;
@@ -711,6 +768,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (; walk.valid(); walk.next()) {
       const TileInfo ti = walk.info(pre_h, pre_c, p.S);
       const Phase &P = p.ph[ti.ph];
+      // tile row held by this thread's TMEM lane (M = 64 tiles: lanes 0..15
+      // of each quadrant; kBM, past every segment's end, for the others)
+      const int r_in = !(any_small && small_segment(p, seg_off, seg_end, ti.s)) ? q * 32 + lane
+                       : lane < 16                                               ? q * 16 + lane
+                                                                                 : kBM;
       const int row = seg_off[ti.s] + ti.m_blk * kBM + r_in;
       const bool valid = row < seg_end[ti.s];
       // One thread waits for the accumulator; all 128 then act on its verdict,
@@ -820,6 +882,16 @@ int ph1_shift(int dflt) {
   return v >= 0 ? v : dflt;
 }
 
+// M = 64 tiles for segments of at most 64 rows: 1 (default), or 0 from
+// MOE_FFN_SMALL_TILES=0 for comparison runs.
+int small_tiles() {
+  static int v = [] {
+    const char *e = getenv("MOE_FFN_SMALL_TILES");
+    return (e && e[0] == '0') ? 0 : 1;
+  }();
+  return v;
+}
+
 // Tile order: 1 (default) merges multi-tile and one-tile segments
 // (tile_order.cuh); MOE_FFN_INTERLEAVE=0 keeps plain segment order, for
 // comparison.
@@ -847,7 +919,8 @@ bool ensure_smem_attr() {
 // Cooperative launch: every CTA is resident at once, so a phase-1 tile that
 // waits for phase-0 tiles of other CTAs can always be satisfied.
 moe_status launch(const CUtensorMap &a0, const CUtensorMap &b0, const CUtensorMap &a1,
-                  const CUtensorMap &b1, const FfnParams &p, int64_t max_tiles, cudaStream_t st) {
+                  const CUtensorMap &b1, const CUtensorMap &a0s, const CUtensorMap &a1s,
+                  const FfnParams &p, int64_t max_tiles, cudaStream_t st) {
   int64_t grid = moe_host::sm_count();
   if (max_tiles < grid) grid = max_tiles;
   if (grid < 1) return MOE_OK;
@@ -861,7 +934,7 @@ moe_status launch(const CUtensorMap &a0, const CUtensorMap &b0, const CUtensorMa
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, grouped_ffn_kernel, a0, b0, a1, b1, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, grouped_ffn_kernel, a0, b0, a1, b1, a0s, a1s, p) != cudaSuccess)
     return MOE_ERR_CUDA;
   return moe_host::launch_status();
 }
@@ -930,7 +1003,7 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   if (n_rows == 0) return MOE_OK;
   if (!ensure_smem_attr()) return MOE_ERR_CUDA;
 
-  CUtensorMap m_x, m_wgu, m_h, m_wd;
+  CUtensorMap m_x, m_wgu, m_h, m_wd, m_xs, m_hs;
   const uint64_t gu_rows = packed ? (uint64_t)E * 2 * I * H / kBK : (uint64_t)E * 2 * I;
   const uint64_t gu_cols = packed ? (uint64_t)kBK : (uint64_t)H;
   const uint64_t d_rows = packed ? (uint64_t)E * H * I / kBK : (uint64_t)E * H;
@@ -940,6 +1013,9 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   if (!ok_x ||
       !make_map(&m_wgu, w_gate_up, gu_rows, gu_cols) ||
       !make_map(&m_h, h, (uint64_t)n_rows, (uint64_t)I) ||
+      !make_map(&m_xs, x_perm, gather_src ? (uint64_t)gather_T : (uint64_t)n_rows, (uint64_t)H,
+                kBMSmall) ||
+      !make_map(&m_hs, h, (uint64_t)n_rows, (uint64_t)I, kBMSmall) ||
       !make_map(&m_wd, w_down, d_rows, d_cols))
     return MOE_ERR_CUDA;
 
@@ -965,6 +1041,7 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   p.interleave = interleave_tiles();
   // a gate/up tile (depth H) takes about H/I down tiles' time (depth I)
   p.ph1_shift = ph1_shift((H + I / 2) / I);
+  p.small_rows = small_tiles() ? kBMSmall : 0;
   p.gather_src = gather_src;
   p.gather_k = gather_k;
   p.gather_T = (int32_t)gather_T;
@@ -990,7 +1067,8 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   d.out_ld = H;
   d.out_nblk_stride = 256;
   d.mode = 1;
-  return launch(m_x, m_wgu, m_h, m_wd, p, m_tiles_max * (g.n_blocks + d.n_blocks), st);
+  return launch(m_x, m_wgu, m_h, m_wd, m_xs, m_hs, p, m_tiles_max * (g.n_blocks + d.n_blocks),
+                st);
 }
 
 }  // namespace
