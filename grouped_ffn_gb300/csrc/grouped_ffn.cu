@@ -28,7 +28,8 @@
 //              hand a finished accumulator to the epilogue.
 //   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
 //              SwiGLU in fp32, bf16 stores masked to the segment.
-// A segment of at most 64 rows (not gathered) runs M = 64 tiles instead:
+// A tile with at most 64 rows left in its segment (a small segment, or the
+// last block of a longer one; rows not gathered) is an M = 64 tile instead:
 // 64 A rows a stage and M = 64 MMAs, so a stage moves 40 KiB through shared
 // memory, and the epilogue takes rows from lanes 0..15 of each quadrant.
 // Double-buffered accumulators overlap a tile's epilogue with the next
@@ -68,9 +69,9 @@ constexpr size_t kReadyOff = moe::kFfnReadyOff;
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-// Segments of at most kBMSmall rows run M = 64 tiles: half the A tile is
-// loaded and read, so a stage moves 40 KiB through shared memory instead of
-// 48.  Their accumulator row r sits in TMEM lane 32 (r / 16) + r % 16
+// Tiles with at most kBMSmall rows left in their segment run M = 64: half the
+// A tile is loaded and read, so a stage moves 40 KiB through shared memory
+// instead of 48.  Their accumulator row r sits in TMEM lane 32 (r / 16) + r % 16
 // (16 rows in each warp's lane quadrant), column n in column n.
 constexpr int kBMSmall = 64;
 constexpr uint32_t kIdescSmall = (kIdesc & ~(0x1Fu << 24)) | ((uint32_t)(kBMSmall >> 4) << 24);
@@ -418,10 +419,12 @@ __device__ __forceinline__ void warp_exclusive_scan(int32_t *a, int n, int lane)
   if (lane == 31) a[n] = incl;
 }
 
-// Whether segment s runs M = 64 tiles (never with gathered rows).
-__device__ __forceinline__ bool small_segment(const FfnParams &p, const int32_t *seg_off,
-                                              const int32_t *seg_end, int s) {
-  return p.gather_src == nullptr && seg_end[s] - seg_off[s] <= p.small_rows;
+// Whether m-block m_blk of segment s is an M = 64 tile: at most small_rows
+// rows from its first row to the segment's end (a one-block segment of at
+// most 64 rows, or the last block of a longer one), never with gathered rows.
+__device__ __forceinline__ bool small_tile(const FfnParams &p, const int32_t *seg_off,
+                                           const int32_t *seg_end, int s, int m_blk) {
+  return p.gather_src == nullptr && seg_end[s] - (seg_off[s] + m_blk * kBM) <= p.small_rows;
 }
 
 // The k-block loop of one tile, with its instruction descriptor fixed at
@@ -536,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool hot = p.interleave && mt >= 2;
     pre_h[s] = hot ? mt : 0;
     pre_c[s] = hot ? 0 : mt;
-    if (mt > 0 && small_segment(p, seg_off, seg_end, s)) has_small = 1;
+    if (mt > 0 && small_tile(p, seg_off, seg_end, s, mt - 1)) has_small = 1;
   }
   // any M = 64 tile in this launch?  If not, every role runs the plain path.
   const bool any_small = __syncthreads_or(has_small) != 0;
@@ -584,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       L.need = mt * NB0;  // phase-0 tiles of the segment, all of which store h
       const int e = seg_exp[ti.s];
       L.row_a = seg_off[ti.s] + ti.m_blk * kBM;
-      L.small = any_small && small_segment(p, seg_off, seg_end, ti.s);
+      L.small = any_small && small_tile(p, seg_off, seg_end, ti.s, ti.m_blk);
       // a weight tile read by this m-block only need not stay in L2; one
       // that the segment's other m-blocks read too should
       L.wpol = mt >= 2 ? policy_evict_last() : policy_evict_first();
@@ -770,9 +773,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Phase &P = p.ph[ti.ph];
       // tile row held by this thread's TMEM lane (M = 64 tiles: lanes 0..15
       // of each quadrant; kBM, past every segment's end, for the others)
-      const int r_in = !(any_small && small_segment(p, seg_off, seg_end, ti.s)) ? q * 32 + lane
-                       : lane < 16                                               ? q * 16 + lane
-                                                                                 : kBM;
+      const int r_in = !(any_small && small_tile(p, seg_off, seg_end, ti.s, ti.m_blk))
+                           ? q * 32 + lane
+                       : lane < 16 ? q * 16 + lane
+                                   : kBM;
       const int row = seg_off[ti.s] + ti.m_blk * kBM + r_in;
       const bool valid = row < seg_end[ti.s];
       // One thread waits for the accumulator; all 128 then act on its verdict,
