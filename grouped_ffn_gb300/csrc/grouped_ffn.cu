@@ -13,7 +13,7 @@
 //                      epilogue h = bf16(silu(acc[:, :128]) * acc[:, 128:])
 //   phase 1 (down):    acc[128 x 256] = h[128 x I] * Wd^T tile, epilogue bf16.
 // A segment's phase-1 tiles start once all its phase-0 tiles have stored
-// their h rows (a per-segment counter; bounded wait).  A 128-row tile
+// their h rows (a per-segment counter; bounded wait).  A tile (128 rows, or 64)
 // always starts at a segment's first row plus a multiple of 128 and uses
 // that segment's expert; rows past the segment's end are computed from
 // whatever follows (or TMA zero fill) and are never stored.
