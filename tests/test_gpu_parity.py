@@ -954,6 +954,45 @@ def test_gather_ffn_ragged_segments_match_oracle():
     assert_close(f64(y), ry, "y_perm (gather)")
 
 
+def test_ffn_tile_size_boundaries_match_oracle_and_gather_bits():
+    """Segments around the M = 64 rule (a tile runs M = 64 when at most 64
+    rows remain in its segment): 1, 16, 63, 64, 65, 127, 128 and 129 rows,
+    192 (a last block of exactly 64 rows), 193 (of 65) and 320.  Compared in
+    full with the oracle, and bit for bit with the gather path, whose tiles
+    are always 128 rows: a row's bits must not depend on the tile's M."""
+    m = moe()
+    H, I = 512, 256
+    counts = [1, 16, 63, 64, 65, 127, 128, 129, 192, 193, 320]
+    E = len(counts) + 1
+    A = sum(counts)
+    w = wl.Workload("m64", 81, T=A, H=H, E=E, k=1, I=I, R=1, ranks_per_node=1)
+    g = torch.Generator(device="cuda").manual_seed(23)
+    x = torch.randn(A, H, generator=g, device="cuda").to(torch.bfloat16)
+    src = torch.arange(A, dtype=torch.int32, device="cuda")   # row r reads token r
+    offs = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32, device="cuda")
+    se = torch.tensor([(5 * s + 3) % E for s in range(len(counts))], dtype=torch.int32, device="cuda")
+    wgu, wd = wl.make_w_gate_up(w, "cuda"), wl.make_w_down(w, "cuda")
+    pgu, pd = torch.empty_like(wgu), torch.empty_like(wd)
+    m.moe_pack_expert_weights(wgu, wd, pgu, pd)
+    ws = m.new_workspace(1, 1, len(counts))
+    outs = []
+    for gather in (False, True):
+        h = torch.full((A, I), float("nan"), dtype=torch.bfloat16, device="cuda")
+        y = torch.full((A, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        if gather:
+            m.moe_grouped_ffn_gather(x, 1, src, offs, se, pgu, pd, h, y, ws)
+        else:
+            m.moe_grouped_ffn_packed(x, offs, se, pgu, pd, h, y, ws)
+        m.moe_check_device_status(ws)
+        outs.append((h, y))
+    rh, ry = oracle.grouped_ffn(f64(x), offs.cpu().numpy(), se.cpu().numpy(),
+                                oracle.bf16_bits_to_f64(bits(wgu)), oracle.bf16_bits_to_f64(bits(wd)), I)
+    assert_close(f64(outs[0][0]), rh, "h")
+    assert_close(f64(outs[0][1]), ry, "y_perm")
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
+
+
 # ------------------------------------------------------------------ merge: node-local pre-reduction
 @pytest.mark.parametrize("name", ["decode", "group_limited", "replica"])
 def test_combine_merged_bit_exact_and_message_counts(name):
