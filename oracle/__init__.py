@@ -686,6 +686,108 @@ def route_replicas_waterfill(topk_ids: np.ndarray, pl, c_num: int, c_den: int):
     return slot, inter
 
 
+def refine_consolidate(topk_ids: np.ndarray, slot: np.ndarray, pl):
+    """Greedy refinement of a feasible replica routing ([Zepp] Section 5,
+    "Routing": starting from the water-filling's assignments, consolidate
+    each token's remote expert requests onto fewer nodes while keeping the
+    same load bounds; Section 1: remaining requests go to fewer remote
+    nodes).
+
+    Readings:
+      * The water-filling's counts M[i][p] (assignments of source rank i
+        served by replica p) stay fixed, so every replica's load, every
+        source's row total, the bounds of Eq. 1 and the number of
+        inter-node assignments are unchanged; only which of a source's
+        remote assignments takes which remote replica changes.
+      * Assignments that the water-filling served on the source's own node
+        keep their slot (its fill order gives the node-local copies to a
+        source's earliest assignments, and the refinement keeps that), as do
+        assignments of experts with one copy.
+      * Sources are independent (they share no counts).  Within source
+        rank i, tokens go in ascending order; each token's re-choosable
+        requests (replicated expert, remote copy) are covered greedily by
+        nodes: first a node the token already sends to (a fixed remote
+        request or an earlier choice), then the node covering the most of
+        its open requests, ties to the lower node id; a request takes the
+        lowest-rank copy of its expert on that node that still has count
+        left for source i.
+      * A source keeps its refined choices only if they do not raise its
+        number of distinct (token, remote node) pairs (the merged dispatch
+        messages of [Zepp] Section 4.2); otherwise its original ones.
+
+    Returns (slot [A] int32, pairs before, pairs after)."""
+    T, k = topk_ids.shape
+    A = T * k
+    ids = topk_ids.reshape(-1)
+    slot = np.asarray(slot, dtype=np.int32)
+    out = slot.copy()
+    rpn = pl.ranks_per_node
+    node_of = lambda r: int(r) // rpn
+    src_of = [int(pl.token_src_rank[t]) if pl.token_src_rank is not None else t % pl.n_ranks
+              for t in range(T)]
+    reps_of = [[int(s) for s in pl.rep_slots[pl.rep_offsets[e]:pl.rep_offsets[e + 1]]]
+               for e in range(pl.n_experts)]
+
+    def pairs(t, sl):
+        n_t = node_of(src_of[t])
+        return len({node_of(pl.slot_rank[sl[t * k + j]]) for j in range(k)} - {n_t})
+
+    before = after = 0
+    for i in range(pl.n_ranks):
+        toks = [t for t in range(T) if src_of[t] == i]
+        n_i = node_of(i)
+        # remaining count of source i's assignments per remote copy (slot)
+        left = {}
+        for t in toks:
+            for j in range(k):
+                a = t * k + j
+                e = int(ids[a])
+                s = int(slot[a])
+                if len(reps_of[e]) > 1 and node_of(pl.slot_rank[s]) != n_i:
+                    left[s] = left.get(s, 0) + 1
+        cand = slot.copy()
+        for t in toks:
+            used = set()
+            open_j = []
+            for j in range(k):
+                a = t * k + j
+                e = int(ids[a])
+                m = node_of(pl.slot_rank[int(slot[a])])
+                if m == n_i:
+                    continue
+                if len(reps_of[e]) > 1:
+                    open_j.append(j)
+                else:
+                    used.add(m)
+            while open_j:
+                cover = {}
+                for j in open_j:
+                    e = int(ids[t * k + j])
+                    for m in {node_of(pl.slot_rank[s]) for s in reps_of[e]
+                              if left.get(s, 0) > 0 and node_of(pl.slot_rank[s]) != n_i}:
+                        cover.setdefault(m, []).append(j)
+                best = min(cover, key=lambda m: (m not in used, -len(cover[m]), m))
+                for j in cover[best]:
+                    e = int(ids[t * k + j])
+                    s = min((s for s in reps_of[e]
+                             if left.get(s, 0) > 0 and node_of(pl.slot_rank[s]) == best),
+                            key=lambda s: int(pl.slot_rank[s]))
+                    left[s] -= 1
+                    cand[t * k + j] = s
+                used.add(best)
+                open_j = [j for j in open_j if j not in cover[best]]
+        b = sum(pairs(t, slot) for t in toks)
+        c = sum(pairs(t, cand) for t in toks)
+        before += b
+        if c <= b:
+            for t in toks:
+                out[t * k:(t + 1) * k] = cand[t * k:(t + 1) * k]
+            after += c
+        else:
+            after += b
+    return out, before, after
+
+
 # ------------------------------------------------------------------ merge (simulated)
 def dispatch_messages(slot: np.ndarray, pl, T: int, k: int):
     """Inter-node dispatch transfers of one step, before and after merge
