@@ -586,9 +586,11 @@ def parse_relax(text):
 
 
 def replica_sweep(w, dev, relax):
-    """Balancedness and inter-node assignments at each Zipf exponent of the
-    sweep, for the fixed replica rule and for water-filling routing (route +
-    layout only; the FFN result does not depend on the copy chosen)."""
+    """Balancedness, inter-node assignments and merged dispatch messages
+    (distinct (token, remote node) pairs) at each Zipf exponent of the
+    sweep, for the fixed replica rule, for water-filling routing and for
+    water-filling followed by the consolidation refinement (route + layout
+    only; the FFN result does not depend on the copy chosen)."""
     from grouped_ffn_gb300 import moe
     pl = wl.make_placement(w)
     pl_dev = moe.DevicePlacement.from_tables(pl, dev)
@@ -610,8 +612,13 @@ def replica_sweep(w, dev, relax):
         moe.moe_balance_stats(rc, bal, mx, tot)
         node = pl_dev.slot_rank[slot.long()] // w.ranks_per_node
         tok_node = (torch.arange(A, device=dev) // w.k % R) // w.ranks_per_node
+        remote = node != tok_node
+        tok = torch.arange(A, device=dev) // w.k
+        n_nodes = (R + w.ranks_per_node - 1) // w.ranks_per_node
+        fixed_msgs = int(torch.unique(tok[remote] * n_nodes + node[remote]).numel())
         rec["fixed_rule"] = {"balancedness": float(bal.item()), "max_rank_load": int(mx.item()),
-                             "inter_node": int((node != tok_node).sum().item())}
+                             "inter_node": int(remote.sum().item()),
+                             "messages_after_merge": fixed_msgs}
         inter = i32(1)
         moe.moe_route_replicas(ids, pl_dev, relax[0], relax[1], slot, inter, ws)
         moe.moe_dispatch_layout_routed(ids, slot, pl_dev, counts, offs, dest, src, rc, ws)
@@ -619,6 +626,23 @@ def replica_sweep(w, dev, relax):
         moe.moe_check_device_status(ws)
         rec["waterfill"] = {"relax_C": relax[0] / relax[1], "balancedness": float(bal.item()),
                             "max_rank_load": int(mx.item()), "inter_node": int(inter.item())}
+        # the greedy consolidation of each token's remote requests, timed
+        msgs = i32(2)
+        stream = torch.cuda.current_stream(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        moe.moe_route_refine(ids, pl_dev, slot, msgs, ws, stream)
+        e1.record(stream)
+        moe.moe_dispatch_layout_routed(ids, slot, pl_dev, counts, offs, dest, src, rc, ws)
+        moe.moe_balance_stats(rc, bal, mx, tot)
+        moe.moe_check_device_status(ws)
+        before, after = (int(v) for v in msgs.cpu())
+        rec["waterfill"]["messages_after_merge"] = before
+        rec["waterfill_refined"] = {"balancedness": float(bal.item()),
+                                    "max_rank_load": int(mx.item()),
+                                    "inter_node": int(inter.item()),
+                                    "messages_after_merge": after,
+                                    "refine_us": round(e0.elapsed_time(e1) * 1e3, 1)}
         out.append(rec)
     return out
 

@@ -601,6 +601,247 @@ __global__ void route_assign_kernel(RouteArgs r, LayoutArgs p, int32_t *slot) {
   if ((threadIdx.x & 31) == 0 && inter) atomicAdd(r.inter_node, inter);
 }
 
+// "Zepp", Section 5 "Routing": starting from a feasible routing, a greedy
+// refinement consolidates each token's remote expert requests onto fewer
+// nodes within the same load bounds.  Each source rank's counts per copy
+// stay as given, so every copy's load, the bounds and the number of
+// inter-node assignments are unchanged; a request of a replicated expert
+// that was sent to a remote copy may move to another remote copy of its
+// expert whose count for this rank is not used up.  One CTA per source
+// rank: its tokens in ascending order; each token covers its open requests
+// node by node -- a node it already sends to first, then the node that
+// covers most of them, ties to the lower node id -- and a request takes the
+// lowest-rank copy on that node with count left.  The rank keeps the result
+// only if its (token, remote node) pairs do not rise.
+constexpr int kRefineThreads = 256;
+
+struct RefineArgs {
+  const int32_t *topk_ids;
+  const int32_t *token_src_rank;  // [T] or null: token t lives on rank t mod R
+  int64_t T;
+  int32_t k, E, S, R, rpn, n_nodes;
+  const int32_t *rep_offsets, *rep_slots, *slot_rank;
+  int32_t *slot;      // [A] in: the routing to refine; out: refined
+  int32_t *cand;      // [A] scratch: the refined slot of every open request
+  int32_t *messages;  // [2] (token, remote node) pairs before / after (accumulated)
+  int32_t *status;
+};
+
+// Shared memory (int32 words) of route_refine_kernel.
+inline size_t refine_smem_words(int E, int S, int n_nodes) {
+  return (size_t)(E + 1) + 3 * (size_t)S + 2 * (size_t)n_nodes + kRefineThreads + 16;
+}
+
+// Distinct values of v over the lanes in `mask` (every lane calls this).
+__device__ __forceinline__ int distinct_in(uint32_t mask, int v, int lane) {
+  const uint32_t grp = __match_any_sync(0xffffffffu, (mask >> lane) & 1u ? v : -1 - lane);
+  const bool first = ((mask >> lane) & 1u) && (__ffs(grp) - 1 == lane);
+  return __popc(__ballot_sync(0xffffffffu, first));
+}
+
+__global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs r) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
+  extern __shared__ int32_t rs[];
+  int32_t *rep_off = rs;                    // [E+1]
+  int32_t *rep_sl = rep_off + (r.E + 1);    // [S]
+  int32_t *slot_node = rep_sl + r.S;        // [S] node of each slot, -1 if invalid
+  int32_t *left = slot_node + r.S;          // [S] this rank's count left per remote copy
+  int32_t *cnt = left + r.S;                // [n_nodes] open requests a node covers
+  int32_t *used = cnt + r.n_nodes;          // [n_nodes] nodes the current token sends to
+  int32_t *list = used + r.n_nodes;         // [kRefineThreads] open tokens of a chunk
+  int32_t *misc = list + kRefineThreads;    // [1] pairs, [2] saved, [4..11] per-warp counts
+
+  const int i = blockIdx.x;  // source rank
+  const int n_i = i / r.rpn;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // placement tables, clamped so that no entry indexes outside them
+  for (int e = tid; e <= r.E; e += blockDim.x) rep_off[e] = min(max(r.rep_offsets[e], 0), r.S);
+  for (int s = tid; s < r.S; s += blockDim.x) {
+    const int v = r.rep_slots[s];
+    rep_sl[s] = (v >= 0 && v < r.S) ? v : -1;
+    const int rk = r.slot_rank[s];
+    slot_node[s] = (rk >= 0 && rk < r.R) ? rk / r.rpn : -1;
+    left[s] = 0;
+  }
+  for (int m = tid; m < r.n_nodes; m += blockDim.x) cnt[m] = used[m] = 0;
+  if (tid < 16) misc[tid] = 0;
+  __syncthreads();
+
+  const bool by_mod = r.token_src_rank == nullptr;
+  const int64_t n_pos = by_mod ? (r.T > i ? (r.T - 1 - i) / r.R + 1 : 0) : r.T;
+  auto token_of = [&](int64_t u) { return by_mod ? i + u * r.R : u; };
+  auto belongs = [&](int64_t u) { return by_mod || __ldg(r.token_src_rank + u) == i; };
+  // request a of this rank: its slot's node, and whether it may move
+  auto classify = [&](int64_t a, int &s, int &m, bool &open) {
+    const int e = __ldg(r.topk_ids + a);
+    s = r.slot[a];
+    m = (s >= 0 && s < r.S) ? slot_node[s] : -1;
+    const bool remote = m >= 0 && m != n_i;
+    open = remote && e >= 0 && e < r.E && rep_off[e + 1] - rep_off[e] > 1;
+    if (!remote) m = -1;
+  };
+
+  // pass 1: this rank's count per remote copy, and its pairs before
+  int pairs = 0;
+  for (int64_t u = tid; u < n_pos; u += blockDim.x) {
+    if (!belongs(u)) continue;
+    const int64_t t = token_of(u);
+    int nodes[32];
+    int nd = 0;
+    for (int j = 0; j < r.k; ++j) {
+      int s, m;
+      bool open;
+      classify(t * r.k + j, s, m, open);
+      if (open) atomicAdd(&left[s], 1);
+      if (m < 0) continue;
+      bool seen = false;
+      for (int q = 0; q < nd; ++q) seen |= nodes[q] == m;
+      if (!seen) nodes[nd++] = m;
+    }
+    pairs += nd;
+  }
+  atomicAdd(&misc[1], pairs);
+  __syncthreads();
+
+  // pass 2: chunks of positions; warp 0 refines the chunk's open tokens in order
+  int delta = 0;  // pairs saved (warp 0, lane 0)
+  for (int64_t base = 0; base < n_pos; base += blockDim.x) {
+    const int64_t u = base + tid;
+    bool has_open = false;
+    if (u < n_pos && belongs(u)) {
+      const int64_t t = token_of(u);
+      for (int j = 0; j < r.k && !has_open; ++j) {
+        int s, m;
+        classify(t * r.k + j, s, m, has_open);
+      }
+    }
+    // compact the chunk's open tokens in ascending position: per-warp counts,
+    // then each warp's offset is the sum of the lower warps' counts
+    const uint32_t b = __ballot_sync(0xffffffffu, has_open);
+    if (lane == 0) misc[4 + warp] = __popc(b);
+    __syncthreads();
+    int wbase = 0, n_open = 0;
+    for (int w = 0; w < kRefineThreads / 32; ++w) {
+      wbase += w < warp ? misc[4 + w] : 0;
+      n_open += misc[4 + w];
+    }
+    if (has_open) list[wbase + __popc(b & ((1u << lane) - 1u))] = (int32_t)(u - base);
+    __syncthreads();
+    if (warp == 0) {
+      for (int q = 0; q < n_open; ++q) {
+        const int64_t t = token_of(base + list[q]);
+        const int64_t a = t * r.k + lane;
+        int s0 = -1, m0 = -1;
+        bool open = false;
+        const int e = lane < r.k ? __ldg(r.topk_ids + a) : -1;
+        if (lane < r.k) classify(a, s0, m0, open);
+        const uint32_t rem = __ballot_sync(0xffffffffu, m0 >= 0);
+        const int before = distinct_in(rem, m0, lane);
+        if (m0 >= 0 && !open) used[m0] = 1;  // fixed remote requests
+        __syncwarp();
+        int cur_s = s0, cur_m = m0;
+        uint32_t open_set = __ballot_sync(0xffffffffu, open);
+        const int lo = open ? rep_off[e] : 0, hi = open ? rep_off[e + 1] : 0;
+        while (open_set) {
+          const bool mine = (open_set >> lane) & 1u;
+          // count each candidate node once per request
+          if (mine)
+            for (int c = lo; c < hi; ++c) {
+              const int s2 = rep_sl[c];
+              const int m2 = s2 >= 0 ? slot_node[s2] : -1;
+              if (m2 < 0 || m2 == n_i || left[s2] <= 0) continue;
+              bool dup = false;
+              for (int c2 = lo; c2 < c; ++c2) {
+                const int s3 = rep_sl[c2];
+                dup |= s3 >= 0 && slot_node[s3] == m2 && left[s3] > 0;
+              }
+              if (!dup) atomicAdd(&cnt[m2], 1);
+            }
+          __syncwarp();
+          uint32_t key = 0xffffffffu;
+          if (mine)
+            for (int c = lo; c < hi; ++c) {
+              const int s2 = rep_sl[c];
+              const int m2 = s2 >= 0 ? slot_node[s2] : -1;
+              if (m2 < 0 || m2 == n_i || left[s2] <= 0) continue;
+              const uint32_t kk = ((used[m2] ? 1u : 0u) ^ 1u) << 16 |
+                                  (uint32_t)(32 - cnt[m2]) << 10 | (uint32_t)m2;
+              key = min(key, kk);
+            }
+          key = __reduce_min_sync(0xffffffffu, key);
+          __syncwarp();
+          if (mine)
+            for (int c = lo; c < hi; ++c)
+              if (rep_sl[c] >= 0 && slot_node[rep_sl[c]] >= 0) cnt[slot_node[rep_sl[c]]] = 0;
+          __syncwarp();
+          if (key == 0xffffffffu) {  // no copy left (inconsistent input)
+            if (lane == 0)
+              moe::report_error(r.status, MOE_ERR_PLACEMENT, (int32_t)t, moe::K_LAYOUT_FINALIZE);
+            break;
+          }
+          const int best = (int)(key & 1023u);
+          bool covers = false;
+          if (mine)
+            for (int c = lo; c < hi && !covers; ++c) {
+              const int s2 = rep_sl[c];
+              covers = s2 >= 0 && slot_node[s2] == best && left[s2] > 0;
+            }
+          // requests on `best` take their copies in ascending request order
+          uint32_t cov = __ballot_sync(0xffffffffu, covers), took = 0;
+          for (uint32_t cc = cov; cc; cc &= cc - 1) {
+            if (lane == __ffs(cc) - 1) {
+              for (int c = lo; c < hi; ++c) {
+                const int s2 = rep_sl[c];
+                if (s2 >= 0 && slot_node[s2] == best && left[s2] > 0) {
+                  left[s2] -= 1;
+                  cur_s = s2;
+                  cur_m = best;
+                  took = 1;
+                  break;
+                }
+              }
+            }
+            __syncwarp();
+          }
+          open_set &= ~__ballot_sync(0xffffffffu, took != 0);
+          if (lane == 0) used[best] = 1;
+          __syncwarp();
+        }
+        const int after = distinct_in(rem, cur_m, lane);
+        delta += before - after;
+        if (open) r.cand[a] = cur_s;
+        __syncwarp();
+        if (m0 >= 0) used[m0] = 0;
+        if (cur_m >= 0) used[cur_m] = 0;
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+  }
+  if (tid == 0) misc[2] = delta;
+  __syncthreads();
+  const int before = misc[1], saved = misc[2];
+  const bool keep = saved >= 0;
+  if (keep) {  // pass 3: move the open requests to their refined copies
+    for (int64_t u = tid; u < n_pos; u += blockDim.x) {
+      if (!belongs(u)) continue;
+      const int64_t t = token_of(u);
+      for (int j = 0; j < r.k; ++j) {
+        int s, m;
+        bool open;
+        const int64_t a = t * r.k + j;
+        classify(a, s, m, open);
+        if (open) r.slot[a] = r.cand[a];
+      }
+    }
+  }
+  if (tid == 0) {
+    atomicAdd(r.messages, before);
+    atomicAdd(r.messages + 1, keep ? before - saved : before);
+  }
+}
+
 
 
 constexpr size_t kTicketOff = moe::kLayoutTicketOff;
@@ -908,18 +1149,66 @@ moe_status check_placement(const moe_placement *pl, int64_t T, int32_t k) {
   return MOE_OK;
 }
 
-}  // namespace
-
-extern "C" size_t moe_route_replicas_workspace_size(int64_t T, int32_t k, int32_t n_experts,
-                                                    int32_t n_slots, int32_t n_ranks) {
-  if (T < 0 || k < 1 || n_experts < 1 || n_slots < 1 || n_ranks < 1) return 0;
+// Bytes of the replica routing's workspace before the refinement's scratch.
+size_t route_ws_bytes(int64_t T, int32_t k, int32_t n_experts, int32_t n_slots, int32_t n_ranks) {
   const int64_t Kx = n_slots > n_experts ? n_slots - n_experts : 0;
   // flags sized for the routing keys and for the slots of a following
   // layout call on the same workspace, so neither reaches the scratch tail
   const int64_t K = std::max<int64_t>(std::max<int64_t>(Kx * n_ranks, 1), n_slots);
   const int64_t tiles = std::max<int64_t>(n_tiles_for(T * (int64_t)k), 1);
-  return kFlagsOff + (size_t)(tiles * K) * sizeof(uint32_t) +
-         route_ws_words_after_flags(n_experts, n_slots, n_ranks) * sizeof(int32_t);
+  const size_t b = kFlagsOff + (size_t)(tiles * K) * sizeof(uint32_t) +
+                   route_ws_words_after_flags(n_experts, n_slots, n_ranks) * sizeof(int32_t);
+  return (b + 15) & ~(size_t)15;
+}
+
+}  // namespace
+
+extern "C" size_t moe_route_replicas_workspace_size(int64_t T, int32_t k, int32_t n_experts,
+                                                    int32_t n_slots, int32_t n_ranks) {
+  if (T < 0 || k < 1 || n_experts < 1 || n_slots < 1 || n_ranks < 1) return 0;
+  // + the refinement's scratch: one int32 per assignment
+  return route_ws_bytes(T, k, n_experts, n_slots, n_ranks) +
+         (size_t)(T * (int64_t)k) * sizeof(int32_t);
+}
+
+extern "C" moe_status moe_route_refine(const int32_t *topk_ids, int64_t T, int32_t k,
+                                       const moe_placement *pl, int32_t *slot, int32_t *messages,
+                                       void *ws, size_t ws_bytes, void *stream) {
+  if (moe_status s = check_placement(pl, T, k)) return s;
+  const int64_t A = T * (int64_t)k;
+  if (!messages || (A > 0 && (!topk_ids || !slot))) return MOE_ERR_INVALID_ARG;
+  if (k > 32) return MOE_ERR_UNSUPPORTED;
+  const size_t need = moe_route_replicas_workspace_size(T, k, pl->n_experts, pl->n_slots,
+                                                        pl->n_ranks);
+  if (moe_status s = moe_host::check_ws(ws, ws_bytes, need)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(messages, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (A == 0) return MOE_OK;
+  RefineArgs r{};
+  r.topk_ids = topk_ids;
+  r.token_src_rank = pl->token_src_rank;
+  r.T = T;
+  r.k = k;
+  r.E = pl->n_experts;
+  r.S = pl->n_slots;
+  r.R = pl->n_ranks;
+  r.rpn = pl->ranks_per_node;
+  r.n_nodes = (pl->n_ranks + pl->ranks_per_node - 1) / pl->ranks_per_node;
+  r.rep_offsets = pl->rep_offsets;
+  r.rep_slots = pl->rep_slots;
+  r.slot_rank = pl->slot_rank;
+  r.slot = slot;
+  r.cand = reinterpret_cast<int32_t *>(
+      static_cast<char *>(ws) + route_ws_bytes(T, k, pl->n_experts, pl->n_slots, pl->n_ranks));
+  r.messages = messages;
+  r.status = moe_host::status_ptr(ws);
+  const size_t smem = refine_smem_words(r.E, r.S, r.n_nodes) * sizeof(int32_t);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(route_refine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return moe_host::launch_pdl(route_refine_kernel, dim3((unsigned)r.R), dim3(kRefineThreads), smem,
+                              st, r);
 }
 
 extern "C" moe_status moe_route_replicas(const int32_t *topk_ids, int64_t T, int32_t k,

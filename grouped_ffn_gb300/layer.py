@@ -28,11 +28,15 @@ class MoELayer:
                  shared_w_gate_up: Optional[torch.Tensor] = None,
                  shared_w_down: Optional[torch.Tensor] = None, device="cuda",
                  packed: bool = True, replica_relax: Optional[tuple] = None,
-                 gather: bool = False, masked_cap: Optional[int] = None,
+                 replica_refine: bool = False, gather: bool = False,
+                 masked_cap: Optional[int] = None,
                  fp8_dispatch: bool = False, fuse_shared: bool = True):
         """replica_relax=(c_num, c_den) chooses each assignment's replica by
         locality-preferred water-filling with load bounds C = c_num/c_den
         (moe_route_replicas); None keeps the fixed replica rule.
+        replica_refine=True then consolidates each token's remote requests
+        onto fewer nodes with the same per-copy counts (moe_route_refine);
+        `messages` holds the (token, remote node) pairs before and after.
         gather=True reads the FFN's rows straight from x through the
         inverse permutation (moe_grouped_ffn_gather): no permute step.
         masked_cap=c uses the fixed-capacity layout (moe_dispatch_layout_masked):
@@ -117,7 +121,11 @@ class MoELayer:
         self._ev_layout = torch.cuda.Event()
         self._ev_stats = torch.cuda.Event()
         self.replica_relax = replica_relax
+        if replica_refine and replica_relax is None:
+            raise ValueError("replica_refine refines the water-filling routing (replica_relax)")
+        self.replica_refine = replica_refine
         self.inter_node = torch.zeros(1, **i32)
+        self.messages = torch.zeros(2, **i32)
         if self.fuse_shared:
             pass
         elif shared_w_gate_up is not None:
@@ -130,7 +138,8 @@ class MoELayer:
             self.shared_I = 0
         # per step: route, layout scan + finalize, permute, FFN, combine,
         # balance (+1 shared FFN, +4 replica routing: prep, key scan,
-        # water-fill, assign, +1 FP8 dequantization, +1 weight prefetch);
+        # water-fill, assign, +1 refinement, +1 FP8 dequantization, +1
+        # weight prefetch);
         # packing happens once, here
         # L2 prefetch of the FFN's first weight tiles, on the side stream
         # right after routing: worth it when the step is weight-bound and its
@@ -146,7 +155,8 @@ class MoELayer:
         # also finalizes (no second launch) on the contiguous layout
         one_tile = max_tokens * k <= 4096 and masked_cap is None
         self.launches_per_step = 7 + (1 if shared_w_gate_up is not None else 0) + \
-            (4 if replica_relax is not None else 0) - (1 if gather else 0) + \
+            (4 if replica_relax is not None else 0) + (1 if replica_refine else 0) - \
+            (1 if gather else 0) + \
             (1 if fp8_dispatch else 0) + (1 if self.prefetch_bytes else 0) - (1 if one_tile else 0)
 
     @staticmethod
@@ -191,6 +201,9 @@ class MoELayer:
         else:
             moe.moe_route_replicas(ids, self.placement, *self.replica_relax, self.slot[:A],
                                    self.inter_node, self.ws, stream)
+            if self.replica_refine:
+                moe.moe_route_refine(ids, self.placement, self.slot[:A], self.messages, self.ws,
+                                     stream)
             moe.moe_dispatch_layout_routed(ids, self.slot[:A], self.placement, self.seg_counts,
                                            self.seg_offsets, self.dest_row[:A],
                                            self.src_assign[:A], self.rank_counts, self.ws, stream)

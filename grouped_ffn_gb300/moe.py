@@ -71,6 +71,8 @@ _SIGNATURES = {
     "moe_route_replicas_workspace_size": (_SZ, [_I64, _I32, _I32, _I32, _I32]),
     "moe_route_replicas": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC), _I32, _I32,
                                           _P, _P, _P, _SZ, _P]),
+    "moe_route_refine": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC), _P, _P, _P,
+                                        _SZ, _P]),
     "moe_dispatch_layout_routed": (ctypes.c_int, [_P, _P, _I64, _I32, ctypes.POINTER(PlacementC),
                                                   _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
@@ -288,6 +290,19 @@ def moe_route_replicas(topk_ids, placement: DevicePlacement, c_num: int, c_den: 
     _check("moe_route_replicas", lib().moe_route_replicas(
         _ptr(topk_ids), T, k, ctypes.byref(placement.c), c_num, c_den, _ptr(slot),
         _ptr(inter_node), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_route_refine(topk_ids, placement: DevicePlacement, slot, messages, ws, stream=None):
+    """Consolidate each token's remote requests onto fewer nodes, in place on
+    slot (same per-copy counts); messages is a device int32[2] that receives
+    the (token, remote node) pairs before and after."""
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(slot, torch.int32, "slot")
+    _need(messages, torch.int32, "messages")
+    T, k = topk_ids.shape
+    _check("moe_route_refine", lib().moe_route_refine(
+        _ptr(topk_ids), T, k, ctypes.byref(placement.c), _ptr(slot), _ptr(messages), _ptr(ws),
+        ws.numel(), _stream(stream)))
 
 
 def moe_dispatch_layout_routed(topk_ids, slot_in, placement: DevicePlacement, seg_counts,

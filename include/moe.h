@@ -219,7 +219,7 @@ moe_status moe_dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k,
  *  - a source's assignments, in ascending assignment order, fill its
  *    destinations in locality order (own GPU, own node, remote).
  *  The refinement that consolidates a token's remote requests onto fewer
- *  nodes is not applied.
+ *  nodes is a separate call on this call's output, moe_route_refine.
  *  slot        device int32 [T*k] (output): the chosen slot per assignment.
  *  inter_node  device int32 scalar (output): assignments whose slot is on a
  *              node other than their token's.
@@ -234,6 +234,41 @@ moe_status moe_route_replicas(const int32_t *topk_ids, int64_t T, int32_t k,
                               const moe_placement *placement, int32_t c_num, int32_t c_den,
                               int32_t *slot, int32_t *inter_node, void *ws, size_t ws_bytes,
                               void *stream);
+
+/* Greedy refinement of a replica routing: consolidate each token's remote
+ * expert requests onto fewer nodes within the same load bounds.  "Zepp",
+ * Section 5, "Routing" (starting from the water-filling's feasible
+ * assignments, a greedy refinement moves a token's remote requests onto
+ * fewer nodes while the load bounds still hold) and Section 1 (remaining
+ * requests consolidated onto fewer remote nodes); the merged dispatch of
+ * Section 4.2 then sends a token once per remote node.  Readings fixed
+ * here:
+ *  - every source rank keeps its count of assignments per copy, so each
+ *    copy's load, the bounds of Eq. 1 and the number of inter-node
+ *    assignments are exactly those of the input routing; only which of a
+ *    source's requests that went to a remote copy of a replicated expert
+ *    takes which remote copy changes (node-local choices and experts with
+ *    one copy keep their slot);
+ *  - per source rank, tokens in ascending order; a token covers its open
+ *    requests node by node: a node it already sends to first, then the
+ *    node covering the most open requests, ties to the lower node id; a
+ *    request takes the lowest-rank copy on that node whose count for the
+ *    source is not used up;
+ *  - a source rank keeps the refined choices only if its number of
+ *    distinct (token, remote node) pairs does not rise.
+ *  slot      device int32 [T*k], in/out: a routing in which every slot hosts
+ *            its assignment's expert (for example moe_route_replicas's).
+ *  messages  device int32 [2] (output): distinct (token, remote node) pairs
+ *            before and after, i.e. the inter-node dispatch messages after
+ *            merging.
+ *  ws: moe_route_replicas_workspace_size(T, k, E, S, R) bytes (the same
+ *  workspace as moe_route_replicas; this call uses its last 4*T*k bytes).
+ *  Limits: k <= 32, the placement limits of moe_dispatch_layout.  Device
+ *  errors: MOE_ERR_PLACEMENT when a request finds no copy (input slots
+ *  that do not host their expert). */
+moe_status moe_route_refine(const int32_t *topk_ids, int64_t T, int32_t k,
+                            const moe_placement *placement, int32_t *slot, int32_t *messages,
+                            void *ws, size_t ws_bytes, void *stream);
 
 /* moe_dispatch_layout with each assignment's slot already chosen (for
  * example by moe_route_replicas) instead of the fixed replica rule; same

@@ -767,15 +767,19 @@ def refine_consolidate(topk_ids: np.ndarray, slot: np.ndarray, pl):
                               if left.get(s, 0) > 0 and node_of(pl.slot_rank[s]) != n_i}:
                         cover.setdefault(m, []).append(j)
                 best = min(cover, key=lambda m: (m not in used, -len(cover[m]), m))
+                taken = []
                 for j in cover[best]:
                     e = int(ids[t * k + j])
-                    s = min((s for s in reps_of[e]
-                             if left.get(s, 0) > 0 and node_of(pl.slot_rank[s]) == best),
-                            key=lambda s: int(pl.slot_rank[s]))
+                    on_best = [s for s in reps_of[e]
+                               if left.get(s, 0) > 0 and node_of(pl.slot_rank[s]) == best]
+                    if not on_best:      # only when a token repeats an expert id
+                        continue
+                    s = min(on_best, key=lambda s: int(pl.slot_rank[s]))
                     left[s] -= 1
                     cand[t * k + j] = s
+                    taken.append(j)
                 used.add(best)
-                open_j = [j for j in open_j if j not in cover[best]]
+                open_j = [j for j in open_j if j not in taken]
         b = sum(pairs(t, slot) for t in toks)
         c = sum(pairs(t, cand) for t in toks)
         before += b

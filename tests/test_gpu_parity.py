@@ -873,6 +873,98 @@ def test_route_replicas_skewed_sources_and_figure6():
     assert np.array_equal(slot.cpu().numpy(), ref_slot) and inter == ref_inter == 4
 
 
+def _gpu_refine(ids, pl_dev, slot, ws):
+    m = moe()
+    msgs = torch.full((2,), -9, dtype=torch.int32, device="cuda")
+    m.moe_route_refine(ids, pl_dev, slot, msgs, ws)
+    m.moe_check_device_status(ws)
+    return slot, tuple(int(v) for v in msgs.cpu())
+
+
+@pytest.mark.parametrize("zipf", [0.0, 0.5, 1.0, 1.5])
+def test_route_refine_parity_replica_workload(zipf):
+    """The consolidation refinement ("Zepp", Section 5) on the full replica
+    workload at each exponent of the sweep: slots and message counts
+    bit-exact against the oracle, per-copy loads unchanged, and the layout
+    from the refined slots on the same workspace."""
+    w = wl.WORKLOADS["replica"].with_zipf(zipf)
+    pl = wl.make_placement(w)
+    ids, _ = gpu_route(w, wl.make_logits(w, "cuda"))
+    ids_np = ids.cpu().numpy()
+    slot, inter, pl_dev, ws = _gpu_route_replicas(ids, pl, (1, 10))
+    ref_in, ref_inter = oracle.route_replicas_waterfill(ids_np, pl, 1, 10)
+    ref_slot, before, after = oracle.refine_consolidate(ids_np, ref_in, pl)
+    slot, msgs = _gpu_refine(ids, pl_dev, slot, ws)
+    assert np.array_equal(slot.cpu().numpy(), ref_slot)
+    assert msgs == (before, after) and after < before
+    assert np.array_equal(np.bincount(ref_slot, minlength=pl.n_slots),
+                          np.bincount(ref_in, minlength=pl.n_slots))
+    m = moe()
+    A, S, R = w.A, pl.n_slots, w.R
+    out = [torch.full((n,), -7, dtype=torch.int32, device="cuda") for n in (S, S + 1, A, A, R)]
+    m.moe_dispatch_layout_routed(ids, slot, pl_dev, *out, ws)
+    m.moe_check_device_status(ws)
+    ref = oracle.dispatch_layout_from_slots(ids_np, ref_slot, pl)
+    for key, t in zip(("seg_counts", "seg_offsets", "dest_row", "src_assign", "rank_counts"), out):
+        assert np.array_equal(t.cpu().numpy(), ref[key]), key
+
+
+def test_route_refine_hand_worked_and_explicit_sources():
+    """The hand-worked refinement cases of the oracle's pins, and a
+    replica-shaped layer with skewed explicit source ranks, on the GPU."""
+    cases = [([[1, 2], [2, 3], [0]], [[0, 1], [0, 2], [2, 1]], [2, 2, 1, 0, 0, 3], (4, 3)),
+             ([[1, 2], [1, 2], [0]], [[0, 1], [0, 2], [2, 1]], [1, 1, 2, 0, 0, 2], (3, 3)),
+             ([[1, 3], [0], [0], [3]], [[3, 0], [0, 2]], [3, 3, 1, 0], (3, 2))]
+    for hosts, ids_l, want_ranks, want_msgs in cases:
+        ids_np = np.array(ids_l, dtype=np.int32)
+        src = np.zeros(ids_np.shape[0], dtype=np.int32)
+        pl = wl.placement_from_hosts(len(hosts), 4, 1, hosts, token_src_rank=src)
+        ids = torch.tensor(ids_np, device="cuda")
+        slot, _, pl_dev, ws = _gpu_route_replicas(ids, pl, (0, 1))
+        slot, msgs = _gpu_refine(ids, pl_dev, slot, ws)
+        assert [int(pl.slot_rank[s]) for s in slot.cpu().numpy()] == want_ranks
+        assert msgs == want_msgs
+    rng = np.random.default_rng(11)
+    w = wl.WORKLOADS["replica"].scaled(T=5000)
+    hosts = wl.replica_hosts(w)
+    src = np.where(rng.random(w.T) < 0.6, rng.integers(0, 4, w.T), rng.integers(0, 16, w.T))
+    pl = wl.placement_from_hosts(w.E, w.R, w.ranks_per_node, hosts, token_src_rank=src)
+    ids, _ = gpu_route(w, wl.make_logits(w, "cuda"))
+    for c in [(0, 1), (1, 5)]:
+        slot, _, pl_dev, ws = _gpu_route_replicas(ids, pl, c)
+        ref_in, _ = oracle.route_replicas_waterfill(ids.cpu().numpy(), pl, *c)
+        ref_slot, before, after = oracle.refine_consolidate(ids.cpu().numpy(), ref_in, pl)
+        slot, msgs = _gpu_refine(ids, pl_dev, slot, ws)
+        assert np.array_equal(slot.cpu().numpy(), ref_slot) and msgs == (before, after)
+
+
+@pytest.mark.parametrize("seed", list(range(900, 940)) + [2108, 3030, 3042])
+def test_route_refine_random_small(seed):
+    """Random small placements (1 to 4 copies per expert, 1 or 2 ranks per
+    node, explicit sources, top-1 to top-4, C from 0 to 1).  Seeds 2108,
+    3030 and 3042 have a source whose greedy result would raise its pairs,
+    so it keeps its input routing."""
+    rng = np.random.default_rng(seed)
+    R = int(rng.choice([4, 6, 8]))
+    rpn = int(rng.choice([1, 2]))
+    E = int(rng.integers(3, 9))
+    k = int(rng.integers(1, min(E, 4) + 1))
+    T = int(rng.integers(1, 200))
+    hosts = [sorted(rng.choice(R, size=int(rng.integers(1, 5)), replace=False).tolist())
+             for _ in range(E)]
+    src = rng.integers(0, R, size=T).astype(np.int32)
+    pl = wl.placement_from_hosts(E, R, rpn, hosts, token_src_rank=src)
+    ids_np = np.array([rng.choice(E, size=k, replace=False) for _ in range(T)], dtype=np.int32)
+    ids = torch.tensor(ids_np, device="cuda")
+    c = (int(rng.integers(0, 3)), 2)
+    slot, _, pl_dev, ws = _gpu_route_replicas(ids, pl, c)
+    ref_in, _ = oracle.route_replicas_waterfill(ids_np, pl, *c)
+    assert np.array_equal(slot.cpu().numpy(), ref_in)
+    ref_slot, before, after = oracle.refine_consolidate(ids_np, ref_in, pl)
+    slot, msgs = _gpu_refine(ids, pl_dev, slot, ws)
+    assert np.array_equal(slot.cpu().numpy(), ref_slot) and msgs == (before, after)
+
+
 def test_routed_layer_output_equals_fixed_rule_output():
     """Copies of an expert hold the same weights and rows are independent,
     so choosing other copies must not change the layer's output bit."""
