@@ -2,12 +2,20 @@
 
 One step = route -> dispatch layout -> permute -> grouped SwiGLU FFN (+ the
 shared expert where the workload has one) -> combine -> balancedness, over
-one batch of seeded synthetic inputs already resident in HBM.  Default
-workload: the 4,000-token prefill layer (hidden 8192, 64 experts, top-2,
-I=2048, 8 simulated ranks), on which both target fractions of the metric
-(grouped GEMM vs tensor peak, permute/combine vs HBM bandwidth) are quoted.
+one batch of seeded synthetic inputs already resident in HBM.
+
+The headline line is the largest single-GPU layer: the group-limited layer
+(4,096 tokens, hidden 7168, 256 routed experts in 8 groups, top-8 of the
+top-4 groups, I=2048, plus a shared expert of width 2048, 32 simulated
+ranks).  The same JSON line carries a record per further layer under
+"workloads": the decode step (64 tokens), the 4,000-token prefill layer
+(hidden 8192, 64 experts, top-2) and the replica layer (16,384 tokens,
+hidden 4096, 32 experts, top-4, with its Zipf sweep of balancedness and
+merged messages), each with its own stage table, roofline fraction and
+clocks, timed over fewer steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--also decode,prefill,replica | --also none]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
@@ -35,6 +43,10 @@ if ROOT not in sys.path:
 import workloads as wl  # noqa: E402
 
 METRIC = "MoE-layer tokens/s; grouped-GEMM % bf16 peak; permute/combine % HBM BW"
+# the largest layer that fits one GPU (the most weights and flops per step)
+HEADLINE = "group_limited"
+DEFAULT_EXTRAS = ("decode", "prefill", "replica")
+EXTRA_STEPS = 10
 
 
 def load_peaks():
@@ -803,7 +815,9 @@ def run_reference(args, world, rank):
     shared = None if sgu is None else (oracle.bf16_bits_to_f64(_bits(sgu[0])),
                                        oracle.bf16_bits_to_f64(_bits(sd[0])))
     rng = np.random.default_rng(777)
-    n_tok = max(1, min(w.T, args.ref_tokens))
+    # a step's sample: about 32 routed assignments (its expert weights
+    # dominate the oracle's time)
+    n_tok = max(1, min(w.T, args.ref_tokens or max(1, 32 // w.k)))
     samples = [np.sort(rng.choice(w.T, size=n_tok, replace=False))
                for _ in range(args.warmup + args.steps)]
     for toks in samples:      # host copies of the needed experts, outside the timer
@@ -837,16 +851,45 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+def extra_workloads(args):
+    """Workloads recorded after the headline: the default set behind the
+    default headline with the default step, else what --also names."""
+    if args.also == "none" or not args.also:
+        return []
+    if args.also == "auto":
+        plain = (args.workload == HEADLINE and mode_name(args) == "" and not args.graph
+                 and args.zipf is None and not args.tokens and not args.experts)
+        return list(DEFAULT_EXTRAS) if plain else []
+    names = [n.strip() for n in args.also.split(",") if n.strip()]
+    for n in names:
+        if n not in wl.WORKLOADS:
+            raise SystemExit(f"unknown workload in --also: {n}")
+    return [n for n in names if n != args.workload]
+
+
+def compact_record(rec):
+    """A further workload's record: its throughput, stage table, roofline,
+    target fractions, balancedness and clocks (no end-to-end or CPU legs)."""
+    keep = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "gpu_launches",
+            "roofline", "stages", "gemm_pct_bf16_peak", "permute_pct_hbm", "combine_pct_hbm",
+            "balancedness", "merge", "clocks", "replica_zipf_sweep")
+    return {k: rec[k] for k in keep if k in rec}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="prefill", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--also", default="auto",
+                    help="further workloads recorded in the same line (comma list, 'none'; "
+                         "auto: decode,prefill,replica after the default headline)")
     ap.add_argument("--zipf", type=float, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--ref-tokens", type=int, default=0,
+                    help="tokens per reference step (0: 32 routed assignments' worth)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--graph", action="store_true",
@@ -875,6 +918,17 @@ def main():
         if not torch.cuda.is_available():
             raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
         out = run_ours(args, world, rank, local)
+        extras = extra_workloads(args)
+        if extras:
+            out["workloads"] = {}
+            for name in extras:
+                torch.cuda.empty_cache()
+                sub = argparse.Namespace(**vars(args))
+                sub.workload, sub.zipf, sub.tokens, sub.experts = name, None, 0, 0
+                sub.steps = max(3, min(args.steps, EXTRA_STEPS))
+                sub.warmup = max(3, min(args.warmup, 3))
+                sub.no_e2e = sub.no_cpu_baseline = True
+                out["workloads"][name] = compact_record(run_ours(sub, world, rank, local))
     if rank == 0 and out is not None:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -43,7 +43,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -876,37 +875,6 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Phase-1 shift (Ph1Plan's delta): the given default, or MOE_FFN_PH1_SHIFT
-// for comparison runs.
-int ph1_shift(int dflt) {
-  static int v = [] {
-    const char *e = getenv("MOE_FFN_PH1_SHIFT");
-    return e ? atoi(e) : -1;
-  }();
-  return v >= 0 ? v : dflt;
-}
-
-// M = 64 tiles for segments of at most 64 rows: 1 (default), or 0 from
-// MOE_FFN_SMALL_TILES=0 for comparison runs.
-int small_tiles() {
-  static int v = [] {
-    const char *e = getenv("MOE_FFN_SMALL_TILES");
-    return (e && e[0] == '0') ? 0 : 1;
-  }();
-  return v;
-}
-
-// Tile order: 1 (default) merges multi-tile and one-tile segments
-// (tile_order.cuh); MOE_FFN_INTERLEAVE=0 keeps plain segment order, for
-// comparison.
-int interleave_tiles() {
-  static int v = [] {
-    const char *e = getenv("MOE_FFN_INTERLEAVE");
-    return (e && e[0] == '0') ? 0 : 1;
-  }();
-  return v;
-}
-
 bool ensure_smem_attr() {
   constexpr int kMaxDevices = 64;
   static bool done[kMaxDevices] = {false};
@@ -997,7 +965,8 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
                    void *ws, size_t ws_bytes, void *stream, bool packed,
                    const int32_t *gather_src = nullptr, int32_t gather_k = 1,
                    int64_t gather_T = 0, const int32_t *masked_m = nullptr, int32_t cap = 0,
-                   int64_t extra_lo = 0, int64_t extra_rows = 0, int32_t extra_expert = 0) {
+                   int64_t extra_lo = 0, int64_t extra_rows = 0, int32_t extra_expert = 0,
+                   const moe_ffn_schedule *sched = nullptr) {
   // an extra segment (a shared expert) is appended after the S listed ones
   const int32_t S_listed = S;
   if (extra_rows > 0) S = S + 1;
@@ -1042,10 +1011,11 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   p.n_phases = 2;
   p.ready = ready;
   p.status = moe_host::status_ptr(ws);
-  p.interleave = interleave_tiles();
+  // schedule: which CTA runs which tile, never a row's arithmetic
+  p.interleave = sched ? sched->interleave : 1;
   // a gate/up tile (depth H) takes about H/I down tiles' time (depth I)
-  p.ph1_shift = ph1_shift((H + I / 2) / I);
-  p.small_rows = small_tiles() ? kBMSmall : 0;
+  p.ph1_shift = (sched && sched->ph1_shift >= 0) ? sched->ph1_shift : (H + I / 2) / I;
+  p.small_rows = (sched == nullptr || sched->small_tiles) ? kBMSmall : 0;
   p.gather_src = gather_src;
   p.gather_k = gather_k;
   p.gather_T = (int32_t)gather_T;
@@ -1107,6 +1077,23 @@ extern "C" moe_status moe_grouped_ffn_packed_shared(
   return run_ffn(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up_packed, w_down_packed, H,
                  I, h, y_perm, ws, ws_bytes, stream, true, nullptr, 1, 0, nullptr, 0, shared_row0,
                  shared_rows, shared_expert);
+}
+
+extern "C" moe_status moe_grouped_ffn_packed_scheduled(
+    const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_offsets, const int32_t *seg_expert,
+    int32_t S, int32_t E, const uint16_t *w_gate_up_packed, const uint16_t *w_down_packed, int32_t H,
+    int32_t I, int64_t shared_row0, int64_t shared_rows, int32_t shared_expert,
+    const moe_ffn_schedule *schedule, uint16_t *h, uint16_t *y_perm, void *ws, size_t ws_bytes,
+    void *stream) {
+  if (shared_row0 < 0 || shared_rows < 0 || shared_row0 + shared_rows > n_rows)
+    return MOE_ERR_INVALID_ARG;
+  if (shared_rows > 0 && (shared_expert < 0 || shared_expert >= E)) return MOE_ERR_INVALID_ARG;
+  if (schedule && (schedule->ph1_shift < -1 || (schedule->interleave & ~1) != 0 ||
+                   (schedule->small_tiles & ~1) != 0))
+    return MOE_ERR_INVALID_ARG;
+  return run_ffn(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up_packed, w_down_packed, H,
+                 I, h, y_perm, ws, ws_bytes, stream, true, nullptr, 1, 0, nullptr, 0, shared_row0,
+                 shared_rows, shared_expert, schedule);
 }
 
 extern "C" moe_status moe_grouped_ffn_gather(const uint16_t *x, int64_t T, int32_t k,
@@ -1266,7 +1253,7 @@ extern "C" moe_status moe_prefetch_ffn_weights(const int32_t *topk_ids, int64_t 
   a.w_gu = w_gate_up_packed;
   a.NB = I / 128;
   a.nk = H / kBK;
-  a.interleave = interleave_tiles();
+  a.interleave = 1;  // the FFN's default tile order
   int64_t kb = max_bytes / ((int64_t)wave * tile_bytes);
   if (kb > a.nk) kb = a.nk;
   if (kb > 32) kb = 32;  // one k-block per lane

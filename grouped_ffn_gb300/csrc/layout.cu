@@ -628,17 +628,236 @@ struct RefineArgs {
 };
 
 // Shared memory (int32 words) of route_refine_kernel.
-inline size_t refine_smem_words(int E, int S, int n_nodes) {
-  return (size_t)(E + 1) + 3 * (size_t)S + 2 * (size_t)n_nodes + kRefineThreads + 16;
+inline size_t refine_smem_words(int E, int S, int kmax) {
+  return 2 * (size_t)E + 1 + 4 * (size_t)S + kRefineThreads + 16 +
+         2 * (size_t)kRefineThreads * kmax;
 }
 
-// Distinct values of v over the lanes in `mask` (every lane calls this).
-__device__ __forceinline__ int distinct_in(uint32_t mask, int v, int lane) {
-  const uint32_t grp = __match_any_sync(0xffffffffu, (mask >> lane) & 1u ? v : -1 - lane);
-  const bool first = ((mask >> lane) & 1u) && (__ffs(grp) - 1 == lane);
-  return __popc(__ballot_sync(0xffffffffu, first));
+// The placement and count tables a CTA keeps in shared memory.
+struct RefineTables {
+  const int32_t *rep_off;    // [E+1] clamped to [0, S]
+  const int32_t *rep_sl;     // [S] slot per copy, -1 if invalid
+  const int32_t *slot_node;  // [S] node of each slot, -1 if invalid
+  int32_t *left;             // [S] this rank's count left per remote copy
+  int n_i;                   // the rank's node
+};
+
+// One token's greedy cover, by one thread, against counts that no other
+// token of the same round changes (see route_refine_kernel).  e/s0/m0: the
+// token's k <= KMAX requests (expert, input slot, remote node or -1); open:
+// requests that may move.  Returns the refined slot of each request in
+// cur_s and the token's remote-node count before and after.  Every loop over
+// requests runs to the compile-time KMAX, so the per-request values stay in
+// registers.
+template <int KMAX>
+__device__ __forceinline__ void refine_token_lane(const RefineTables &tb, int k, const int (&e)[KMAX],
+                                                  const int (&s0)[KMAX], const int (&m0)[KMAX],
+                                                  uint32_t open, int (&cur_s)[KMAX], int &before,
+                                                  int &after, bool &failed) {
+  // distinct remote nodes: the token's before, and those of the requests
+  // that do not move
+  int usedn[KMAX];
+  int nu = 0;
+  before = 0;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    cur_s[j] = s0[j];
+    usedn[j] = -1;
+    if (j >= k || m0[j] < 0) continue;
+    bool seen = false;
+#pragma unroll
+    for (int q = 0; q < j; ++q) seen |= q < k && m0[q] == m0[j];
+    before += seen ? 0 : 1;
+  }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (j >= k || m0[j] < 0 || ((open >> j) & 1u)) continue;
+    bool seen = false;
+#pragma unroll
+    for (int q = 0; q < KMAX; ++q) seen |= usedn[q] == m0[j];
+    if (!seen) {
+#pragma unroll
+      for (int q = 0; q < KMAX; ++q)
+        if (q == nu) usedn[q] = m0[j];
+      ++nu;
+    }
+  }
+  // a copy this token already took once counts one less for its later
+  // requests (only a token that repeats an expert id takes a copy twice)
+  int took_s[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) took_s[j] = -1;
+  auto avail = [&](int s2) {
+    int c = tb.left[s2];
+#pragma unroll
+    for (int q = 0; q < KMAX; ++q) c -= took_s[q] == s2 ? 1 : 0;
+    return c > 0;
+  };
+  auto cand_node = [&](int s2) {  // remote node of a copy with count left, else -1
+    if (s2 < 0) return -1;
+    const int m2 = tb.slot_node[s2];
+    return (m2 >= 0 && m2 != tb.n_i && avail(s2)) ? m2 : -1;
+  };
+  // whether request q has a copy with count left on node m2
+  auto has_on = [&](int eq, int m2) {
+    for (int c = tb.rep_off[eq]; c < tb.rep_off[eq + 1]; ++c)
+      if (cand_node(tb.rep_sl[c]) == m2) return true;
+    return false;
+  };
+  failed = false;
+  for (int iter = 0; iter < KMAX && open; ++iter) {
+    uint32_t best_key = 0xffffffffu;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (!((open >> j) & 1u)) continue;
+      const int lo = tb.rep_off[e[j]], hi = tb.rep_off[e[j] + 1];
+      for (int c = lo; c < hi; ++c) {
+        const int m2 = cand_node(tb.rep_sl[c]);
+        if (m2 < 0) continue;
+        bool dup = false;
+        for (int c2 = lo; c2 < c && !dup; ++c2) dup = cand_node(tb.rep_sl[c2]) == m2;
+        if (dup) continue;
+        int cover = 0;  // open requests with a copy on m2
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q)
+          if ((open >> q) & 1u) cover += (q == j || has_on(e[q], m2)) ? 1 : 0;
+        bool in_used = false;
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) in_used |= usedn[q] == m2;
+        const uint32_t key =
+            (in_used ? 0u : 1u) << 16 | (uint32_t)(32 - cover) << 10 | (uint32_t)m2;
+        best_key = min(best_key, key);
+      }
+    }
+    if (best_key == 0xffffffffu) {  // no copy left: inconsistent input
+      failed = true;
+      break;
+    }
+    const int best = (int)(best_key & 1023u);
+    uint32_t took = 0;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (!((open >> j) & 1u)) continue;
+      for (int c = tb.rep_off[e[j]]; c < tb.rep_off[e[j] + 1]; ++c) {
+        const int s2 = tb.rep_sl[c];
+        if (cand_node(s2) != best) continue;
+        took_s[j] = s2;
+        cur_s[j] = s2;
+        took |= 1u << j;
+        break;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < KMAX; ++q)
+      if (q == nu) usedn[q] = best;
+    ++nu;
+    open &= ~took;
+  }
+  after = 0;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    const int mj = j >= k ? -1 : (cur_s[j] == s0[j] ? m0[j] : tb.slot_node[cur_s[j]]);
+    if (mj < 0) continue;
+    bool seen = false;
+#pragma unroll
+    for (int q = 0; q < j; ++q) {
+      const int mq = q >= k ? -1 : (cur_s[q] == s0[q] ? m0[q] : tb.slot_node[cur_s[q]]);
+      seen |= mq == mj;
+    }
+    after += seen ? 0 : 1;
+  }
 }
 
+// refine_token_lane for at most 32 nodes and a token without repeated
+// expert ids: node sets are bit masks, and nmask[e] holds the remote nodes on
+// which expert e has a copy with count left (valid for the whole round).
+template <int KMAX>
+__device__ __forceinline__ void refine_token_lane_masks(
+    const RefineTables &tb, const uint32_t *nmask, int k, const int (&e)[KMAX],
+    const int (&s0)[KMAX], const int (&m0)[KMAX], uint32_t open, int (&cur_s)[KMAX],
+    int &before, int &after, bool &failed) {
+  uint32_t all0 = 0, used = 0, mj[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    cur_s[j] = s0[j];
+    mj[j] = 0;
+    if (j >= k || m0[j] < 0) continue;
+    all0 |= 1u << m0[j];
+    if ((open >> j) & 1u)
+      mj[j] = nmask[e[j]];
+    else
+      used |= 1u << m0[j];
+  }
+  before = __popc(all0);
+  failed = false;
+  while (open) {
+    uint32_t uni = 0;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) uni |= ((open >> j) & 1u) ? mj[j] : 0u;
+    if (uni == 0) {  // no copy left: inconsistent input
+      failed = true;
+      break;
+    }
+    uint32_t best_key = 0xffffffffu;
+    for (uint32_t u = uni; u; u &= u - 1) {
+      const int m = __ffs(u) - 1;
+      int cover = 0;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) cover += ((open >> j) & (mj[j] >> m) & 1u) ? 1 : 0;
+      const uint32_t key = (((used >> m) & 1u) ^ 1u) << 16 | (uint32_t)(32 - cover) << 10 |
+                           (uint32_t)m;
+      best_key = min(best_key, key);
+    }
+    const int best = (int)(best_key & 1023u);
+    uint32_t took = 0;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (!((open >> j) & (mj[j] >> best) & 1u)) continue;
+      for (int c = tb.rep_off[e[j]]; c < tb.rep_off[e[j] + 1]; ++c) {
+        const int s2 = tb.rep_sl[c];
+        if (s2 >= 0 && tb.slot_node[s2] == best && tb.left[s2] > 0) {
+          cur_s[j] = s2;
+          took |= 1u << j;
+          break;
+        }
+      }
+    }
+    used |= 1u << best;
+    open &= ~took;
+    if (!took) {  // a mask that disagrees with the counts: inconsistent input
+      failed = true;
+      break;
+    }
+  }
+  uint32_t all1 = 0;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (j >= k) continue;
+    const int mj2 = cur_s[j] == s0[j] ? m0[j] : tb.slot_node[cur_s[j]];
+    if (mj2 >= 0) all1 |= 1u << mj2;
+  }
+  after = __popc(all1);
+}
+
+// nmask[e] for every expert: remote nodes (bits) holding a copy of e whose
+// count for this rank is left; experts with one copy get 0.  By `lanes`
+// threads starting at `first`.
+__device__ __forceinline__ void refine_node_masks(const RefineTables &tb, uint32_t *nmask, int E,
+                                                  int first, int lanes) {
+  for (int ex = first; ex < E; ex += lanes) {
+    uint32_t mk = 0;
+    const int lo = tb.rep_off[ex], hi = tb.rep_off[ex + 1];
+    if (hi - lo > 1)
+      for (int c = lo; c < hi; ++c) {
+        const int s2 = tb.rep_sl[c];
+        const int m2 = s2 >= 0 ? tb.slot_node[s2] : -1;
+        if (m2 >= 0 && m2 != tb.n_i && tb.left[s2] > 0) mk |= 1u << m2;
+      }
+    nmask[ex] = mk;
+  }
+}
+
+template <int KMAX>
 __global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs r) {
   moe::pdl_wait();
   moe::pdl_trigger();
@@ -647,9 +866,12 @@ __global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs
   int32_t *rep_sl = rep_off + (r.E + 1);    // [S]
   int32_t *slot_node = rep_sl + r.S;        // [S] node of each slot, -1 if invalid
   int32_t *left = slot_node + r.S;          // [S] this rank's count left per remote copy
-  int32_t *cnt = left + r.S;                // [n_nodes] open requests a node covers
-  int32_t *used = cnt + r.n_nodes;          // [n_nodes] nodes the current token sends to
-  int32_t *list = used + r.n_nodes;         // [kRefineThreads] open tokens of a chunk
+  int32_t *use = left + r.S;                // [S] a round's takes per copy
+  int32_t *list = use + r.S;                // [kRefineThreads] open tokens of a chunk
+  uint32_t *nmask = reinterpret_cast<uint32_t *>(list + kRefineThreads + 16);  // [E]
+  // [kRefineThreads * KMAX] each: the chunk's open tokens' expert ids and slots
+  int32_t *stage_e = reinterpret_cast<int32_t *>(nmask + r.E);
+  int32_t *stage_s = stage_e + kRefineThreads * KMAX;
   int32_t *misc = list + kRefineThreads;    // [1] pairs, [2] saved, [4..11] per-warp counts
 
   const int i = blockIdx.x;  // source rank
@@ -662,19 +884,20 @@ __global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs
     rep_sl[s] = (v >= 0 && v < r.S) ? v : -1;
     const int rk = r.slot_rank[s];
     slot_node[s] = (rk >= 0 && rk < r.R) ? rk / r.rpn : -1;
-    left[s] = 0;
+    left[s] = use[s] = 0;
   }
-  for (int m = tid; m < r.n_nodes; m += blockDim.x) cnt[m] = used[m] = 0;
   if (tid < 16) misc[tid] = 0;
   __syncthreads();
+  const RefineTables tb{rep_off, rep_sl, slot_node, left, n_i};
 
   const bool by_mod = r.token_src_rank == nullptr;
   const int64_t n_pos = by_mod ? (r.T > i ? (r.T - 1 - i) / r.R + 1 : 0) : r.T;
   auto token_of = [&](int64_t u) { return by_mod ? i + u * r.R : u; };
   auto belongs = [&](int64_t u) { return by_mod || __ldg(r.token_src_rank + u) == i; };
-  // request a of this rank: its slot's node, and whether it may move
-  auto classify = [&](int64_t a, int &s, int &m, bool &open) {
-    const int e = __ldg(r.topk_ids + a);
+  // request a of this rank: its expert, its slot's remote node (-1 if local
+  // or invalid), and whether it may move
+  auto classify = [&](int64_t a, int &e, int &s, int &m, bool &open) {
+    e = __ldg(r.topk_ids + a);
     s = r.slot[a];
     m = (s >= 0 && s < r.S) ? slot_node[s] : -1;
     const bool remote = m >= 0 && m != n_i;
@@ -690,9 +913,9 @@ __global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs
     int nodes[32];
     int nd = 0;
     for (int j = 0; j < r.k; ++j) {
-      int s, m;
+      int e, s, m;
       bool open;
-      classify(t * r.k + j, s, m, open);
+      classify(t * r.k + j, e, s, m, open);
       if (open) atomicAdd(&left[s], 1);
       if (m < 0) continue;
       bool seen = false;
@@ -703,17 +926,30 @@ __global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs
   }
   atomicAdd(&misc[1], pairs);
   __syncthreads();
+  const bool masks = r.n_nodes <= 32;
+  if (masks) refine_node_masks(tb, nmask, r.E, tid, blockDim.x);
+  __syncthreads();
 
-  // pass 2: chunks of positions; warp 0 refines the chunk's open tokens in order
-  int delta = 0;  // pairs saved (warp 0, lane 0)
+  // pass 2: chunks of positions; warp 0 refines the chunk's open tokens in
+  // order.  Batches of 32 consecutive open tokens, one per lane, decide
+  // against the counts as they stand before the batch.  That is exactly the
+  // one-by-one result unless a copy's count runs out inside the batch (then
+  // a later token could see that copy gone): if any copy's takes reach its
+  // count, the batch is redone one token at a time, the whole warp on each.
+  int delta = 0;  // pairs saved (warp 0)
   for (int64_t base = 0; base < n_pos; base += blockDim.x) {
     const int64_t u = base + tid;
     bool has_open = false;
+    int ce[KMAX], cs[KMAX];
     if (u < n_pos && belongs(u)) {
       const int64_t t = token_of(u);
-      for (int j = 0; j < r.k && !has_open; ++j) {
-        int s, m;
-        classify(t * r.k + j, s, m, has_open);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        int m;
+        bool o = false;
+        ce[j] = cs[j] = -1;
+        if (j < r.k) classify(t * r.k + j, ce[j], cs[j], m, o);
+        has_open |= o;
       }
     }
     // compact the chunk's open tokens in ascending position: per-warp counts,
@@ -726,100 +962,117 @@ __global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs
       wbase += w < warp ? misc[4 + w] : 0;
       n_open += misc[4 + w];
     }
-    if (has_open) list[wbase + __popc(b & ((1u << lane) - 1u))] = (int32_t)(u - base);
+    if (has_open) {
+      const int idx = wbase + __popc(b & ((1u << lane) - 1u));
+      list[idx] = (int32_t)(u - base);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        stage_e[idx * KMAX + j] = ce[j];
+        stage_s[idx * KMAX + j] = cs[j];
+      }
+    }
     __syncthreads();
     if (warp == 0) {
-      for (int q = 0; q < n_open; ++q) {
-        const int64_t t = token_of(base + list[q]);
-        const int64_t a = t * r.k + lane;
-        int s0 = -1, m0 = -1;
-        bool open = false;
-        const int e = lane < r.k ? __ldg(r.topk_ids + a) : -1;
-        if (lane < r.k) classify(a, s0, m0, open);
-        const uint32_t rem = __ballot_sync(0xffffffffu, m0 >= 0);
-        const int before = distinct_in(rem, m0, lane);
-        if (m0 >= 0 && !open) used[m0] = 1;  // fixed remote requests
-        __syncwarp();
-        int cur_s = s0, cur_m = m0;
-        uint32_t open_set = __ballot_sync(0xffffffffu, open);
-        const int lo = open ? rep_off[e] : 0, hi = open ? rep_off[e + 1] : 0;
-        while (open_set) {
-          const bool mine = (open_set >> lane) & 1u;
-          // count each candidate node once per request
-          if (mine)
-            for (int c = lo; c < hi; ++c) {
-              const int s2 = rep_sl[c];
-              const int m2 = s2 >= 0 ? slot_node[s2] : -1;
-              if (m2 < 0 || m2 == n_i || left[s2] <= 0) continue;
-              bool dup = false;
-              for (int c2 = lo; c2 < c; ++c2) {
-                const int s3 = rep_sl[c2];
-                dup |= s3 >= 0 && slot_node[s3] == m2 && left[s3] > 0;
-              }
-              if (!dup) atomicAdd(&cnt[m2], 1);
+      // Rounds of up to 32 consecutive open tokens, one per lane, decided
+      // against the counts as they stand before the round.  A token's
+      // decision is the one-by-one result as long as every count it looked
+      // at is still positive at its turn, i.e. up to and including the first
+      // token whose take empties a copy; the round commits that prefix and
+      // the next round starts after it.
+      int q0 = 0;
+      while (q0 < n_open) {
+        const int n_here = min(32, n_open - q0);
+        const bool mine = lane < n_here;
+        int e[KMAX], s0[KMAX], m0[KMAX], cur_s[KMAX];
+        uint32_t open = 0;
+        int64_t t = 0;
+        int before = 0, after = 0;
+        bool failed = false, repeats = false;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) e[j] = s0[j] = m0[j] = -1;
+        if (mine) {
+          t = token_of(base + list[q0 + lane]);
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j) {
+            if (j >= r.k) continue;
+            // as classify(), from the chunk's staged copies
+            const int ej = stage_e[(q0 + lane) * KMAX + j], sj = stage_s[(q0 + lane) * KMAX + j];
+            int mj = (sj >= 0 && sj < r.S) ? slot_node[sj] : -1;
+            const bool remote = mj >= 0 && mj != n_i;
+            if (remote && ej >= 0 && ej < r.E && rep_off[ej + 1] - rep_off[ej] > 1)
+              open |= 1u << j;
+            e[j] = ej;
+            s0[j] = sj;
+            m0[j] = remote ? mj : -1;
+          }
+          // an expert id twice among the token's requests
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j)
+#pragma unroll
+            for (int q = 0; q < j; ++q) repeats |= j < r.k && e[q] == e[j];
+          if (masks && !repeats)
+            refine_token_lane_masks<KMAX>(tb, nmask, r.k, e, s0, m0, open, cur_s, before, after,
+                                          failed);
+          else
+            refine_token_lane<KMAX>(tb, r.k, e, s0, m0, open, cur_s, before, after, failed);
+          if (failed)
+            moe::report_error(r.status, MOE_ERR_PLACEMENT, (int32_t)t, moe::K_LAYOUT_FINALIZE);
+        }
+        // takes in token order: the first token that empties a copy ends the
+        // prefix.  A token that names an expert twice may take one copy twice,
+        // so its choice depends on the counts' values, not only on which are
+        // positive: it is exact only as the round's first token, and ends
+        // the prefix before itself elsewhere.
+        int stop = n_here;
+        bool emptied = false;
+        for (int l = 0; l < n_here; ++l) {
+          int flag = 0;  // 1: empties a copy (kept, then stop); 2: stop before it
+          if (lane == l) {
+            if (repeats && l > 0) {
+              flag = 2;
+            } else {
+#pragma unroll
+              for (int j = 0; j < KMAX; ++j)
+                if (((open >> j) & 1u) && ++use[cur_s[j]] >= left[cur_s[j]]) flag = 1;
             }
-          __syncwarp();
-          uint32_t key = 0xffffffffu;
-          if (mine)
-            for (int c = lo; c < hi; ++c) {
-              const int s2 = rep_sl[c];
-              const int m2 = s2 >= 0 ? slot_node[s2] : -1;
-              if (m2 < 0 || m2 == n_i || left[s2] <= 0) continue;
-              const uint32_t kk = ((used[m2] ? 1u : 0u) ^ 1u) << 16 |
-                                  (uint32_t)(32 - cnt[m2]) << 10 | (uint32_t)m2;
-              key = min(key, kk);
-            }
-          key = __reduce_min_sync(0xffffffffu, key);
-          __syncwarp();
-          if (mine)
-            for (int c = lo; c < hi; ++c)
-              if (rep_sl[c] >= 0 && slot_node[rep_sl[c]] >= 0) cnt[slot_node[rep_sl[c]]] = 0;
-          __syncwarp();
-          if (key == 0xffffffffu) {  // no copy left (inconsistent input)
-            if (lane == 0)
-              moe::report_error(r.status, MOE_ERR_PLACEMENT, (int32_t)t, moe::K_LAYOUT_FINALIZE);
+          }
+          flag = __shfl_sync(0xffffffffu, flag, l);
+          if (flag) {
+            stop = flag == 1 ? l + 1 : l;
+            emptied = flag == 1;
             break;
           }
-          const int best = (int)(key & 1023u);
-          bool covers = false;
-          if (mine)
-            for (int c = lo; c < hi && !covers; ++c) {
-              const int s2 = rep_sl[c];
-              covers = s2 >= 0 && slot_node[s2] == best && left[s2] > 0;
+        }
+        __syncwarp();
+        if (mine && lane < stop) {
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j)
+            if ((open >> j) & 1u) {
+              use[cur_s[j]] = 0;
+              r.cand[t * r.k + j] = cur_s[j];
             }
-          // requests on `best` take their copies in ascending request order
-          uint32_t cov = __ballot_sync(0xffffffffu, covers), took = 0;
-          for (uint32_t cc = cov; cc; cc &= cc - 1) {
-            if (lane == __ffs(cc) - 1) {
-              for (int c = lo; c < hi; ++c) {
-                const int s2 = rep_sl[c];
-                if (s2 >= 0 && slot_node[s2] == best && left[s2] > 0) {
-                  left[s2] -= 1;
-                  cur_s = s2;
-                  cur_m = best;
-                  took = 1;
-                  break;
-                }
-              }
-            }
-            __syncwarp();
-          }
-          open_set &= ~__ballot_sync(0xffffffffu, took != 0);
-          if (lane == 0) used[best] = 1;
+          delta += before - after;
+        }
+        __syncwarp();
+        if (mine && lane < stop) {
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j)
+            if ((open >> j) & 1u) atomicSub(&left[cur_s[j]], 1);
+        }
+        __syncwarp();
+        // counts change availability only when a copy runs out: then the
+        // node masks are rebuilt from them
+        if (masks && emptied) {
+          refine_node_masks(tb, nmask, r.E, lane, 32);
           __syncwarp();
         }
-        const int after = distinct_in(rem, cur_m, lane);
-        delta += before - after;
-        if (open) r.cand[a] = cur_s;
-        __syncwarp();
-        if (m0 >= 0) used[m0] = 0;
-        if (cur_m >= 0) used[cur_m] = 0;
-        __syncwarp();
+        q0 += stop;
       }
     }
     __syncthreads();
   }
-  if (tid == 0) misc[2] = delta;
+  // each of warp 0's lanes holds the pairs saved by its tokens
+  if (warp == 0) atomicAdd(&misc[2], delta);
   __syncthreads();
   const int before = misc[1], saved = misc[2];
   const bool keep = saved >= 0;
@@ -828,10 +1081,10 @@ __global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs
       if (!belongs(u)) continue;
       const int64_t t = token_of(u);
       for (int j = 0; j < r.k; ++j) {
-        int s, m;
+        int e, s, m;
         bool open;
         const int64_t a = t * r.k + j;
-        classify(a, s, m, open);
+        classify(a, e, s, m, open);
         if (open) r.slot[a] = r.cand[a];
       }
     }
@@ -1202,13 +1455,17 @@ extern "C" moe_status moe_route_refine(const int32_t *topk_ids, int64_t T, int32
       static_cast<char *>(ws) + route_ws_bytes(T, k, pl->n_experts, pl->n_slots, pl->n_ranks));
   r.messages = messages;
   r.status = moe_host::status_ptr(ws);
-  const size_t smem = refine_smem_words(r.E, r.S, r.n_nodes) * sizeof(int32_t);
+  // shared memory: at most 2 * 4096 + 1 + 4 * 1024 + 272 + 2 * 256 * 32 words (113 KiB)
+  const int kmax = k <= 4 ? 4 : k <= 8 ? 8 : k <= 16 ? 16 : 32;
+  const size_t smem = refine_smem_words(r.E, r.S, kmax) * sizeof(int32_t);
+  auto kern = kmax == 4 ? route_refine_kernel<4>
+              : kmax == 8 ? route_refine_kernel<8>
+              : kmax == 16 ? route_refine_kernel<16> : route_refine_kernel<32>;
   if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(route_refine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
     return MOE_ERR_CUDA;
-  return moe_host::launch_pdl(route_refine_kernel, dim3((unsigned)r.R), dim3(kRefineThreads), smem,
-                              st, r);
+  return moe_host::launch_pdl(kern, dim3((unsigned)r.R), dim3(kRefineThreads), smem, st, r);
 }
 
 extern "C" moe_status moe_route_replicas(const int32_t *topk_ids, int64_t T, int32_t k,

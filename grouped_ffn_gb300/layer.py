@@ -30,7 +30,8 @@ class MoELayer:
                  packed: bool = True, replica_relax: Optional[tuple] = None,
                  replica_refine: bool = False, gather: bool = False,
                  masked_cap: Optional[int] = None,
-                 fp8_dispatch: bool = False, fuse_shared: bool = True):
+                 fp8_dispatch: bool = False, fuse_shared: bool = True,
+                 ffn_schedule: Optional[moe.FfnSchedule] = None):
         """replica_relax=(c_num, c_den) chooses each assignment's replica by
         locality-preferred water-filling with load bounds C = c_num/c_den
         (moe_route_replicas); None keeps the fixed replica rule.
@@ -47,13 +48,19 @@ class MoELayer:
         fuse_shared=True runs a shared expert of the routed experts' width
         inside the routed experts' FFN launch (moe_permute_shared +
         moe_grouped_ffn_packed_shared) in the plain contiguous bf16 step;
-        otherwise it is a second launch.  The results are the same bits."""
+        otherwise it is a second launch.  The results are the same bits.
+        ffn_schedule (packed weights, contiguous layout) sets the grouped
+        FFN's tile schedule; None is the library's default.  Every schedule
+        gives the same bits."""
         if (gather or masked_cap is not None) and not packed:
             raise ValueError("gather and fixed-capacity modes stream packed weights")
         if gather and (masked_cap is not None or fp8_dispatch):
             raise ValueError("gather mode reads x directly: no fixed capacity, no FP8 dispatch")
         if masked_cap is not None and (replica_relax is not None or masked_cap < 1):
             raise ValueError("fixed-capacity layout: cap >= 1, fixed replica rule")
+        if ffn_schedule is not None and (not packed or gather or masked_cap is not None):
+            raise ValueError("ffn_schedule applies to the packed contiguous FFN")
+        self.ffn_schedule = ffn_schedule
         self.gather = gather
         self.masked_cap = masked_cap
         self.fp8_dispatch = fp8_dispatch
@@ -165,11 +172,14 @@ class MoELayer:
         moe.moe_pack_expert_weights(w_gate_up, w_down, gu, d)
         return gu, d
 
-    def _ffn(self, *args):
-        if self.packed:
-            moe.moe_grouped_ffn_packed(*args)
+    def _ffn(self, x_perm, offs, experts, wgu, wd, h, y, ws, stream):
+        if self.ffn_schedule is not None:
+            moe.moe_grouped_ffn_packed_scheduled(x_perm, offs, experts, wgu, wd, 0, 0, 0,
+                                                 self.ffn_schedule, h, y, ws, stream)
+        elif self.packed:
+            moe.moe_grouped_ffn_packed(x_perm, offs, experts, wgu, wd, h, y, ws, stream)
         else:
-            moe.moe_grouped_ffn(*args)
+            moe.moe_grouped_ffn(x_perm, offs, experts, wgu, wd, h, y, ws, stream)
 
     def _shared_offs(self, T: int) -> torch.Tensor:
         t = self._shared_offsets.get(T)
@@ -220,10 +230,16 @@ class MoELayer:
             moe.moe_permute_shared(x, self.k, self.dest_row[:A], self.x_perm[:A + T], self.ws,
                                    stream)
             mark("permute")
-            moe.moe_grouped_ffn_packed_shared(self.x_perm[:A + T], self.seg_offsets,
-                                              self.placement.slot_expert, self.w_gate_up,
-                                              self.w_down, A, T, self.E, self.h[:A + T],
-                                              self.y_perm[:A + T], self.ws, stream)
+            if self.ffn_schedule is not None:
+                moe.moe_grouped_ffn_packed_scheduled(
+                    self.x_perm[:A + T], self.seg_offsets, self.placement.slot_expert,
+                    self.w_gate_up, self.w_down, A, T, self.E, self.ffn_schedule,
+                    self.h[:A + T], self.y_perm[:A + T], self.ws, stream)
+            else:
+                moe.moe_grouped_ffn_packed_shared(self.x_perm[:A + T], self.seg_offsets,
+                                                  self.placement.slot_expert, self.w_gate_up,
+                                                  self.w_down, A, T, self.E, self.h[:A + T],
+                                                  self.y_perm[:A + T], self.ws, stream)
         else:
             self._dispatch(x, A, A, None, stream, mark)
             self._ffn(self.x_perm[:A], self.seg_offsets, self.placement.slot_expert,

@@ -43,6 +43,13 @@ class RouteCfg(ctypes.Structure):
                 ("group_topn", ctypes.c_int32)]
 
 
+class FfnSchedule(ctypes.Structure):
+    """moe_ffn_schedule: which CTA runs which FFN tile (never a row's bits).
+    ph1_shift -1 = default; interleave and small_tiles 1 = default."""
+    _fields_ = [("ph1_shift", ctypes.c_int32), ("interleave", ctypes.c_int32),
+                ("small_tiles", ctypes.c_int32)]
+
+
 class PlacementC(ctypes.Structure):
     _fields_ = [("n_experts", ctypes.c_int32), ("n_slots", ctypes.c_int32),
                 ("n_ranks", ctypes.c_int32), ("ranks_per_node", ctypes.c_int32),
@@ -101,6 +108,10 @@ _SIGNATURES = {
     "moe_grouped_ffn_packed_shared": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P, _I32,
                                                      _I32, _I64, _I64, _I32, _P, _P, _P, _SZ,
                                                      _P]),
+    "moe_grouped_ffn_packed_scheduled": (ctypes.c_int, [_P, _I64, _P, _P, _I32, _I32, _P, _P,
+                                                        _I32, _I32, _I64, _I64, _I32,
+                                                        ctypes.POINTER(FfnSchedule), _P, _P, _P,
+                                                        _SZ, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_version": (ctypes.c_char_p, []),
 }
@@ -256,17 +267,19 @@ def moe_prefetch_ffn_weights(topk_ids, placement: DevicePlacement, w_gate_up_pac
 
 
 def moe_dispatch_layout_noalloc(topk_ids, placement: DevicePlacement, slot, seg_counts,
-                                seg_offsets, dest_row, src_assign, rank_counts, status=None,
+                                seg_offsets, dest_row, src_assign, rank_counts, *, status,
                                 stream=None):
     """The layout with the library's fixed device scratch instead of a
-    workspace, for callers that cannot allocate; `status` is an optional
-    device int32[3] that receives device-side errors."""
+    workspace, for callers that cannot allocate.  `status` (required here) is
+    a caller-owned device int32[3] that receives device-side errors; read it
+    after the stream has run the call."""
     for n, t in (("topk_ids", topk_ids), ("slot", slot), ("seg_counts", seg_counts),
                  ("seg_offsets", seg_offsets), ("dest_row", dest_row),
-                 ("src_assign", src_assign), ("rank_counts", rank_counts)):
+                 ("src_assign", src_assign), ("rank_counts", rank_counts),
+                 ("status", status)):
         _need(t, torch.int32, n)
-    if status is not None:
-        _need(status, torch.int32, "status")
+    if status.numel() < 3:
+        raise ValueError("moe_dispatch_layout_noalloc: status needs 3 int32 words")
     T, k = topk_ids.shape
     _check("moe_dispatch_layout_noalloc", lib().moe_dispatch_layout_noalloc(
         _ptr(topk_ids), T, k, ctypes.byref(placement.c), _ptr(slot), _ptr(seg_counts),
@@ -481,6 +494,29 @@ def moe_grouped_ffn_packed_shared(x_perm, seg_offsets, seg_expert, w_gate_up_pac
         _ptr(x_perm), n_rows, _ptr(seg_offsets), _ptr(seg_expert), seg_expert.numel(), E,
         _ptr(w_gate_up_packed), _ptr(w_down_packed), H, I, shared_row0, shared_rows,
         shared_expert, _ptr(h), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_grouped_ffn_packed_scheduled(x_perm, seg_offsets, seg_expert, w_gate_up_packed,
+                                     w_down_packed, shared_row0: int, shared_rows: int,
+                                     shared_expert: int, schedule: FfnSchedule, h, y_perm, ws,
+                                     stream=None):
+    """moe_grouped_ffn_packed_shared with an explicit tile schedule."""
+    for n, t in (("x_perm", x_perm), ("w_gate_up_packed", w_gate_up_packed),
+                 ("w_down_packed", w_down_packed), ("h", h), ("y_perm", y_perm)):
+        _bf16(t, n)
+    _need(seg_offsets, torch.int32, "seg_offsets")
+    _need(seg_expert, torch.int32, "seg_expert")
+    n_rows, H = x_perm.shape
+    E, two_i, H2 = w_gate_up_packed.shape
+    I = two_i // 2
+    if H2 != H or tuple(w_down_packed.shape) != (E, H, I) or tuple(h.shape) != (n_rows, I) \
+            or tuple(y_perm.shape) != (n_rows, H):
+        raise ValueError("moe_grouped_ffn_packed_scheduled: inconsistent shapes")
+    _check("moe_grouped_ffn_packed_scheduled", lib().moe_grouped_ffn_packed_scheduled(
+        _ptr(x_perm), n_rows, _ptr(seg_offsets), _ptr(seg_expert), seg_expert.numel(), E,
+        _ptr(w_gate_up_packed), _ptr(w_down_packed), H, I, shared_row0, shared_rows,
+        shared_expert, None if schedule is None else ctypes.byref(schedule), _ptr(h),
+        _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 # ------------------------------------------------------------------ fixed-capacity layout

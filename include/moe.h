@@ -300,7 +300,11 @@ moe_status moe_dispatch_layout_routed(const int32_t *topk_ids, const int32_t *sl
  *  all calls on one GPU share the array: calls that may overlap on the same
  *  GPU (for example on two streams) race.  Order them on one stream.
  *  status: device int32[3] (code, detail, kernel id) for device-side errors,
- *  written like the workspace status word of the other calls; may be NULL. */
+ *  written like the workspace status word of the other calls.  It may be
+ *  NULL, but then a device-side error (an expert id out of range, an
+ *  inconsistent placement, an expired look-back wait) is dropped: the call
+ *  still returns MOE_OK and the outputs cannot be checked.  Pass a status
+ *  array whenever the inputs are not known to be valid. */
 moe_status moe_dispatch_layout_noalloc(const int32_t *topk_ids, int64_t T, int32_t k,
                                        const moe_placement *placement, int32_t *slot,
                                        int32_t *seg_counts, int32_t *seg_offsets,
@@ -476,6 +480,34 @@ moe_status moe_grouped_ffn_packed_shared(const uint16_t *x_perm, int64_t n_rows,
                                          int64_t shared_row0, int64_t shared_rows,
                                          int32_t shared_expert, uint16_t *h, uint16_t *y_perm,
                                          void *ws, size_t ws_bytes, void *stream);
+
+/* The tile schedule of the grouped FFN.  It decides which CTA runs which
+ * tile and in what order, never the arithmetic of a row: every setting gives
+ * the same output bits.  The pages fix no schedule; this is the library's own
+ * (an ordering of the pages' grouped GEMM over per-expert segments).
+ *  ph1_shift    phase-1 (down-projection) positions first given to the CTAs
+ *               that took one gate/up tile fewer, per such CTA; -1 for the
+ *               default round(H / I), 0 for plain round-robin.
+ *  interleave   1: merge the tiles of segments with several 128-row blocks
+ *               and of one-block segments in proportion to their counts (the
+ *               default); 0: plain segment order.
+ *  small_tiles  1: a tile whose segment ends within 64 rows of its first row
+ *               runs as an M = 64 tile (the default); 0: every tile M = 128. */
+typedef struct {
+  int32_t ph1_shift;
+  int32_t interleave;
+  int32_t small_tiles;
+} moe_ffn_schedule;
+
+/* moe_grouped_ffn_packed_shared with an explicit tile schedule (NULL: the
+ * default one, {-1, 1, 1}).  Same arguments and results otherwise;
+ * MOE_ERR_INVALID_ARG for ph1_shift < -1 or flags outside {0, 1}. */
+moe_status moe_grouped_ffn_packed_scheduled(
+    const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_offsets,
+    const int32_t *seg_expert, int32_t S, int32_t E, const uint16_t *w_gate_up_packed,
+    const uint16_t *w_down_packed, int32_t H, int32_t I, int64_t shared_row0,
+    int64_t shared_rows, int32_t shared_expert, const moe_ffn_schedule *schedule, uint16_t *h,
+    uint16_t *y_perm, void *ws, size_t ws_bytes, void *stream);
 
 /* moe_grouped_ffn_packed without the permuted copy: dispatched row r of
  * the gate/up GEMM is read straight from token row src_assign[r] / k of x

@@ -102,3 +102,22 @@ def test_tensor_peak_follows_the_timed_region_clocks(bench):
     p, label = bench.tensor_peak(peaks, slow)
     assert p == 1707.8 and label.startswith("sustained")
 
+
+
+def test_headline_and_further_workloads(bench):
+    """The default run puts the largest single-GPU layer in the headline and
+    records decode, prefill and replica beside it; any other headline or
+    step variant records none unless --also names them."""
+    import argparse
+    base = dict(workload=bench.HEADLINE, also="auto", gather=False, unpacked=False,
+                masked_cap=0, fp8_dispatch=False, replica_relax="", graph=False, zipf=None,
+                tokens=0, experts=0)
+    ns = lambda **kw: argparse.Namespace(**{**base, **kw})
+    assert bench.HEADLINE == "group_limited"
+    assert bench.extra_workloads(ns()) == ["decode", "prefill", "replica"]
+    assert bench.extra_workloads(ns(workload="prefill")) == []
+    assert bench.extra_workloads(ns(gather=True)) == []
+    assert bench.extra_workloads(ns(also="none")) == []
+    assert bench.extra_workloads(ns(workload="prefill", also="decode,prefill")) == ["decode"]
+    rec = {"value": 1.0, "e2e": {}, "cpu_baseline": {}, "stages": {}, "clocks": {}}
+    assert set(bench.compact_record(rec)) == {"value", "stages", "clocks"}

@@ -69,9 +69,9 @@ def test_layout_after_an_empty_call_on_the_same_scratch(name):
     ref = _outputs(w.T, w.k, pl_dev)
     moe.moe_dispatch_layout(ids, pl_dev, *ref, fresh)
     # the library's scratch
-    moe.moe_dispatch_layout_noalloc(ids[:0], pl_dev, *_outputs(0, w.k, pl_dev))
-    got = _outputs(w.T, w.k, pl_dev)
     status = torch.zeros(3, dtype=torch.int32, device="cuda")
+    moe.moe_dispatch_layout_noalloc(ids[:0], pl_dev, *_outputs(0, w.k, pl_dev), status=status)
+    got = _outputs(w.T, w.k, pl_dev)
     moe.moe_dispatch_layout_noalloc(ids, pl_dev, *got, status=status)
     torch.cuda.synchronize()
     assert status.tolist() == [0, 0, 0]
@@ -96,6 +96,34 @@ def test_noalloc_layout_rejects_requests_beyond_its_scratch():
     T, k = 4096 * 256 // 2, 2
     ids = torch.zeros(T, k, dtype=torch.int32, device="cuda")
     out = _outputs(T, k, pl_dev)
+    status = torch.zeros(3, dtype=torch.int32, device="cuda")
     with pytest.raises(moe.MoeError) as ei:
-        moe.moe_dispatch_layout_noalloc(ids, pl_dev, *out)
+        moe.moe_dispatch_layout_noalloc(ids, pl_dev, *out, status=status)
     assert ei.value.status == 2          # MOE_ERR_UNSUPPORTED, nothing launched
+
+
+def test_noalloc_device_error_reaches_status_and_the_next_call_is_clean():
+    """An expert id out of range in a layout of several 4096-assignment tiles
+    is reported in the caller's status array (MOE_ERR_DEVICE_INDEX) rather
+    than dropped; the shared scratch it leaves behind does not disturb the
+    next call, which again gives the workspace layout."""
+    from grouped_ffn_gb300 import moe
+    w, ids = _ids("prefill", 31)          # 8000 assignments: 2 tiles
+    pl_dev = moe.DevicePlacement.from_tables(wl.make_placement(w))
+    bad = ids.clone()
+    bad[5000 // w.k, 0] = w.E + 3         # in the second tile
+    status = torch.zeros(3, dtype=torch.int32, device="cuda")
+    moe.moe_dispatch_layout_noalloc(bad, pl_dev, *_outputs(w.T, w.k, pl_dev), status=status)
+    torch.cuda.synchronize()
+    assert status[0].item() == 4         # MOE_ERR_DEVICE_INDEX
+    ws = moe.new_workspace(w.T, w.k, pl_dev.n_slots)
+    ref = _outputs(w.T, w.k, pl_dev)
+    moe.moe_dispatch_layout(ids, pl_dev, *ref, ws)
+    moe.moe_check_device_status(ws)
+    got = _outputs(w.T, w.k, pl_dev)
+    status.zero_()
+    moe.moe_dispatch_layout_noalloc(ids, pl_dev, *got, status=status)
+    torch.cuda.synchronize()
+    assert status.tolist() == [0, 0, 0]
+    for r, g in zip(ref, got):
+        assert torch.equal(r, g)
