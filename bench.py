@@ -89,7 +89,8 @@ def mode_name(args) -> str:
     default one only."""
     parts = [n for n, on in (("gather", args.gather), ("unpacked", args.unpacked),
                              ("masked", bool(args.masked_cap)), ("fp8", args.fp8_dispatch),
-                             ("relax", bool(args.replica_relax))) if on]
+                             ("relax", bool(args.replica_relax)),
+                             ("pair-ffn", getattr(args, "pair_ffn", False))) if on]
     return "+".join(parts)
 
 
@@ -270,7 +271,8 @@ def run_ours(args, world, rank, local):
                      shared_w_gate_up=sgu, shared_w_down=sd, device=dev,
                      packed=not args.unpacked, replica_relax=parse_relax(args.replica_relax),
                      gather=args.gather, masked_cap=args.masked_cap or None,
-                     fp8_dispatch=args.fp8_dispatch, fuse_shared=not args.no_fuse_shared)
+                     fp8_dispatch=args.fp8_dispatch, fuse_shared=not args.no_fuse_shared,
+                     ffn_schedule=moe.FfnSchedule(cta_pairs=1) if args.pair_ffn else None)
     y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -904,6 +906,8 @@ def main():
                     help="fixed-capacity layout with this many rows per slot (0: contiguous)")
     ap.add_argument("--fp8-dispatch", action="store_true",
                     help="dispatch E4M3 codes + block scales, restore bf16 before the FFN")
+    ap.add_argument("--pair-ffn", action="store_true",
+                    help="run the grouped FFN's tiles on pairs of SMs (tcgen05 cta_group::2)")
     ap.add_argument("--no-fuse-shared", action="store_true",
                     help="run the shared expert as a second FFN launch")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")

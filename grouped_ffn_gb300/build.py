@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
 
-SOURCES = ["api.cu", "route.cu", "layout.cu", "movers.cu", "fp8.cu", "grouped_ffn.cu"]
+SOURCES = ["api.cu", "route.cu", "layout.cu", "movers.cu", "fp8.cu", "grouped_ffn.cu",
+           "grouped_ffn_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", INCLUDE, "-I", CSRC]

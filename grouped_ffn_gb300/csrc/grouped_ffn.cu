@@ -46,7 +46,9 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "ffn_pair.h"
 #include "tile_order.cuh"
+#include "umma.cuh"
 
 namespace {
 
@@ -128,239 +130,7 @@ struct FfnParams {
   Phase ph[2];
 };
 
-// ------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait; gives up when another role aborted or the deadline passed
-// (then it raises the abort flag and records MOE_ERR_DEVICE_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int32_t *abort_flag, int32_t *status,
-                                          int32_t kid, uint64_t limit_ns = moe::kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = moe::global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    const uint64_t dt = moe::global_timer_ns() - t0;
-    if (dt > limit_ns) {
-      *abort_flag = 1;
-      moe::report_error(status, MOE_ERR_DEVICE_TIMEOUT, (int32_t)(dt / 1000), kid);
-      return false;
-    }
-  }
-}
-
-// Bounded wait used while tearing down: ignores the abort flag.
-__device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = moe::global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (moe::global_timer_ns() - t0 > moe::kWaitLimitNs) return;
-  }
-}
-
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
-}
-
-// A tiled load with an L2 eviction-priority hint (a createpolicy value).
-__device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *m, int32_t x,
-                                                 int32_t y, uint64_t *bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-// L2 policies for weight tiles: read by one m-block only -> evicted first;
-// read by several m-blocks of a segment -> kept last.
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m, int32_t x,
-                                            int32_t y, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Four rows (y0..y3) of a one-row-high box at column x, into 4 consecutive
-// 128-byte rows of shared memory (same swizzle as a tiled load there).
-__device__ __forceinline__ void tma_gather4(void *smem_dst, const CUtensorMap *m, int32_t x,
-                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3,
-                                            uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Orders generic-proxy global writes/reads with async-proxy (TMA) accesses.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-__device__ __forceinline__ int32_t ld_acquire_s32(const int32_t *p) {
-  int32_t v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Bounded wait until a global counter written by other CTAs reaches `need`
-// (acquire loads).  Gives up like mbar_wait: on another role's abort, or at
-// the deadline, raising the abort flag and recording the timeout.
-__device__ __forceinline__ bool wait_counter(const int32_t *counter, int32_t need,
-                                             volatile int32_t *abort_flag, int32_t *status,
-                                             int32_t kid, uint64_t limit_ns = moe::kWaitLimitNs) {
-  if (ld_acquire_s32(counter) >= need) return true;
-  const uint64_t t0 = moe::global_timer_ns();
-  for (;;) {
-    if (ld_acquire_s32(counter) >= need) return true;
-    if (*abort_flag) return false;
-    const uint64_t dt = moe::global_timer_ns() - t0;
-    if (dt > limit_ns) {
-      *abort_flag = 1;
-      moe::report_error(status, MOE_ERR_DEVICE_TIMEOUT, (int32_t)(dt / 1000), kid);
-      return false;
-    }
-    __nanosleep(64);
-  }
-}
-
-__device__ __forceinline__ void epilogue_bar() {  // the 128 epilogue threads only
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(dst)),
-               "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128
-// bytes, 8-row groups 1024 bytes apart (SBO), descriptor version 1.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;            // leading-dimension offset (unused here)
-  d |= (uint64_t)(1024 >> 4) << 32;  // stride-dimension offset
-  d |= (uint64_t)1 << 46;            // version
-  d |= (uint64_t)2 << 61;            // 128-byte swizzle
-  return d;
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&p);
-}
-
-// silu(g) * u = g / (1 + e^-g) * u in fp32, with CUDA's fast exponential and
-// division intrinsics: their few-ulp error is far below the bf16 rounding of
-// h, and the gate/up epilogue (128 of these per thread and tile) shares its
-// SM sub-partitions with the TMA and MMA issuing warps.  For g below about
-// -88, e^-g overflows and the result is 0 (the exact value is below 1e-36).
-__device__ __forceinline__ float silu_mul(uint32_t g_bits, uint32_t u_bits) {
-  const float g = __uint_as_float(g_bits);
-  const float u = __uint_as_float(u_bits);
-  return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
+using namespace umma;
 
 // --------------------------------------------------------------- the kernel
 struct TileInfo {
@@ -395,28 +165,6 @@ struct TileWalk {
     return ti;
   }
 };
-
-// In-place exclusive scan of a[0..n) by one warp (lane L owns a chunk);
-// a[n] receives the total.
-__device__ __forceinline__ void warp_exclusive_scan(int32_t *a, int n, int lane) {
-  const int per = (n + 31) / 32;
-  const int lo = lane * per, hi = min(n, lo + per);
-  int sum = 0;
-  for (int i = lo; i < hi; ++i) sum += a[i];
-  int incl = sum;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
-  }
-  int run = incl - sum;
-  for (int i = lo; i < hi; ++i) {
-    const int c = a[i];
-    a[i] = run;
-    run += c;
-  }
-  if (lane == 31) a[n] = incl;
-}
 
 // Whether m-block m_blk of segment s is an M = 64 tile: at most small_rows
 // rows from its first row to the segment's end (a one-block segment of at
@@ -997,6 +745,37 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   int32_t *ready = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kReadyOff);
   if (cudaMemsetAsync(ready, 0, (size_t)S * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
 
+  // packed weights and rows from a dispatched buffer: SM pairs when the
+  // schedule asks for them (measured slower than single-SM tiles on every
+  // layer here, so not the default)
+  if (packed && gather_src == nullptr && sched != nullptr && sched->cta_pairs) {
+    moe_pair::PairRun r{};
+    r.x_perm = x_perm;
+    r.n_rows = n_rows;
+    r.seg_offsets = seg_offsets;
+    r.masked_m = masked_m;
+    r.cap = cap;
+    r.seg_expert = seg_expert;
+    r.S = S;
+    r.n_listed = S_listed;
+    r.E = E;
+    r.H = H;
+    r.I = I;
+    r.extra_lo = extra_lo;
+    r.extra_hi = extra_lo + extra_rows;
+    r.extra_expert = extra_expert;
+    r.w_gate_up_packed = w_gate_up;
+    r.w_down_packed = w_down;
+    r.h = h;
+    r.y_perm = y_perm;
+    r.ready = ready;
+    r.status = moe_host::status_ptr(ws);
+    r.interleave = sched ? sched->interleave : 1;
+    r.ph1_shift = (sched && sched->ph1_shift >= 0) ? sched->ph1_shift : (H + I / 2) / I;
+    r.max_pair_tiles = ((n_rows + 255) / 256 + S) * (int64_t)(I / 128 + H / 256);
+    return moe_pair::run(r, st);
+  }
+
   FfnParams p{};
   p.seg_offsets = seg_offsets;
   p.seg_expert = seg_expert;
@@ -1089,7 +868,7 @@ extern "C" moe_status moe_grouped_ffn_packed_scheduled(
     return MOE_ERR_INVALID_ARG;
   if (shared_rows > 0 && (shared_expert < 0 || shared_expert >= E)) return MOE_ERR_INVALID_ARG;
   if (schedule && (schedule->ph1_shift < -1 || (schedule->interleave & ~1) != 0 ||
-                   (schedule->small_tiles & ~1) != 0))
+                   (schedule->small_tiles & ~1) != 0 || (schedule->cta_pairs & ~1) != 0))
     return MOE_ERR_INVALID_ARG;
   return run_ffn(x_perm, n_rows, seg_offsets, seg_expert, S, E, w_gate_up_packed, w_down_packed, H,
                  I, h, y_perm, ws, ws_bytes, stream, true, nullptr, 1, 0, nullptr, 0, shared_row0,

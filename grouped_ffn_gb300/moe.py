@@ -45,9 +45,13 @@ class RouteCfg(ctypes.Structure):
 
 class FfnSchedule(ctypes.Structure):
     """moe_ffn_schedule: which CTA runs which FFN tile (never a row's bits).
-    ph1_shift -1 = default; interleave and small_tiles 1 = default."""
+    ph1_shift -1 = default; interleave and small_tiles 1 = default; cta_pairs
+    1 runs tiles on pairs of SMs (0 = default)."""
     _fields_ = [("ph1_shift", ctypes.c_int32), ("interleave", ctypes.c_int32),
-                ("small_tiles", ctypes.c_int32)]
+                ("small_tiles", ctypes.c_int32), ("cta_pairs", ctypes.c_int32)]
+
+    def __init__(self, ph1_shift=-1, interleave=1, small_tiles=1, cta_pairs=0):
+        super().__init__(ph1_shift, interleave, small_tiles, cta_pairs)
 
 
 class PlacementC(ctypes.Structure):

@@ -491,16 +491,22 @@ moe_status moe_grouped_ffn_packed_shared(const uint16_t *x_perm, int64_t n_rows,
  *  interleave   1: merge the tiles of segments with several 128-row blocks
  *               and of one-block segments in proportion to their counts (the
  *               default); 0: plain segment order.
- *  small_tiles  1: a tile whose segment ends within 64 rows of its first row
- *               runs as an M = 64 tile (the default); 0: every tile M = 128. */
+ *  small_tiles  single-SM tiles only: 1, a tile whose segment ends within 64
+ *               rows of its first row runs as an M = 64 tile (the default);
+ *               0, every tile M = 128.
+ *  cta_pairs    0: one SM per tile (the default); 1: tiles of 256 rows run on
+ *               pairs of SMs (tcgen05 cta_group::2, a cluster of two CTAs;
+ *               each SM stages its own rows and half of every weight tile).
+ *               Same bits; slower on the layers measured here. */
 typedef struct {
   int32_t ph1_shift;
   int32_t interleave;
   int32_t small_tiles;
+  int32_t cta_pairs;
 } moe_ffn_schedule;
 
 /* moe_grouped_ffn_packed_shared with an explicit tile schedule (NULL: the
- * default one, {-1, 1, 1}).  Same arguments and results otherwise;
+ * default one, {-1, 1, 1, 0}).  Same arguments and results otherwise;
  * MOE_ERR_INVALID_ARG for ph1_shift < -1 or flags outside {0, 1}. */
 moe_status moe_grouped_ffn_packed_scheduled(
     const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_offsets,

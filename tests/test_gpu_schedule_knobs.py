@@ -4,7 +4,8 @@ arithmetic of a row: the layer's h, y_perm and y are bit-identical under
 every setting.  ph1_shift (phase-1 positions given first to the CTAs with
 one gate/up tile fewer) and interleave=0 (plain segment order) change which
 CTA runs a tile and when; small_tiles=0 runs segments of at most 64 rows as
-128-row tiles instead of M = 64 ones."""
+128-row tiles instead of M = 64 ones; cta_pairs=1 runs 256-row tiles on a pair
+of SMs (tcgen05 cta_group::2) instead of 128-row tiles on one."""
 
 import hashlib
 
@@ -50,8 +51,8 @@ def test_tile_schedules_give_identical_bits():
     from grouped_ffn_gb300 import moe
     ref, small = _layer_hash(None)
     assert small >= 8, small   # the M = 64 path is exercised
-    for sched in ((0, 1, 1), (7, 1, 1), (-1, 0, 1), (0, 0, 1), (-1, 1, 0), (-1, 0, 0),
-                  (-1, 1, 1)):
+    for sched in ((0, 1, 1, 1), (7, 1, 1, 1), (-1, 0, 1, 1), (0, 0, 1, 1), (-1, 1, 1, 1),
+                  (-1, 1, 1, 0), (0, 1, 1, 0), (-1, 0, 1, 0), (-1, 1, 0, 0), (-1, 0, 0, 0)):
         assert _layer_hash(moe.FfnSchedule(*sched)) == (ref, small), sched
 
 
@@ -66,7 +67,7 @@ def test_schedule_arguments_are_checked():
     h = torch.empty(4, 128, dtype=torch.bfloat16, device=dev)
     y = torch.empty(4, 256, dtype=torch.bfloat16, device=dev)
     ws = moe.new_workspace(4, 1, 1, device=dev)
-    for bad in ((-2, 1, 1), (0, 2, 1), (0, 1, -1)):
+    for bad in ((-2, 1, 1, 1), (0, 2, 1, 1), (0, 1, -1, 1), (0, 1, 1, 2)):
         with pytest.raises(moe.MoeError):
             moe.moe_grouped_ffn_packed_scheduled(x, offs, ex, wgu, wd, 0, 0, 0,
                                                  moe.FfnSchedule(*bad), h, y, ws)
