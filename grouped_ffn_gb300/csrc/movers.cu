@@ -294,6 +294,52 @@ __global__ void balance_kernel(const int32_t *__restrict__ rc, int R, double *ba
   }
 }
 
+// Balancedness over L layers: the sum of the layers' mean per-rank loads
+// over the sum of their busiest-rank loads ("The slowest expert sets the
+// pace": avg_tokens / max_tokens summed across layers).  One warp per layer
+// at a time, then a block reduction; the fp64 division is the per-layer
+// formula's, total / (R * sum of maxima).
+__global__ void balance_layers_kernel(const int32_t *__restrict__ rc, int L, int R, double *bal,
+                                      int64_t *max_sum, int64_t *total) {
+  moe::pdl_wait();
+  moe::pdl_trigger();
+  __shared__ long long s_tot[32], s_max[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  long long tsum = 0, msum = 0;
+  for (int l = warp; l < L; l += nw) {
+    const int32_t *row = rc + (int64_t)l * R;
+    long long ls = 0;
+    int lm = 0;
+    for (int r = lane; r < R; r += 32) {
+      const int v = row[r];
+      ls += v;
+      lm = max(lm, v);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      ls += __shfl_xor_sync(0xffffffffu, ls, off);
+      lm = max(lm, __shfl_xor_sync(0xffffffffu, lm, off));
+    }
+    tsum += ls;
+    msum += lm;
+  }
+  if (lane == 0) {
+    s_tot[warp] = tsum;
+    s_max[warp] = msum;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long T = 0, M = 0;
+    for (int i = 0; i < nw; ++i) {
+      T += s_tot[i];
+      M += s_max[i];
+    }
+    *total = T;
+    *max_sum = M;
+    *bal = (T == 0) ? 1.0 : (double)T / ((double)R * (double)M);
+  }
+}
+
 unsigned mover_grid(int64_t T) {
   const int64_t cap = (int64_t)moe_host::sm_count() * 32;
   return (unsigned)(T < cap ? T : cap);
@@ -394,6 +440,16 @@ extern "C" moe_status moe_combine_masked(const uint16_t *y_perm, int64_t n_rows,
                                          void *ws, size_t ws_bytes, void *stream) {
   return run_combine(y_perm, n_rows, dest_row, topk_w, T, k, H, shared, y, 1, ws, ws_bytes,
                      stream);
+}
+
+extern "C" moe_status moe_balance_stats_layers(const int32_t *rank_counts, int32_t L, int32_t R,
+                                               double *balancedness, int64_t *max_sum,
+                                               int64_t *total, void *stream) {
+  if (L < 1 || R < 1 || !rank_counts || !balancedness || !max_sum || !total)
+    return MOE_ERR_INVALID_ARG;
+  return moe_host::launch_pdl(balance_layers_kernel, dim3(1), dim3(256), 0,
+                              static_cast<cudaStream_t>(stream), rank_counts, L, R, balancedness,
+                              max_sum, total);
 }
 
 extern "C" moe_status moe_balance_stats(const int32_t *rank_counts, int32_t R, double *balancedness,

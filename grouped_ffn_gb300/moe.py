@@ -97,6 +97,7 @@ _SIGNATURES = {
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "moe_combine_merged": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(PlacementC), _I64, _I32,
                                           _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_balance_stats_layers": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
     "moe_balance_stats": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_layout_masked": (ctypes.c_int, [_P, _I64, _I32, ctypes.POINTER(PlacementC),
                                                   _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
@@ -452,6 +453,19 @@ def moe_combine_merged(y_perm, dest_row, topk_w, slot, placement: DevicePlacemen
     _check("moe_combine_merged", lib().moe_combine_merged(
         _ptr(y_perm), _ptr(dest_row), _ptr(topk_w), _ptr(slot), ctypes.byref(placement.c), T, k,
         y.shape[1], _ptr(shared), _ptr(y), _ptr(messages), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_balance_stats_layers(rank_counts, balancedness, max_sum, total, stream=None):
+    """Balancedness over layers: rank_counts int32 [L, R]; outputs device
+    float64[1], int64[1], int64[1]."""
+    _need(rank_counts, torch.int32, "rank_counts")
+    _need(balancedness, torch.float64, "balancedness")
+    _need(max_sum, torch.int64, "max_sum")
+    _need(total, torch.int64, "total")
+    L, R = rank_counts.shape
+    _check("moe_balance_stats_layers", lib().moe_balance_stats_layers(
+        _ptr(rank_counts), L, R, _ptr(balancedness), _ptr(max_sum), _ptr(total),
+        _stream(stream)))
 
 
 def moe_balance_stats(rank_counts, balancedness, max_count, total, ws=None, stream=None):

@@ -585,6 +585,20 @@ moe_status moe_balance_stats(const int32_t *rank_counts, int32_t R, double *bala
                              int32_t *max_count, int64_t *total, void *ws, size_t ws_bytes,
                              void *stream);
 
+/* Balancedness of a step over L MoE layers.  "14. Serving Mixture-of-Experts
+ * Models", "The slowest expert sets the pace": avg_tokens / max_tokens,
+ * "summed across layers".  Reading: both are summed over the layers -- the
+ * sum of each layer's mean per-rank load over the sum of each layer's
+ * busiest-rank load, computed as total / (R * max_sum) in fp64; 1.0 when
+ * total is 0.  With L = 1 this is moe_balance_stats.
+ *  rank_counts device int32 [L][R] (row l: one layer's rank_counts).
+ *  balancedness device double, max_sum device int64 (sum over layers of the
+ *  busiest rank's load), total device int64 (all assignments).
+ *  Limits: L >= 1, R >= 1. */
+moe_status moe_balance_stats_layers(const int32_t *rank_counts, int32_t L, int32_t R,
+                                    double *balancedness, int64_t *max_sum, int64_t *total,
+                                    void *stream);
+
 /* Static text for a status code. */
 const char *moe_status_string(moe_status status);
 

@@ -521,6 +521,24 @@ def balance_stats(rank_counts: np.ndarray):
     return float(total) / (float(len(rc)) * float(mx)), mx, total
 
 
+def balance_stats_layers(rank_counts: np.ndarray):
+    """Balancedness of a step over several MoE layers ([MoE14] "The slowest
+    expert sets the pace": avg_tokens / max_tokens, "summed across
+    layers").  Reading: avg_tokens and max_tokens are each summed over the
+    layers -- the sum of every layer's mean per-rank load over the sum of
+    every layer's busiest-rank load; one layer gives balance_stats.
+    rank_counts [L, R].  Returns (balancedness, sum of per-layer maxima,
+    total); balancedness is 1.0 when nothing is routed."""
+    rc = np.asarray(rank_counts, dtype=np.int64)
+    L, R = rc.shape
+    avg_sum = sum(float(rc[l].sum()) / float(R) for l in range(L))
+    max_sum = int(sum(int(rc[l].max()) for l in range(L))) if R else 0
+    total = int(rc.sum())
+    if total == 0:
+        return 1.0, max_sum, total
+    return avg_sum / float(max_sum), max_sum, total
+
+
 # ------------------------------------------------------------------ layer
 def moe_layer_tokens(tokens, logits, x_bits, w_gate_up, w_down, pl, route_cfg,
                      shared_w=None, I=None, shared_I=None):

@@ -323,6 +323,34 @@ def test_worked_example_on_gpu(case):
     assert b.item() == cs["balancedness_num"] / cs["balancedness_den"]
 
 
+@pytest.mark.parametrize("L,R", [(1, 8), (2, 4), (7, 32), (61, 16), (3, 1024), (40, 1), (1, 1)])
+def test_balance_stats_layers_bit_exact(L, R):
+    """Balancedness summed across layers: the double, the sum of per-layer
+    maxima and the total are the oracle's bit for bit; the mirrored worked
+    example gives 4/9, one layer gives moe_balance_stats' value, and an
+    empty step gives 1.0."""
+    m = moe()
+    rng = np.random.default_rng(L * 1000 + R)
+    cases = [rng.integers(0, 5000, size=(L, R)).astype(np.int32),
+             np.zeros((L, R), np.int32)]
+    if (L, R) == (2, 4):
+        cases.append(np.array([[36, 13, 9, 6], [6, 9, 13, 36]], np.int32))
+    for rc in cases:
+        b = torch.empty(1, dtype=torch.float64, device="cuda")
+        mx = torch.empty(1, dtype=torch.int64, device="cuda")
+        tot = torch.empty(1, dtype=torch.int64, device="cuda")
+        m.moe_balance_stats_layers(torch.from_numpy(rc).cuda(), b, mx, tot)
+        ref = oracle.balance_stats_layers(rc)
+        assert (b.item(), int(mx.item()), int(tot.item())) == ref
+        if rc.shape == (2, 4) and rc[0, 0] == 36:
+            assert b.item() == 32.0 / 72.0
+        if L == 1:
+            b1 = torch.empty(1, dtype=torch.float64, device="cuda")
+            mx1 = torch.empty(1, dtype=torch.int32, device="cuda")
+            m.moe_balance_stats(torch.from_numpy(rc[0]).cuda(), b1, mx1, tot)
+            assert b1.item() == b.item()
+
+
 def test_layout_reports_bad_expert_id_without_faulting():
     m = moe()
     pl = wl.make_placement(wl.WORKLOADS["tiny"])

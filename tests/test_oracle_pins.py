@@ -427,3 +427,22 @@ def test_layer_on_sampled_tokens_matches_stagewise_oracle():
     toks = [0, 5, 23]
     y2 = oracle.moe_layer_tokens(toks, lg, x, wgu, wd, pl, cfg, I=w.I)
     assert np.array_equal(y[toks], y2)
+
+
+def test_balancedness_summed_across_layers():
+    """"The slowest expert sets the pace": avg_tokens / max_tokens, summed
+    across layers.  Two layers of the worked example's loads, the second
+    mirrored: means 16 + 16, maxima 36 + 36, so 32/72 = 4/9 (summing the
+    counts first would give 32/42 instead).  One layer reduces to the
+    per-step statistic, identical layers to the one-layer value, and an
+    empty step to 1.0."""
+    a = np.array([36, 13, 9, 6])
+    bal, mx, tot = oracle.balance_stats_layers(np.stack([a, a[::-1]]))
+    assert (mx, tot) == (72, 128) and bal == 32.0 / 72.0
+    assert bal != 32.0 / 42.0
+    one = oracle.balance_stats_layers(a[None, :])
+    assert one[0] == oracle.balance_stats(a)[0] == 16.0 / 36.0
+    three = oracle.balance_stats_layers(np.stack([a, a, a]))
+    assert three[0] == 16.0 / 36.0 and three[1:] == (108, 192)
+    assert oracle.balance_stats_layers(np.zeros((3, 4), dtype=np.int32))[0] == 1.0
+    assert oracle.balance_stats_layers(np.full((2, 8), 5))[0] == 1.0
