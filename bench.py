@@ -65,7 +65,7 @@ def load_peaks():
 # ------------------------------------------------------------------ ncu traffic
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "grouped_ffn_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "grouped_ffn_gb300", "csrc", f)
-                  for f in ("grouped_ffn.cu", "common.cuh", "tile_order.cuh")]
+                  for f in ("grouped_ffn.cu", "common.cuh", "tile_order.cuh", "umma.cuh")]
 
 
 def kernel_source_hash() -> str:
@@ -94,19 +94,29 @@ def mode_name(args) -> str:
     return "+".join(parts)
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes (read + write) per grouped-FFN launch from the committed ncu
-    capture, or None if there is none for this workload or the kernel source
-    changed since it was taken."""
+def measured_traffic(workload: str, algorithmic_bytes: int):
+    """DRAM bytes (read + write) of one grouped-FFN launch, scaled from the
+    committed ncu capture of a smaller case of the same layer shape: the
+    capture's traffic per algorithmic byte times this launch's algorithmic
+    bytes (traffic grows with the weights streamed and the rows moved, as
+    the algorithmic count does).  Returns (bytes, source) or (None, None) if
+    there is no capture for this workload or the kernel source changed since
+    it was taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
-        return None
+        return None, None
     if rec.get("kernel_sha256") != kernel_source_hash():
-        return None
+        return None, None
     w = rec.get("workloads", {}).get(workload)
-    return None if w is None else int(w["dram_bytes_read"]) + int(w["dram_bytes_write"])
+    if w is None:
+        return None, None
+    ratio = (int(w["dram_bytes_read"]) + int(w["dram_bytes_write"])) / int(w["algorithmic_bytes"])
+    src = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of %s (%s), %.3f per algorithmic "
+           "byte, times this launch's algorithmic bytes; %s"
+           % (w["case"], w["command"], ratio, os.path.relpath(TRAFFIC_FILE, ROOT)))
+    return int(round(ratio * algorithmic_bytes)), src
 
 
 # ------------------------------------------------------------------ dist
@@ -509,9 +519,8 @@ def finish(args, w, pl, layer, logits, x, wgu, wd, sgu, sd, names, stage_ms, ms_
         roof = {"bound": "tensor", "achieved": g["flops"] / (g_ms * 1e-3) / 1e12,
                 "peak": t_peak, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(w.name) if mode_name(args) == "" else None
-    roof["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, " +
-                              os.path.relpath(TRAFFIC_FILE, ROOT)) if roof["traffic"] else None
+    roof["traffic"], roof["traffic_source"] = (
+        measured_traffic(w.name, g["bytes"]) if mode_name(args) == "" else (None, None))
     roof["kernel"] = "grouped_ffn_kernel (gate/up + down launches)"
     roof["peak_source"] = peaks["source"] + (" " + t_peak_label if roof["bound"] == "tensor" else
                                              " copy bandwidth")

@@ -121,3 +121,26 @@ def test_headline_and_further_workloads(bench):
     assert bench.extra_workloads(ns(workload="prefill", also="decode,prefill")) == ["decode"]
     rec = {"value": 1.0, "e2e": {}, "cpu_baseline": {}, "stages": {}, "clocks": {}}
     assert set(bench.compact_record(rec)) == {"value", "stages", "clocks"}
+
+
+def test_traffic_is_scaled_from_the_committed_capture(bench, tmp_path, monkeypatch):
+    """roofline.traffic: the capture's DRAM bytes per algorithmic byte times
+    the full launch's algorithmic bytes, and nothing once the kernel source
+    differs from the captured one."""
+    import json
+    rec = {"kernel_sha256": bench.kernel_source_hash(),
+           "workloads": {"prefill": {"case": "small", "command": "cmd", "dram_bytes_read": 900,
+                                     "dram_bytes_write": 110, "algorithmic_bytes": 1000}}}
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    t, src = bench.measured_traffic("prefill", 5000)
+    assert t == 5050 and "1.010 per algorithmic byte" in src
+    assert bench.measured_traffic("decode", 5000) == (None, None)
+    rec["kernel_sha256"] = "0" * 64
+    f.write_text(json.dumps(rec))
+    assert bench.measured_traffic("prefill", 5000) == (None, None)
+    # the committed record covers every bench workload and matches the sources
+    with open(os.path.join(ROOT, "profiles", "grouped_ffn_traffic.json")) as fh:
+        committed = json.load(fh)
+    assert set(committed["workloads"]) >= {"group_limited", "prefill", "replica", "decode"}
