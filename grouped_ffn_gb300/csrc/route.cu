@@ -100,6 +100,66 @@ __device__ F group_score(const float (&v)[VPL], uint32_t avail, int lane, int n_
   return mine;
 }
 
+// Groups of exactly 32 experts (element i of every lane is group i) with a
+// score over at most the top 2 logits: every lane computes every group's
+// score at once.  Per group, a 5-step butterfly merges the lanes' (largest,
+// second largest) pairs into the group's two largest logits (as a multiset,
+// so equal logits count twice, as in a selection one at a time); the score
+// is sigmoid(largest) + sigmoid(second), in the same order and precision as
+// group_score.  Then each lane ranks the groups itself (score descending,
+// id ascending, the order select_groups uses): the kept set, the last kept
+// score and the best dropped one, with no further shuffles.
+template <int VPL>
+__device__ __forceinline__ uint32_t select_groups_g32(const float (&v)[VPL], int n_groups,
+                                                      int top_n, int n_sel, float &last_kept,
+                                                      float &best_dropped) {
+  float a1[VPL], a2[VPL];
+#pragma unroll
+  for (int g = 0; g < VPL; ++g) {
+    a1[g] = v[g];
+    a2[g] = -FLT_MAX;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+    for (int g = 0; g < VPL; ++g) {
+      if (g < n_groups) {
+        const float o1 = __shfl_xor_sync(0xffffffffu, a1[g], off);
+        const float o2 = __shfl_xor_sync(0xffffffffu, a2[g], off);
+        const float hi = a1[g] >= o1 ? a1[g] : o1;
+        const float lo = a1[g] >= o1 ? o1 : a1[g];
+        const float sec = a2[g] >= o2 ? a2[g] : o2;
+        a1[g] = hi;
+        a2[g] = lo >= sec ? lo : sec;
+      }
+    }
+  }
+  float sc[VPL];
+#pragma unroll
+  for (int g = 0; g < VPL; ++g) {
+    sc[g] = 0.0f;
+    if (g < n_groups) {
+      sc[g] = sigmoid32(a1[g]);
+      if (top_n > 1) sc[g] = sc[g] + sigmoid32(a2[g]);
+    }
+  }
+  uint32_t kept = 0;
+  last_kept = 0.0f;
+  best_dropped = -INFINITY;
+#pragma unroll
+  for (int g = 0; g < VPL; ++g) {
+    if (g >= n_groups) continue;
+    int rank = 0;
+#pragma unroll
+    for (int h = 0; h < VPL; ++h)
+      if (h < n_groups && h != g && (sc[h] > sc[g] || (sc[h] == sc[g] && h < g))) ++rank;
+    if (rank < n_sel) kept |= 1u << g;
+    if (rank == n_sel - 1) last_kept = sc[g];
+    if (rank == n_sel) best_dropped = sc[g];
+  }
+  return kept;
+}
+
 // Bit mask of the n_sel best groups (lane g holds group g's score; ties to
 // the lower id), with the score of the last one kept and of the best one
 // left out (-inf if none).
@@ -194,10 +254,16 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
       // the fp64 selection is the same set; otherwise the warp recomputes
       // the scores in fp64 and selects again.
       const bool gvalid = lane < a.n_groups;
-      const float my_g32 = group_score<VPL, float>(v, avail, lane, a.n_groups, gid, a.group_topn);
       float last_kept, best_dropped;
-      uint32_t kept = select_groups<float>(my_g32, gvalid, lane, a.topk_groups, last_kept,
-                                           best_dropped);
+      uint32_t kept;
+      if (gsz == 32 && a.group_topn <= 2) {
+        kept = select_groups_g32<VPL>(v, a.n_groups, a.group_topn, a.topk_groups, last_kept,
+                                      best_dropped);
+      } else {
+        const float my_g32 =
+            group_score<VPL, float>(v, avail, lane, a.n_groups, gid, a.group_topn);
+        kept = select_groups<float>(my_g32, gvalid, lane, a.topk_groups, last_kept, best_dropped);
+      }
       const float n = (float)a.group_topn;
       const float eps = n * 2e-7f + (n - 1.0f) * n * 6e-8f;
       if (a.topk_groups < a.n_groups && !(last_kept - best_dropped > 4.0f * eps)) {

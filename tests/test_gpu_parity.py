@@ -220,6 +220,36 @@ def test_route_group_limited_near_ties_decided_in_fp64():
     np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
 
 
+@pytest.mark.parametrize("topn", [1, 2])
+def test_route_groups_of_32_near_ties_and_repeated_maxima(topn):
+    """Groups of exactly 32 experts (the group-limited layer's shape, whose
+    group scores are merged across the warp in one pass): exact and
+    one-to-three-ulp ties at the group cut must agree with the oracle
+    (fp64 decides, ties to the lower group id), and a group whose largest
+    logit appears twice scores it twice."""
+    rng = np.random.default_rng(44 + topn)
+    E, n_groups, gsz, T = 256, 8, 32, 1024
+    lg = rng.normal(-4.0, 0.5, size=(T, E)).astype(np.float32)
+    one = np.float32(1.0)
+    for t in range(T):
+        a, b, c = rng.choice(n_groups, size=3, replace=False)
+        ulps = int(rng.integers(0, 4))             # 0 = exact tie
+        hi = one
+        for _ in range(ulps):
+            hi = np.nextafter(hi, np.float32(2.0))
+        la, lb = rng.choice(gsz, size=2, replace=False), rng.choice(gsz, size=2, replace=False)
+        lg[t, a * gsz + la] = [one, one]
+        lg[t, b * gsz + lb] = [one, hi] if topn == 2 else [hi, -9.0]
+        lg[t, c * gsz + rng.choice(gsz, size=2, replace=False)] = [np.float32(3.0)] * 2
+    w = wl.Workload("g32", 0, T=T, H=8, E=E, k=8, I=8, R=1, ranks_per_node=1,
+                    score_fn=wl.SCORE_SIGMOID, n_groups=n_groups, topk_groups=2, group_topn=topn)
+    ids, wts = gpu_route(w, torch.from_numpy(lg).cuda())
+    rid, rw, margin = oracle_route(w, lg)
+    assert margin < 1e-7                           # the cut really is a near tie
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
+
+
 # ------------------------------------------------------------------ layout + balance
 @pytest.mark.parametrize("name,zipf", [(n, None) for n in ALL] +
                          [("replica", s) for s in (0.0, 0.5, 1.5)])
@@ -253,6 +283,28 @@ def test_layout_many_tiles_many_slots_and_ragged_tail():
     ref = oracle.dispatch_layout(ids_np, pl)
     for key in ref:
         assert np.array_equal(got[key], ref[key]), key
+
+
+def test_layout_tile_counts_in_turn_on_one_workspace():
+    """69 tiles of 4096 assignments, then 2, 64, 1 and 65, then 69 again,
+    all on one workspace with no clearing in between: every call must leave
+    the tile ticket and the look-back flags zero for the next one, whatever
+    its tile count (the single-tile call finalizes in its scan CTA and
+    writes no flag)."""
+    m = moe()
+    E, R, k = 64, 8, 2
+    pl = wl.placement_from_hosts(E, R, 8, wl.round_robin_hosts(E, R))
+    pl_dev = m.DevicePlacement.from_tables(pl)
+    rng = np.random.default_rng(33)
+    T_max = 141_000                      # 282,000 assignments: 69 tiles
+    ws = m.new_workspace(T_max, k, pl_dev.n_slots)
+    for T in (T_max, 4001, 64 * 2048, 1500, 131_073, T_max):
+        ids_np = rng.integers(0, E, size=(T, k)).astype(np.int32)
+        ids_np[:, 1] = (ids_np[:, 0] + 1 + rng.integers(0, E - 1, size=T)) % E
+        got = gpu_layout(torch.from_numpy(ids_np).cuda(), pl_dev, T, k, ws=ws)
+        ref = oracle.dispatch_layout(ids_np, pl)
+        for key in ref:
+            assert np.array_equal(got[key], ref[key]), (T, key)
 
 
 def test_layout_with_explicit_token_source_ranks():
