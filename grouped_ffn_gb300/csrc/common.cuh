@@ -27,6 +27,9 @@ enum KernelId : int32_t {
 //   [1] detail (offending index, or elapsed wait in microseconds)
 //   [2] KernelId of the reporter
 constexpr size_t kStatusBytes = MOE_WS_STATUS_BYTES;
+// Status-block word [16]: the grouped FFN's count of finished CTAs; the
+// last CTA of a launch clears it and the per-segment readiness counters.
+constexpr int kFfnExitWord = 16;
 
 // Workspace map (bytes): [0, 256) status block; [256, 256 + 4 * 1024) the
 // grouped FFN's per-segment readiness counters; [4352, 4608) the layout's
@@ -112,6 +115,27 @@ inline moe_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Cooperative launch (every CTA resident at once, so CTAs may wait for one
+// another) with programmatic stream serialization as well.
+template <typename... KArgs, typename... Args>
+inline moe_status launch_coop_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

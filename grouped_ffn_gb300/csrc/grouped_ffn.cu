@@ -109,7 +109,8 @@ struct FfnParams {
   int32_t S, E, n_rows;
   int32_t b_packed;   // B in the tile-contiguous layout (see moe_pack_expert_weights)
   int32_t n_phases;   // 2: phase 1 reads what phase 0 writes, in the same launch
-  int32_t *ready;     // [S] finished phase-0 tiles per segment (zeroed by the host)
+  int32_t *ready;     // [S] finished phase-0 tiles per segment (zero on entry)
+  uint32_t *exit_count;  // finished CTAs; the last one re-zeroes ready[0, S) and this
   int32_t interleave; // merge multi-tile and one-tile segments' tiles (tile_order.cuh)
   int32_t ph1_shift;  // phase-1 positions that go first to the CTAs with one gate/up tile fewer
   int32_t small_rows; // segments with at most this many rows run M = 64 tiles (0: none)
@@ -224,6 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kStages stages, so at most kStages tiles, ahead of the MMA: 8 entries
   // are never overwritten before they are read.
   uint8_t *tile_small = smem + kMiscOff + 16;
+  // set in the CTA that finishes last (the one that clears the counters)
+  volatile int32_t *last_cta = reinterpret_cast<int32_t *>(smem + kMiscOff + 24);
   int32_t *seg_off = reinterpret_cast<int32_t *>(smem + kSegOff);  // [S] first row of s
   int32_t *pre_h = seg_off + (kMaxSegs + 1);  // [S+1] m-tiles before s, multi-tile segments
   int32_t *pre_c = pre_h + (kMaxSegs + 1);    // [S+1] m-tiles before s, one-tile segments
@@ -250,6 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  // Launched behind the permute with programmatic dependent launch: the
+  // set-up above overlaps its tail; nothing it writes is read before this.
+  moe::pdl_wait();
   // the next kernel on the stream (the combine) may start launching now; it
   // waits (griddepcontrol.wait) until this grid has finished
   moe::pdl_trigger();
@@ -591,6 +597,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  // Every wait on and increment of a readiness counter is behind each CTA
+  // that has finished: the last one to finish clears them for the next
+  // launch on this workspace (no memset between the permute and this kernel).
+  if (threadIdx.x == 0) {
+    __threadfence();
+    *last_cta = atomicAdd(p.exit_count, 1u) == gridDim.x - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (*last_cta) {
+    for (int s = threadIdx.x; s < p.S; s += kThreads) p.ready[s] = 0;
+    if (threadIdx.x == 0) *p.exit_count = 0u;
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -637,26 +655,17 @@ bool ensure_smem_attr() {
 }
 
 // Cooperative launch: every CTA is resident at once, so a phase-1 tile that
-// waits for phase-0 tiles of other CTAs can always be satisfied.
+// waits for phase-0 tiles of other CTAs can always be satisfied.  With
+// programmatic dependent launch, so that the launch and the set-up overlap
+// the tail of the kernel before it (the permute).
 moe_status launch(const CUtensorMap &a0, const CUtensorMap &b0, const CUtensorMap &a1,
                   const CUtensorMap &b1, const CUtensorMap &a0s, const CUtensorMap &a1s,
                   const FfnParams &p, int64_t max_tiles, cudaStream_t st) {
   int64_t grid = moe_host::sm_count();
   if (max_tiles < grid) grid = max_tiles;
   if (grid < 1) return MOE_OK;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, grouped_ffn_kernel, a0, b0, a1, b1, a0s, a1s, p) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return moe_host::launch_status();
+  return moe_host::launch_coop_pdl(grouped_ffn_kernel, dim3((unsigned)grid), dim3(kThreads),
+                                   kSmemBytes, st, a0, b0, a1, b1, a0s, a1s, p);
 }
 
 // Pack kernel: W[e][row][k] -> P[e][nb][kb][half][128][64] in 16-byte units.
@@ -743,12 +752,14 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t m_tiles_max = (n_rows + kBM - 1) / kBM + S;  // sum of ceil(count/128)
   int32_t *ready = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kReadyOff);
-  if (cudaMemsetAsync(ready, 0, (size_t)S * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
 
   // packed weights and rows from a dispatched buffer: SM pairs when the
   // schedule asks for them (measured slower than single-SM tiles on every
   // layer here, so not the default)
   if (packed && gather_src == nullptr && sched != nullptr && sched->cta_pairs) {
+    // this kernel leaves its counters set: clear them before and after
+    if (cudaMemsetAsync(ready, 0, (size_t)S * sizeof(int32_t), st) != cudaSuccess)
+      return MOE_ERR_CUDA;
     moe_pair::PairRun r{};
     r.x_perm = x_perm;
     r.n_rows = n_rows;
@@ -773,7 +784,10 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
     r.interleave = sched ? sched->interleave : 1;
     r.ph1_shift = (sched && sched->ph1_shift >= 0) ? sched->ph1_shift : (H + I / 2) / I;
     r.max_pair_tiles = ((n_rows + 255) / 256 + S) * (int64_t)(I / 128 + H / 256);
-    return moe_pair::run(r, st);
+    if (moe_status s = moe_pair::run(r, st)) return s;
+    return cudaMemsetAsync(ready, 0, (size_t)S * sizeof(int32_t), st) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
   }
 
   FfnParams p{};
@@ -790,6 +804,7 @@ moe_status run_ffn(const uint16_t *x_perm, int64_t n_rows, const int32_t *seg_of
   p.n_phases = 2;
   p.ready = ready;
   p.status = moe_host::status_ptr(ws);
+  p.exit_count = reinterpret_cast<uint32_t *>(ws) + moe::kFfnExitWord;
   // schedule: which CTA runs which tile, never a row's arithmetic
   p.interleave = sched ? sched->interleave : 1;
   // a gate/up tile (depth H) takes about H/I down tiles' time (depth I)

@@ -415,6 +415,12 @@ moe_status moe_dequant_fp8(const uint8_t *xq, const float *x_scale, int64_t n_ro
  *  in one cooperative launch, a segment's down-projection tiles starting
  *  as soon as all its gate/up tiles have stored h.
  *  ws: at least 256 + 4*S bytes (moe_workspace_size(T, k, S) is enough).
+ *  Its per-segment readiness counters (bytes [256, 256 + 4*S)) and the
+ *  finished-CTA counter (status-block word 16) must be zero on entry:
+ *  moe_workspace_init makes them so, and the last CTA of every launch
+ *  clears them again (no per-call memset).  The launch uses programmatic
+ *  dependent launch: it may begin while the previous kernel on the stream
+ *  drains, and reads nothing before that kernel has finished.
  *  Limits: H % 256 == 0, I % 128 == 0, S <= 1024, n_rows < 2^31,
  *  E*2I*H/64 < 2^31, and a tile list of (ceil(n_rows/128) + S) *
  *  (I/128 + H/256) < 2^31 tiles.
