@@ -158,9 +158,9 @@ class MoELayer:
             small and packed and not gather and masked_cap is None and replica_relax is None
             and placement.n_slots == placement.n_experts) else 0
         self._ev_route = torch.cuda.Event()
-        # the layout scan takes up to 4096 assignments in one CTA, which then
+        # the layout scan takes up to 1024 assignments in one CTA, which then
         # also finalizes (no second launch) on the contiguous layout
-        one_tile = max_tokens * k <= 4096 and masked_cap is None
+        one_tile = max_tokens * k <= 1024 and masked_cap is None
         self.launches_per_step = 7 + (1 if shared_w_gate_up is not None else 0) + \
             (4 if replica_relax is not None else 0) + (1 if replica_refine else 0) - \
             (1 if gather else 0) + \

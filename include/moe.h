@@ -291,7 +291,7 @@ moe_status moe_dispatch_layout_routed(const int32_t *topk_ids, const int32_t *sl
  *  Scratch: a fixed 1 MiB device array inside the library (one per GPU that
  *  loads it, held until the process exits).  Nothing is allocated per call:
  *  no cudaMalloc, cudaFree or allocating library routine.
- *  Limit: 64 + ceil(T*k / 4096) * n_slots <= 262144 (32-bit words);
+ *  Limit: 64 + ceil(T*k / 1024) * n_slots <= 262144 (32-bit words);
  *  larger requests return MOE_ERR_UNSUPPORTED without launching.
  *  The first call on each device looks up the array's device address (with
  *  that device current) and caches it; make that first call before any

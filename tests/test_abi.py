@@ -45,9 +45,9 @@ def test_status_strings(lib):
 def test_workspace_size(lib):
     from grouped_ffn_gb300 import moe
     # status block (256) + FFN readiness counters (4096) + ticket block (256)
-    # + one 32-bit flag per (4096-assignment tile, slot)
-    assert moe.moe_workspace_size(4000, 2, 64) == 4608 + 2 * 64 * 4
-    assert moe.moe_workspace_size(16384, 4, 40) == 4608 + 16 * 40 * 4
+    # + one 32-bit flag per (1024-assignment tile, slot)
+    assert moe.moe_workspace_size(4000, 2, 64) == 4608 + 8 * 64 * 4
+    assert moe.moe_workspace_size(16384, 4, 40) == 4608 + 64 * 40 * 4
     assert moe.moe_workspace_size(0, 2, 64) == 4608 + 64 * 4
     assert moe.moe_workspace_size(-1, 2, 64) == 0
 

@@ -66,7 +66,7 @@ def test_masked_layout_parity(name, cap):
 
 
 def test_masked_layout_drops_across_many_tiles_and_ragged_tail():
-    """Several 4096-assignment tiles and a ragged last one, with a capacity
+    """Several 1024-assignment tiles and a ragged last one, with a capacity
     small enough that drops happen in every tile: which assignments keep a
     row must follow assignment order across tile boundaries."""
     m = moe()

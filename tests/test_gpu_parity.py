@@ -273,7 +273,7 @@ def test_layout_and_balance_parity(name, zipf):
 
 
 def test_layout_many_tiles_many_slots_and_ragged_tail():
-    # 25 tiles of 4096 assignments (the last one ragged), 1024 slots on 256 ranks
+    # 100 tiles of 1024 assignments (the last one ragged), 1024 slots on 256 ranks
     T, k, E, R = 51111, 2, 1024, 256
     rng = np.random.default_rng(11)
     ids_np = rng.integers(0, E, size=(T, k)).astype(np.int32)
@@ -286,11 +286,10 @@ def test_layout_many_tiles_many_slots_and_ragged_tail():
 
 
 def test_layout_tile_counts_in_turn_on_one_workspace():
-    """69 tiles of 4096 assignments, then 2, 64, 1 and 65, then 69 again,
-    all on one workspace with no clearing in between: every call must leave
-    the tile ticket and the look-back flags zero for the next one, whatever
-    its tile count (the single-tile call finalizes in its scan CTA and
-    writes no flag)."""
+    """276 tiles of 1024 assignments, then 8, 256, 3 and 257, then 276
+    again, all on one workspace with no clearing in between: every call
+    must leave the tile ticket and the look-back flags zero for the next
+    one, whatever its tile count."""
     m = moe()
     E, R, k = 64, 8, 2
     pl = wl.placement_from_hosts(E, R, 8, wl.round_robin_hosts(E, R))

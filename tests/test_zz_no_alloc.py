@@ -89,7 +89,7 @@ def test_layout_after_an_empty_call_on_the_same_scratch(name):
 
 def test_noalloc_layout_rejects_requests_beyond_its_scratch():
     from grouped_ffn_gb300 import moe
-    # 1024 slots x 256 tiles of 4096 assignments needs more than 262144 flag words
+    # 1024 slots x 1024 tiles of 1024 assignments needs more than 262144 flag words
     E = R = 1024
     pl = wl.placement_from_hosts(E, R, 8, wl.round_robin_hosts(E, R))
     pl_dev = moe.DevicePlacement.from_tables(pl)
@@ -103,7 +103,7 @@ def test_noalloc_layout_rejects_requests_beyond_its_scratch():
 
 
 def test_noalloc_device_error_reaches_status_and_the_next_call_is_clean():
-    """An expert id out of range in a layout of several 4096-assignment tiles
+    """An expert id out of range in a layout of several 1024-assignment tiles
     is reported in the caller's status array (MOE_ERR_DEVICE_INDEX) rather
     than dropped; the shared scratch it leaves behind does not disturb the
     next call, which again gives the workspace layout."""
