@@ -18,7 +18,10 @@
 namespace {
 
 constexpr int kMoverThreads = 128;
-constexpr int kUnroll = 4;
+// The permute loads up to 8 x 16 bytes a thread before storing: a 16 KiB
+// row (hidden 8192) in one pass of its 128 threads (measured 3-4% faster
+// than 4 on the group-limited and replica layers, the same on prefill).
+constexpr int kPermUnroll = 8;
 
 // EXTRA: token t is also copied to row extra_row0 + t (the rows a shared
 // expert runs on inside the same grouped FFN launch).
@@ -31,10 +34,10 @@ __global__ void __launch_bounds__(kMoverThreads) permute_kernel(
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     const uint4 *src = x + t * H8;
     const int32_t *dr = dest_row + t * k;
-    for (int c0 = threadIdx.x; c0 < H8; c0 += kMoverThreads * kUnroll) {
-      uint4 v[kUnroll];
+    for (int c0 = threadIdx.x; c0 < H8; c0 += kMoverThreads * kPermUnroll) {
+      uint4 v[kPermUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < kPermUnroll; ++u) {
         const int c = c0 + u * kMoverThreads;
         if (c < H8) v[u] = moe::ld_stream_u4(src + c);
       }
@@ -47,7 +50,7 @@ __global__ void __launch_bounds__(kMoverThreads) permute_kernel(
         }
         uint4 *dst = xp + (int64_t)r * H8;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kPermUnroll; ++u) {
           const int c = c0 + u * kMoverThreads;
           if (c < H8) dst[c] = v[u];
         }
@@ -55,7 +58,7 @@ __global__ void __launch_bounds__(kMoverThreads) permute_kernel(
       if (EXTRA) {
         uint4 *dst = xp + (extra_row0 + t) * H8;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kPermUnroll; ++u) {
           const int c = c0 + u * kMoverThreads;
           if (c < H8) dst[c] = v[u];
         }
