@@ -9,6 +9,8 @@ of SMs (tcgen05 cta_group::2) instead of 128-row tiles on one."""
 
 import hashlib
 
+import numpy as np
+
 import pytest
 import torch
 
@@ -71,3 +73,50 @@ def test_schedule_arguments_are_checked():
         with pytest.raises(moe.MoeError):
             moe.moe_grouped_ffn_packed_scheduled(x, offs, ex, wgu, wd, 0, 0, 0,
                                                  moe.FfnSchedule(*bad), h, y, ws)
+
+
+def test_ffn_leaves_its_counters_clear_for_the_next_call():
+    """The grouped FFN runs with no memset before it: its per-segment
+    readiness counters (workspace bytes [256, 256 + 4*S)) and its
+    finished-CTA counter (status-block word 16) must be zero on entry, and
+    the last CTA of each launch clears them.  Calls of different segment
+    counts and tile counts, single-SM and SM-pair schedules, one after
+    another on one workspace, each leave them zero and give the same bits
+    as the same call on a fresh workspace."""
+    from grouped_ffn_gb300 import moe
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(17)
+    H, I, E = 512, 256, 12
+    wgu = (torch.randn(E, 2 * I, H, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    wd = (torch.randn(E, H, I, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    pgu, pd = torch.empty_like(wgu), torch.empty_like(wd)
+    moe.moe_pack_expert_weights(wgu, wd, pgu, pd)
+    ws = moe.new_workspace(4096, 2, 1024, device=dev)
+
+    def run(counts, sched, ws_):
+        offs = torch.zeros(len(counts) + 1, dtype=torch.int32)
+        offs[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int32), 0)
+        n = int(offs[-1])
+        x = (torch.randn(n, H, generator=g, device=dev)).to(torch.bfloat16)
+        ex = torch.tensor([i % E for i in range(len(counts))], dtype=torch.int32, device=dev)
+        h = torch.empty(n, I, dtype=torch.bfloat16, device=dev)
+        y = torch.empty(n, H, dtype=torch.bfloat16, device=dev)
+        moe.moe_grouped_ffn_packed_scheduled(x, offs.to(dev), ex, pgu, pd, 0, 0, 0, sched, h, y, ws_)
+        torch.cuda.synchronize()
+        moe.moe_check_device_status(ws_)
+        fresh = moe.new_workspace(4096, 2, 1024, device=dev)
+        y2 = torch.empty_like(y)
+        moe.moe_grouped_ffn_packed_scheduled(x, offs.to(dev), ex, pgu, pd, 0, 0, 0, sched, h, y2,
+                                             fresh)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y2)
+        words = ws_[:256 + 4 * 1024].view(torch.int32).cpu()
+        assert int(words[16]) == 0, "finished-CTA counter left set"
+        assert int(words[64:64 + len(counts)].abs().sum()) == 0, "readiness counters left set"
+
+    rng = np.random.default_rng(3)
+    for sched in (None, moe.FfnSchedule(), moe.FfnSchedule(cta_pairs=1), moe.FfnSchedule(7, 0, 0, 0)):
+        for n_seg in (1, 5, 40, 300):
+            counts = [int(c) for c in rng.integers(0, 300, size=n_seg)]
+            counts[0] = max(counts[0], 1)
+            run(counts, sched if sched is not None else moe.FfnSchedule(), ws)
