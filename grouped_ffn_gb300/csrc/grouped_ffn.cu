@@ -37,8 +37,12 @@
 // CTAs running side by side share B tiles (weights) and A rows in L2; a
 // weight tile that only one m-block reads is loaded with an L2 evict_first
 // policy, one that several m-blocks read with evict_last.
-// All waits are bounded (%globaltimer); on expiry the CTA records
-// MOE_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, frees TMEM, exits.
+// The launch follows the permute with programmatic dependent launch (the
+// set-up above overlaps its tail; griddepcontrol.wait precedes every read),
+// and the per-segment counters are cleared by the last CTA to finish, so no
+// memset sits in between.  All waits are bounded (%globaltimer); on expiry
+// the CTA records MOE_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs,
+// frees TMEM, exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
