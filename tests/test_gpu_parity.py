@@ -710,8 +710,9 @@ def _full_layer(w, dev="cuda"):
 @pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "group_limited", "replica"])
 def test_full_layer_sampled(name):
     """Full-size layer in the configuration the benchmark times: every
-    integer output bit-exact, FFN rows and combined tokens sampled against
-    the oracle, and the combine bit-exact given the GPU's expert outputs."""
+    integer output bit-exact, FFN rows and combined tokens against the
+    oracle (all of them on tiny and decode, sampled on the larger layers),
+    and the combine bit-exact given the GPU's expert outputs."""
     w = wl.WORKLOADS[name]
     pl, logits, x, wgu, wd, sgu, sd, layer, y = _full_layer(w)
     A = w.A
@@ -723,8 +724,9 @@ def test_full_layer_sampled(name):
     assert np.array_equal(layer.dest_row[:A].cpu().numpy(), lay["dest_row"])
     assert np.array_equal(layer.src_assign[:A].cpu().numpy(), lay["src_assign"])
     rng = np.random.default_rng(w.index)
-    # sampled rows of the grouped FFN (x_perm -> h, y_perm)
-    rows = _sample_rows(lay["seg_offsets"], rng)
+    # rows of the grouped FFN (x_perm -> h, y_perm): all of them on the small
+    # layers (tiny, decode), sampled on the large ones
+    rows = np.arange(A) if A <= 256 else _sample_rows(lay["seg_offsets"], rng)
     xp_rows = f64(layer.x_perm[torch.from_numpy(rows).cuda()])
     lazy_gu, lazy_d = _LazyExperts(wgu), _LazyExperts(wd)
     full_x = np.zeros((int(rows.max()) + 1, w.H))
@@ -742,7 +744,8 @@ def test_full_layer_sampled(name):
                                  layer.topk_w[: w.T].cpu().numpy(), shared_bits)
     assert np.array_equal(bits(y), ref_y)
     # whole layer on sampled tokens, from the definition
-    toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, size=min(12, w.T), replace=False)]))
+    toks = (np.arange(w.T) if w.T <= 64 else
+            np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, size=12, replace=False)])))
     cfg = dict(score_fn=w.score_fn, k=w.k, n_groups=w.n_groups, topk_groups=w.topk_groups,
                group_topn=w.group_topn)
     shared = None if sgu is None else (bits(sgu[0]), bits(sd[0]))
