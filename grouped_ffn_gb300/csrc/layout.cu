@@ -630,7 +630,7 @@ struct RefineArgs {
 
 // Shared memory (int32 words) of route_refine_kernel.
 inline size_t refine_smem_words(int E, int S, int kmax) {
-  return 2 * (size_t)E + 1 + 4 * (size_t)S + kRefineThreads + 16 +
+  return 2 * (size_t)E + 1 + 5 * (size_t)S + kRefineThreads + 16 +
          2 * (size_t)kRefineThreads * kmax;
 }
 
@@ -873,6 +873,8 @@ __global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs
   // [kRefineThreads * KMAX] each: the chunk's open tokens' expert ids and slots
   int32_t *stage_e = reinterpret_cast<int32_t *>(nmask + r.E);
   int32_t *stage_s = stage_e + kRefineThreads * KMAX;
+  // [S] a round's takers of each copy, one bit per lane of warp 0
+  uint32_t *takers = reinterpret_cast<uint32_t *>(stage_s + kRefineThreads * KMAX);
   int32_t *misc = list + kRefineThreads;    // [1] pairs, [2] saved, [4..11] per-warp counts
 
   const int i = blockIdx.x;  // source rank
@@ -886,6 +888,7 @@ __global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs
     const int rk = r.slot_rank[s];
     slot_node[s] = (rk >= 0 && rk < r.R) ? rk / r.rpn : -1;
     left[s] = use[s] = 0;
+    takers[s] = 0u;
   }
   if (tid < 16) misc[tid] = 0;
   __syncthreads();
@@ -1026,7 +1029,51 @@ __global__ void __launch_bounds__(kRefineThreads) route_refine_kernel(RefineArgs
         // the prefix before itself elsewhere.
         int stop = n_here;
         bool emptied = false;
-        for (int l = 0; l < n_here; ++l) {
+        const bool lead_repeats = __shfl_sync(0xffffffffu, repeats ? 1 : 0, 0) != 0;
+        if (!lead_repeats) {
+          // All lanes at once: each marks its takes in the copies' lane
+          // masks; a take empties its copy when the takers up to and
+          // including this lane (one take per lane: no repeated ids here)
+          // reach the copy's count.  The first such lane, or the first lane
+          // with repeated ids (which stops before itself), ends the prefix:
+          // the same prefix as taking the lanes one by one.
+          if (mine && !repeats) {
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+              if ((open >> j) & 1u) atomicOr(&takers[cur_s[j]], 1u << lane);
+          }
+          __syncwarp();
+          int flag = 0;
+          if (mine) {
+            if (repeats) {
+              flag = 2;
+            } else {
+              const uint32_t upto = lane == 31 ? 0xffffffffu : (2u << lane) - 1u;
+#pragma unroll
+              for (int j = 0; j < KMAX; ++j)
+                if (((open >> j) & 1u) &&
+                    __popc(takers[cur_s[j]] & upto) >= left[cur_s[j]])
+                  flag = 1;
+            }
+          }
+          const uint32_t b1 = __ballot_sync(0xffffffffu, flag == 1);
+          const uint32_t b2 = __ballot_sync(0xffffffffu, flag == 2);
+          const int f1 = b1 ? __ffs(b1) - 1 : 32, f2 = b2 ? __ffs(b2) - 1 : 32;
+          if (f2 < f1) {
+            stop = f2;
+          } else if (f1 < 32) {
+            stop = f1 + 1;
+            emptied = true;
+          }
+          __syncwarp();
+          if (mine && !repeats) {
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+              if ((open >> j) & 1u) takers[cur_s[j]] = 0u;
+          }
+          __syncwarp();
+        }
+        for (int l = 0; lead_repeats && l < n_here; ++l) {
           int flag = 0;  // 1: empties a copy (kept, then stop); 2: stop before it
           if (lane == l) {
             if (repeats && l > 0) {
@@ -1456,7 +1503,7 @@ extern "C" moe_status moe_route_refine(const int32_t *topk_ids, int64_t T, int32
       static_cast<char *>(ws) + route_ws_bytes(T, k, pl->n_experts, pl->n_slots, pl->n_ranks));
   r.messages = messages;
   r.status = moe_host::status_ptr(ws);
-  // shared memory: at most 2 * 4096 + 1 + 4 * 1024 + 272 + 2 * 256 * 32 words (113 KiB)
+  // shared memory: at most 2 * 4096 + 1 + 5 * 1024 + 272 + 2 * 256 * 32 words (117 KiB)
   const int kmax = k <= 4 ? 4 : k <= 8 ? 8 : k <= 16 ? 16 : 32;
   const size_t smem = refine_smem_words(r.E, r.S, kmax) * sizeof(int32_t);
   auto kern = kmax == 4 ? route_refine_kernel<4>
